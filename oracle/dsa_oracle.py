@@ -1,0 +1,343 @@
+"""Plain fp64 CPU oracle for the DSA prefill on context-parallel (CP) views.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py`` (its ``cpu_baseline`` leg and ``--impl reference`` arm) may
+import this module.  The CUDA product path never imports it, and it imports
+nothing from the product path: the two share no code, tables or helpers.
+
+It is deliberately slow and obvious: Python loops over requests and rows,
+numpy fp64 matmul / exp / sort as the only library steps, no blocking, no
+fusion, no reordering beyond what each definition states.
+
+Pages it follows (cited per function by title and section):
+
+* [xLLM]   "feat: DeepSeek-V4 DSA context-parallel on NPU" (xLLM pull request
+           1997): sections "单层前向数据流" (per-layer data flow), "代码实现 /
+           2. CP 本地元数据" (build_cp_local_metadata), "8. 单测" (unit tests).
+* [blog]   "[DeepSeek v3.2] 上下文并行详解": sections "2.B 核心切分逻辑"
+           (round-robin split), "4. 一些细节 / 第一部分" (in-seq-split
+           example), "第三部分 KV Cache 的流动" (T0..T7 round-robin data flow,
+           gather + rerange).
+* [sglang] "NSA Prefill CP 中两次 All-Gather 的作用说明": section
+           "第一次 All-Gather" (KV / index key rebuilt in logical order).
+
+Method definitions the pages name but do not write out (DeepSeek Sparse
+Attention, named in [xLLM] "背景"): the lightning-indexer score
+I[t,s] = sum_j w[t,j] * ReLU(q_I[t,j] . k_I[s]), a causal top-k over s <= t
+with ties to the lower index, and MLA sparse attention of every query head
+over the selected rows of the shared latent KV (first Dv columns are the
+value), with an optional per-head sink logit.
+
+Readings taken where the pages are silent or ambiguous (each listed in the
+design notes):
+  R1  split granularity is the flat token stream, not per request ([xLLM] 2).
+  R2  in-seq-split is contiguous ([blog] 4 第一部分); padding sits at the end.
+  R3  round-robin indexes the global flat token ([blog] 2.B).
+  R4  local_seq_lens is the KV extent visible to the rank's queries of that
+      request, i.e. last local in-request position + 1 ([xLLM] 单层前向数据流
+      "右对齐"); local_kv_start_loc is its exclusive cumsum.
+  R5  requests with no local row are dropped from the local batch.
+  R6  top-k ties go to the lower index; -0.0 equals +0.0; rows with p+1 <= k
+      select every s <= p and pad with -1; the result is a set (returned in
+      ascending order).
+  R7  the sink is a logit already in scaled units that adds exp(sink - m) to
+      the softmax denominator only; absent means no term.
+  R8  KV rows stay in full flat order; request b's key s is flat row qs_b + s.
+  R9  a prefix (seq_len != query length, i.e. chunked prefill) is rejected.
+
+parity pins: every function here is pinned by tests/test_oracle_pins.py
+against worked examples from the pages (tests/golden/), closed forms,
+invariants, brute force on tiny inputs and independent library routines.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+IN_SEQ_SPLIT = 0
+ROUND_ROBIN = 1
+
+
+# --------------------------------------------------------------------------
+# CP geometry: which flat rows a rank owns
+# --------------------------------------------------------------------------
+
+def padded_geometry(num_tokens: int, cp_size: int) -> tuple[int, int]:
+    """(num_tokens_pad, tokens_per_rank).
+
+    [xLLM] 2 (build_cp_local_metadata): the token count is padded up to a
+    multiple of cp_size and every rank holds tokens_per_rank = pad / cp_size
+    rows.
+    """
+    if cp_size < 1:
+        raise ValueError("cp_size must be >= 1")
+    tokens_per_rank = -(-num_tokens // cp_size)  # ceil
+    return tokens_per_rank * cp_size, tokens_per_rank
+
+
+def local_rows(num_tokens: int, cp_size: int, cp_rank: int, mode: int) -> np.ndarray:
+    """Flat token index held by each local slot of rank ``cp_rank``; -1 = pad.
+
+    in-seq-split: [blog] 4 第一部分 -- rank k holds a contiguous chunk
+      (8000 tokens on 8 ranks: rank k gets 1000k .. 1000k+999); [xLLM] 2 --
+      the flattened stream is cut evenly, padding at the end (R1, R2).
+    round-robin: [blog] 2.B -- rank r holds arange(r, tokens, cp_size), i.e.
+      token g goes to rank g % cp_size, slot g // cp_size (R3).
+    """
+    if not 0 <= cp_rank < cp_size:
+        raise ValueError("cp_rank out of range")
+    _, tpr = padded_geometry(num_tokens, cp_size)
+    rows = np.full(tpr, -1, dtype=np.int64)
+    for i in range(tpr):
+        if mode == IN_SEQ_SPLIT:
+            g = cp_rank * tpr + i
+        elif mode == ROUND_ROBIN:
+            g = cp_rank + i * cp_size
+        else:
+            raise ValueError("unknown mode")
+        if g < num_tokens:
+            rows[i] = g
+    return rows
+
+
+# --------------------------------------------------------------------------
+# build_cp_local_metadata
+# --------------------------------------------------------------------------
+
+def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, mode: int) -> dict:
+    """Local view metadata of one CP rank.
+
+    [xLLM] 2: pad to a multiple of cp_size, tokens_per_rank, local_start /
+    local_end; intersect the global cu-seqlens with the rank's rows to get
+    local_query_start_loc and local_seq_lens; local_kv_start_loc is the
+    right-aligned cumsum of local_seq_lens; cp_size == 1 is the identity.
+    [xLLM] 单层前向数据流 (4): the attention call takes cu_seqlens_q =
+    local_query_start_loc, cu_seqlens_ori_kv = local_kv_start_loc and
+    seqused_kv = local_seq_lens; the local queries see the KV extent that
+    ends at their last position (right-aligned) (R4).
+    [xLLM] 5: batch_size / max_seqlen_q are replaced by the local geometry.
+
+    Extras (R8): local_req_id (global request index), local_req_kv_base (flat
+    row of the request's first token) and local_token_pos (flat row of every
+    local slot, -1 for pad).
+    """
+    qsl = [int(x) for x in query_start_loc]
+    sl = [int(x) for x in seq_lens]
+    B = len(sl)
+    if len(qsl) != B + 1 or qsl[0] != 0:
+        raise ValueError("query_start_loc must have B+1 entries starting at 0")
+    for b in range(B):
+        if qsl[b + 1] - qsl[b] != sl[b]:
+            raise ValueError("seq_lens != query lengths (prefix KV) is not supported (R9)")
+    T = qsl[B]
+    pad, tpr = padded_geometry(T, cp_size)
+    rows = local_rows(T, cp_size, cp_rank, mode)
+
+    if mode == IN_SEQ_SPLIT:
+        local_start = min(cp_rank * tpr, T)
+        local_end = min((cp_rank + 1) * tpr, T)
+    else:
+        # the strided range {local_start + i*cp_size < local_end}
+        local_start = min(cp_rank, T)
+        local_end = T
+
+    q_lens, kv_lens, req_id, kv_base = [], [], [], []
+    for b in range(B):
+        mine = [int(g) for g in rows if g >= 0 and qsl[b] <= g < qsl[b + 1]]
+        if not mine:
+            continue  # R5
+        q_lens.append(len(mine))
+        kv_lens.append(max(mine) - qsl[b] + 1)  # R4: last local position + 1
+        req_id.append(b)
+        kv_base.append(qsl[b])
+
+    lqs = [0]
+    for n in q_lens:
+        lqs.append(lqs[-1] + n)
+    lkv = [0]
+    for n in kv_lens:
+        lkv.append(lkv[-1] + n)
+
+    return {
+        "num_tokens_pad": pad,
+        "tokens_per_rank": tpr,
+        "local_start": local_start,
+        "local_end": local_end,
+        "local_batch": len(q_lens),
+        "local_num_tokens": lqs[-1],
+        "local_max_seqlen_q": max(q_lens) if q_lens else 0,
+        "local_max_seqlen_kv": max(kv_lens) if kv_lens else 0,
+        "local_query_start_loc": lqs,
+        "local_seq_lens": kv_lens,
+        "local_kv_start_loc": lkv,
+        "local_req_id": req_id,
+        "local_req_kv_base": kv_base,
+        "local_token_pos": [int(g) for g in rows],
+    }
+
+
+# --------------------------------------------------------------------------
+# split and rerange
+# --------------------------------------------------------------------------
+
+def split(x: np.ndarray, cp_size: int, mode: int) -> np.ndarray:
+    """Rank-major local layout [cp_size][tokens_per_rank][row...], pad rows zero.
+
+    [blog] 2.B / 第三部分 step 1: each rank gathers its own rows (T0,T4 on
+    rank 0 of 4); [blog] 第三部分 step B: concatenated by rank this is the
+    all-gathered order T0,T4,T1,T5,...; [xLLM] 单层前向数据流 (6): pad to
+    tokens_per_rank.
+    """
+    T = x.shape[0]
+    _, tpr = padded_geometry(T, cp_size)
+    out = np.zeros((cp_size, tpr) + x.shape[1:], dtype=x.dtype)
+    for r in range(cp_size):
+        for i, g in enumerate(local_rows(T, cp_size, r, mode)):
+            if g >= 0:
+                out[r, i] = x[g]
+    return out
+
+
+def rerange(y: np.ndarray, num_tokens: int, cp_size: int, mode: int) -> np.ndarray:
+    """Inverse of :func:`split`: rank-major rows back to logical token order.
+
+    [blog] 第三部分 step B and [sglang] 第一次 All-Gather: after the
+    all-gather the rows are in rank order and are re-arranged into the
+    original flat order T0, T1, T2, ...; pad rows are dropped.
+    """
+    out = np.zeros((num_tokens,) + y.shape[2:], dtype=y.dtype)
+    for r in range(cp_size):
+        for i, g in enumerate(local_rows(num_tokens, cp_size, r, mode)):
+            if g >= 0:
+                out[g] = y[r, i]
+    return out
+
+
+# --------------------------------------------------------------------------
+# lightning indexer, top-k, sparse attention (one query row at a time)
+# --------------------------------------------------------------------------
+
+def indexer_scores(q_idx_row: np.ndarray, w_row: np.ndarray, k_idx_keys: np.ndarray) -> np.ndarray:
+    """I[s] = sum_j w[j] * max(0, q_I[j] . k_I[s]) for every key row s given.
+
+    q_idx_row [HI, DI], w_row [HI], k_idx_keys [n, DI] -> fp64 [n].  The
+    indexer query and weights are the rank's local rows, the index keys are
+    the full-token keys ([xLLM] 单层前向数据流 (2)(3), 4. Indexer full/local).
+    """
+    q = np.asarray(q_idx_row, dtype=np.float64)
+    w = np.asarray(w_row, dtype=np.float64)
+    k = np.asarray(k_idx_keys, dtype=np.float64)
+    dots = q @ k.T                    # [HI, n]: q_I[j] . k_I[s]
+    return w @ np.maximum(dots, 0.0)  # sum over heads j of w[j] * ReLU(.)
+
+
+def topk_positions(scores: np.ndarray, k: int) -> np.ndarray:
+    """The k positions with the largest scores, ties to the lower position.
+
+    R6: a row with n <= k keys selects all of them (never collapses to
+    position 0, cf. [xLLM] 5 "top-k 塌缩到 position 0").  Otherwise the k-th
+    largest value is the threshold; every position above it is selected and
+    the remaining places go to the lowest positions equal to it.  numpy's
+    comparison treats -0.0 == +0.0.  Returned ascending.
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    if np.isnan(s).any():
+        raise ValueError("NaN score")
+    n = s.shape[0]
+    if n <= k:
+        return np.arange(n, dtype=np.int64)
+    threshold = np.sort(s)[n - k]       # k-th largest
+    above = np.nonzero(s > threshold)[0]
+    equal = np.nonzero(s == threshold)[0]
+    chosen = np.concatenate([above, equal[: k - above.shape[0]]])
+    return np.sort(chosen)
+
+
+def sparse_attention(q_row: np.ndarray, kv_sel: np.ndarray, scale: float, Dv: int, sink=None) -> np.ndarray:
+    """MLA attention of every head of one query over the selected latent rows.
+
+    q_row [H, D], kv_sel [n, D] (key = the full D-wide latent row, value =
+    its first Dv columns), sink [H] or None -> fp64 [H, Dv]:
+      l[h, j] = scale * q[h] . kv[j]
+      m[h]    = max(max_j l[h, j], sink[h])
+      o[h]    = sum_j exp(l[h, j] - m[h]) kv[j, :Dv] / (sum_j exp(l[h, j] - m[h]) + exp(sink[h] - m[h]))
+    with the sink terms present only when a sink is given (R7).
+    """
+    q = np.asarray(q_row, dtype=np.float64)
+    kv = np.asarray(kv_sel, dtype=np.float64)
+    logits = scale * (q @ kv.T)                       # [H, n]
+    m = logits.max(axis=1)
+    if sink is not None:
+        sk = np.asarray(sink, dtype=np.float64)
+        m = np.maximum(m, sk)
+    e = np.exp(logits - m[:, None])
+    z = e.sum(axis=1)
+    if sink is not None:
+        z = z + np.exp(sk - m)
+    return (e @ kv[:, :Dv]) / z[:, None]
+
+
+def request_of_slot(md: dict, slot: int) -> int:
+    """Local request index j with local_query_start_loc[j] <= slot < [j+1]."""
+    lqs = md["local_query_start_loc"]
+    for j in range(md["local_batch"]):
+        if lqs[j] <= slot < lqs[j + 1]:
+            return j
+    return -1
+
+
+def view_row(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int, scale: float,
+             Dv: int, sink=None):
+    """Indexer -> top-k -> sparse attention for one local slot of one view.
+
+    Returns (selected global KV rows ascending [<=topk] int64, scores fp64
+    [p+1], output fp64 [H, Dv]); (None, None, zeros) for a pad slot.
+    The local query of flat row g, request b at position p = g - qs_b, sees
+    keys qs_b .. qs_b + p (causal, same request; R8).
+    """
+    g = md["local_token_pos"][slot]
+    H = np.asarray(q_loc[slot]).shape[0]
+    if g < 0:
+        return None, None, np.zeros((H, Dv))
+    j = request_of_slot(md, slot)
+    base = md["local_req_kv_base"][j]
+    p = g - base
+    keys = np.arange(base, base + p + 1)
+    scores = indexer_scores(q_idx_loc[slot], w_loc[slot], np.asarray(k_idx)[keys])
+    sel = base + topk_positions(scores, topk)
+    out = sparse_attention(q_loc[slot], np.asarray(kv)[sel], scale, Dv, sink)
+    return sel, scores, out
+
+
+def prefill_view(md: dict, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int, scale: float, Dv: int,
+                 sink=None, slots=None):
+    """One CP view: (topk_idx [tpr, topk] int64 global rows, -1 pad;
+    out [tpr, H, Dv] fp64, pad rows 0).  ``slots`` restricts the work to a
+    subset of local slots (others stay -1 / 0)."""
+    tpr = md["tokens_per_rank"]
+    H = np.asarray(q_loc).shape[1]
+    idx = np.full((tpr, topk), -1, dtype=np.int64)
+    out = np.zeros((tpr, H, Dv))
+    for i in (range(tpr) if slots is None else slots):
+        sel, _, o = view_row(md, int(i), q_loc, q_idx_loc, w_loc, kv, k_idx, topk, scale, Dv, sink)
+        if sel is not None:
+            idx[i, : sel.shape[0]] = sel
+            out[i] = o
+    return idx, out
+
+
+def prefill(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mode: int, topk: int,
+            scale: float, Dv: int, sink=None):
+    """The whole prefill through cp_size views: split the local tensors, run
+    every view with full KV and index keys, rerange the outputs to flat order
+    ([xLLM] 单层前向数据流: q local, KV full).  Returns out [T, H, Dv] fp64."""
+    q = np.asarray(q, dtype=np.float64)
+    q_idx = np.asarray(q_idx, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T = q.shape[0]
+    qs, qis, ws = split(q, cp_size, mode), split(q_idx, cp_size, mode), split(w, cp_size, mode)
+    _, tpr = padded_geometry(T, cp_size)
+    outs = np.zeros((cp_size, tpr, q.shape[1], Dv))
+    for r in range(cp_size):
+        md = build_local_metadata(query_start_loc, seq_lens, cp_size, r, mode)
+        _, outs[r] = prefill_view(md, qs[r], qis[r], ws[r], kv, k_idx, topk, scale, Dv, sink)
+    return rerange(outs, T, cp_size, mode)

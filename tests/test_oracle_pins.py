@@ -1,0 +1,299 @@
+"""Pins for the fp64 oracle, against things other than the oracle itself:
+worked examples printed on the pages (tests/golden/), hand-derived cases,
+closed forms, invariants the pages state, and independent library routines
+(torch's scaled_dot_product_attention, Python's stable ``sorted``).
+
+Each pin is chosen so that a plausible slip in the oracle (an off-by-one in
+the causal extent, a dropped ReLU, a transposed operand, a wrong tie rule, a
+sink added to the numerator, a wrong rank-row mapping) fails at least one test.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import read_golden, read_golden_lines
+from oracle import dsa_oracle as O
+from workloads import IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, draw_inputs
+
+MODES = (IN_SEQ_SPLIT, ROUND_ROBIN)
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy() if isinstance(t, torch.Tensor) else np.asarray(t, dtype=np.float64)
+
+
+# ---------------------------------------------------------------- split geometry
+
+def test_round_robin_worked_example():
+    g = read_golden("round_robin_cp4_t8.txt")
+    T, cp = g["num_tokens"][0], g["cp_size"][0]
+    for r in range(cp):
+        assert list(O.local_rows(T, cp, r, ROUND_ROBIN)) == g[f"rank{r}"]
+    x = np.arange(T)
+    gathered = O.split(x, cp, ROUND_ROBIN).reshape(-1)
+    assert list(gathered) == g["gathered_order"]
+    assert list(O.rerange(gathered.reshape(cp, -1), T, cp, ROUND_ROBIN)) == g["reranged_order"]
+
+
+def test_in_seq_worked_example():
+    g = read_golden("in_seq_cp8_t8000.txt")
+    T, cp = g["num_tokens"][0], g["cp_size"][0]
+    for r in range(cp):
+        rows = O.local_rows(T, cp, r, IN_SEQ_SPLIT)
+        assert rows[0] == g["first"][r] and rows[-1] == g["last"][r]
+        assert np.all(np.diff(rows) == 1)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T,cp", [(1, 1), (7, 2), (12, 3), (13, 4), (5, 16), (100, 8), (257, 2)])
+def test_split_rerange_identity_and_padding(T, cp, mode):
+    x = np.arange(T * 3, dtype=np.int64).reshape(T, 3) + 1  # no zero rows
+    y = O.split(x, cp, mode)
+    pad, tpr = O.padded_geometry(T, cp)
+    assert y.shape == (cp, tpr, 3) and pad == tpr * cp and pad - T < cp
+    assert np.array_equal(O.rerange(y, T, cp, mode), x)
+    # every real row appears exactly once, pad rows are zero
+    flat = y.reshape(-1, 3)
+    nonzero = flat[np.any(flat != 0, axis=1)]
+    assert nonzero.shape[0] == T and np.all(flat[np.all(flat == 0, axis=1)] == 0)
+
+
+@pytest.mark.parametrize("T,cp", [(8, 4), (11805, 4), (65536, 8), (5, 16), (184265, 16)])
+def test_round_robin_counts_differ_by_at_most_one(T, cp):
+    counts = [int(np.sum(O.local_rows(T, cp, r, ROUND_ROBIN) >= 0)) for r in range(cp)]
+    assert sum(counts) == T and max(counts) - min(counts) <= 1
+
+
+# ---------------------------------------------------------------- metadata
+
+_CASES = {"A": [5, 3, 4], "B": [3, 4], "C": [5, 1]}
+_CP = {"A": 3, "B": 2, "C": 4}
+
+
+def _qsl(lengths):
+    return [0] + list(np.cumsum(lengths))
+
+
+def _ints(s):
+    s = s.strip()
+    return [] if s == "-" else [int(x) for x in s.split()]
+
+
+def test_metadata_hand_cases():
+    for line in read_golden_lines("metadata_hand_cases.txt"):
+        head, lqs, kvl, lkv, rid, base, pos = line.split("|")
+        case, mode_s, rank = head.split()
+        lengths = _CASES[case]
+        mode = IN_SEQ_SPLIT if mode_s == "inseq" else ROUND_ROBIN
+        md = O.build_local_metadata(_qsl(lengths), lengths, _CP[case], int(rank), mode)
+        assert md["local_query_start_loc"] == _ints(lqs), line
+        assert md["local_seq_lens"] == _ints(kvl), line
+        assert md["local_kv_start_loc"] == _ints(lkv), line
+        assert md["local_req_id"] == _ints(rid), line
+        assert md["local_req_kv_base"] == _ints(base), line
+        assert md["local_token_pos"] == _ints(pos), line
+        assert md["local_batch"] == len(_ints(kvl))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("lengths,cp", [([8000, 800, 5, 3000], 4), ([5, 3, 4], 3), ([1, 1, 1], 8),
+                                        ([256], 2), ([17, 1, 30, 2], 5)])
+def test_metadata_partitions_all_query_tokens(lengths, cp, mode):
+    qsl = _qsl(lengths)
+    T = qsl[-1]
+    owner = np.zeros(T, dtype=np.int64)
+    total = 0
+    for r in range(cp):
+        md = O.build_local_metadata(qsl, lengths, cp, r, mode)
+        total += md["local_num_tokens"]
+        for g in md["local_token_pos"]:
+            if g >= 0:
+                owner[g] += 1
+        # local_kv_start_loc is the exclusive cumsum of local_seq_lens
+        assert md["local_kv_start_loc"] == [0] + list(np.cumsum(md["local_seq_lens"]))
+        # every local query's position is inside its request's visible extent
+        for j in range(md["local_batch"]):
+            for slot in range(md["local_query_start_loc"][j], md["local_query_start_loc"][j + 1]):
+                p = md["local_token_pos"][slot] - md["local_req_kv_base"][j]
+                assert 0 <= p < md["local_seq_lens"][j]
+    assert total == T and np.all(owner == 1)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_metadata_cp1_is_identity(mode):
+    lengths = [8000, 800, 5, 3000]
+    qsl = _qsl(lengths)
+    md = O.build_local_metadata(qsl, lengths, 1, 0, mode)
+    assert md["local_query_start_loc"] == qsl
+    assert md["local_kv_start_loc"] == qsl
+    assert md["local_seq_lens"] == lengths
+    assert md["local_token_pos"] == list(range(qsl[-1]))
+    assert md["tokens_per_rank"] == qsl[-1] == md["num_tokens_pad"]
+
+
+def test_metadata_in_seq_right_aligned_extent():
+    # the last in-seq rank sees the full KV stream of the last request; every
+    # other rank's extent ends at its own last local token
+    lengths = [8192]
+    for cp in (2, 4, 8):
+        for r in range(cp):
+            md = O.build_local_metadata([0, 8192], lengths, cp, r, IN_SEQ_SPLIT)
+            assert md["local_seq_lens"] == [8192 // cp * (r + 1)]
+            assert md["local_start"] == 8192 // cp * r and md["local_end"] == 8192 // cp * (r + 1)
+
+
+def test_metadata_rejects_prefix():
+    with pytest.raises(ValueError):
+        O.build_local_metadata([0, 4], [6], 2, 0, IN_SEQ_SPLIT)
+
+
+# ---------------------------------------------------------------- indexer
+
+def test_indexer_hand_example():
+    g = read_golden("indexer_hand_example.txt")
+    q = np.array(g["q_idx"], dtype=float).reshape(2, 2)
+    k = np.array(g["k_idx"], dtype=float).reshape(-1, 2)
+    s = O.indexer_scores(q, g["w"], k)
+    assert np.array_equal(s, np.array(g["scores"], dtype=float))
+    for kk in (2, 3, 4):
+        assert list(O.topk_positions(s, kk)) == g[f"top{kk}"]
+
+
+def test_indexer_closed_form_unit_queries():
+    # head j reads dim j only (q_I[j] = e_j); k_I[s, j] = (j + 1) * (s - 2j - 1)
+    # => I[s] = sum_j w[j] (j+1) max(0, s - 2j - 1): a ramp per head that turns on
+    # at s = 2j + 2.  A transposed q/k, a dropped ReLU or a wrong w index breaks it.
+    HI = DI = 4
+    n = 12
+    q = np.eye(HI, DI)
+    w = np.array([0.5, -1.0, 2.0, 0.25])
+    k = np.array([[(j + 1) * (s - 2 * j - 1) for j in range(DI)] for s in range(n)], dtype=float)
+    expect = np.array([sum(w[j] * (j + 1) * max(0, s - 2 * j - 1) for j in range(HI)) for s in range(n)])
+    assert np.array_equal(O.indexer_scores(q, w, k), expect)
+
+
+def test_indexer_relu_kills_negative_dots_and_w_scales():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((3, 8))
+    k = -np.abs(rng.standard_normal((10, 8)))
+    q = np.abs(q)                     # every dot q . k < 0 -> ReLU 0
+    assert np.all(O.indexer_scores(q, [1.0, 2.0, 3.0], k) == 0.0)
+    k2 = rng.standard_normal((10, 8))
+    w = rng.standard_normal(3)
+    s1 = O.indexer_scores(q, w, k2)
+    assert np.array_equal(O.indexer_scores(q, 2.0 * w, k2), 2.0 * s1)
+    assert np.array_equal(O.indexer_scores(q, -w, k2), -s1)
+
+
+# ---------------------------------------------------------------- top-k
+
+def test_topk_ties_and_short_rows():
+    assert list(O.topk_positions([5, 3, 3, 1, 3, 7], 3)) == [0, 1, 5]
+    assert list(O.topk_positions([2.0] * 10, 4)) == [0, 1, 2, 3]
+    assert list(O.topk_positions([-0.0, 0.0], 1)) == [0]
+    assert list(O.topk_positions([0.0, -0.0, -1.0], 1)) == [0]
+    assert list(O.topk_positions([1.0, 2.0, 3.0], 64)) == [0, 1, 2]   # p+1 <= k: all
+    assert list(O.topk_positions([9.0, 1.0], 2)) == [0, 1]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_equals_stable_sort(seed):
+    # library route: Python's stable sort by (score desc, position asc), take k
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 400))
+    k = int(rng.integers(1, 80))
+    s = rng.integers(-4, 5, n).astype(float)            # many ties
+    ref = sorted(sorted(range(n), key=lambda i: -s[i])[:k])
+    assert list(O.topk_positions(s, k)) == ref
+
+
+# ---------------------------------------------------------------- attention
+
+def _sdpa_causal(q, kv, Dv, scale, sink=None):
+    """torch fp64 scaled_dot_product_attention, causal, KV shared by all heads;
+    the sink is an extra key with logit sink[h] and a zero value."""
+    T, H, D = q.shape
+    qt = torch.from_numpy(q).permute(1, 0, 2)[None]                 # [1,H,T,D]
+    k = torch.from_numpy(kv)[None, None].expand(1, H, T, D)
+    v = torch.from_numpy(kv[:, :Dv])[None, None].expand(1, H, T, Dv)
+    mask = torch.full((T, T), -math.inf, dtype=torch.float64).triu(1)  # s > t masked
+    mask = mask[None, None].expand(1, H, T, T)
+    if sink is not None:
+        k = torch.cat([k, torch.zeros(1, H, 1, D, dtype=torch.float64)], dim=2)
+        v = torch.cat([v, torch.zeros(1, H, 1, Dv, dtype=torch.float64)], dim=2)
+        extra = torch.from_numpy(sink)[None, :, None, None].expand(1, H, T, 1)
+        mask = torch.cat([mask, extra], dim=3)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, k, v, attn_mask=mask, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("with_sink", [False, True])
+@pytest.mark.parametrize("mode", MODES)
+def test_attention_with_full_topk_is_dense_causal(mode, with_sink):
+    rng = np.random.default_rng(11)
+    T, H, D, Dv, HI, DI = 40, 3, 10, 6, 2, 4
+    q = rng.standard_normal((T, H, D))
+    kv = rng.standard_normal((T, D))
+    qi = rng.standard_normal((T, HI, DI))
+    ki = rng.standard_normal((T, DI))
+    w = rng.standard_normal((T, HI))
+    sink = rng.standard_normal(H) if with_sink else None
+    lengths = [17, 23]
+    qsl = _qsl(lengths)
+    out = O.prefill(q, kv, qi, ki, w, qsl, lengths, 3, mode, topk=64, scale=0.3, Dv=Dv, sink=sink)
+    for b, L in enumerate(lengths):
+        lo, hi = qsl[b], qsl[b + 1]
+        ref = _sdpa_causal(q[lo:hi], kv[lo:hi], Dv, 0.3, sink)
+        assert np.allclose(out[lo:hi], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(3)
+    H, D, Dv = 4, 8, 5
+    kv = rng.standard_normal((6, D))
+    q = rng.standard_normal((H, D))
+    # one selected row: the output is that row's value, whatever q is
+    assert np.allclose(O.sparse_attention(q, kv[2:3], 0.7, Dv), np.tile(kv[2, :Dv], (H, 1)), atol=1e-15)
+    # q = 0: equal logits -> the mean of the selected values
+    assert np.allclose(O.sparse_attention(np.zeros((H, D)), kv, 0.7, Dv), np.tile(kv[:, :Dv].mean(0), (H, 1)))
+    # q = 0, sink = 0: the sink takes one share of n+1 in the denominator only
+    assert np.allclose(O.sparse_attention(np.zeros((H, D)), kv, 0.7, Dv, np.zeros(H)),
+                       np.tile(kv[:, :Dv].sum(0) / 7.0, (H, 1)))
+    # sink -> -inf is no sink; permuting the selected rows changes nothing
+    base = O.sparse_attention(q, kv, 0.7, Dv)
+    assert np.allclose(O.sparse_attention(q, kv, 0.7, Dv, np.full(H, -np.inf)), base, atol=1e-15)
+    assert np.allclose(O.sparse_attention(q, kv[::-1], 0.7, Dv), base, atol=1e-14)
+    # scale equivariance: (2q, scale/2) == (q, scale)
+    assert np.allclose(O.sparse_attention(2 * q, kv, 0.35, Dv), base, atol=1e-14)
+    # without a sink the output is a convex combination of the values
+    assert np.all(base <= kv[:, :Dv].max(0) + 1e-12) and np.all(base >= kv[:, :Dv].min(0) - 1e-12)
+
+
+# ---------------------------------------------------------------- CP views
+
+@pytest.mark.parametrize("wl", [TINY, TINY_INT], ids=lambda w: w.name)
+@pytest.mark.parametrize("mode", MODES)
+def test_cp_views_rerange_to_single_view(wl, mode):
+    x = draw_inputs(wl)
+    args = [_f64(x[k]) for k in ("q", "kv", "q_idx", "k_idx", "w")]
+    qsl, sl = wl.query_start_loc(), wl.seq_lens()
+    kw = dict(topk=wl.topk, scale=wl.scale, Dv=wl.Dv, sink=None if x["sink"] is None else _f64(x["sink"]))
+    single = O.prefill(*args, qsl, sl, 1, mode, **kw)
+    views = O.prefill(*args, qsl, sl, wl.cp_size, mode, **kw)
+    assert np.array_equal(single, views)
+
+
+def test_short_rows_select_everything():
+    # rows with p + 1 <= topk select every causal key, in order, padded with -1
+    wl = TINY
+    x = draw_inputs(wl)
+    md = O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), 1, 0, IN_SEQ_SPLIT)
+    idx, _ = O.prefill_view(md, _f64(x["q"]), _f64(x["q_idx"]), _f64(x["w"]), _f64(x["kv"]),
+                            _f64(x["k_idx"]), wl.topk, wl.scale, wl.Dv, slots=[0, 5, 63, 64, 200])
+    assert list(idx[0]) == [0] + [-1] * 63
+    assert list(idx[5][:6]) == list(range(6)) and np.all(idx[5][6:] == -1)
+    assert list(idx[63]) == list(range(64))
+    assert np.all(idx[64] >= 0) and len(set(idx[64])) == 64 and idx[64].max() <= 64
+    assert np.all(idx[200] >= 0) and np.all(np.diff(idx[200]) > 0) and idx[200].max() <= 200
