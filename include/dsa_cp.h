@@ -1,0 +1,257 @@
+/*
+ * dsa_cp.h -- C ABI of libdsa_cp.so: DeepSeek Sparse Attention (DSA) prefill
+ * on context-parallel (CP) local query views, for GB300 (sm_103a).
+ *
+ * The hot path per CP view: lightning-indexer scores of the view's local
+ * queries against the FULL index keys, a causal top-k per query, and MLA
+ * sparse attention of every query head over the selected rows of the FULL
+ * shared latent KV ("q local, KV full"); around it the CP geometry: the
+ * local metadata of a rank, and the split / rerange permutations.
+ *
+ * Sources (pages, cited by title and section):
+ *   [xLLM]   "feat: DeepSeek-V4 DSA context-parallel on NPU" (xLLM PR 1997)
+ *   [blog]   "[DeepSeek v3.2] 上下文并行详解"
+ *   [sglang] "NSA Prefill CP 中两次 All-Gather 的作用说明"
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers unless marked "host".  The
+ *     caller owns and allocates every buffer; the library never allocates,
+ *     frees or synchronises (except dsa_poll_device_error, which syncs).
+ *   - Every call is asynchronous on the caller's CUDA stream (`stream`,
+ *     a cudaStream_t; NULL = the legacy default stream).
+ *   - Arguments are validated on the host before any launch; on an error
+ *     the call returns a status and nothing is written or launched.
+ *   - Device kernels never trap.  A bounds violation found on the device,
+ *     a metadata inconsistency, or a wait that ran past its limit (about
+ *     one second) sets a device error word and the kernel returns early;
+ *     dsa_poll_device_error reports it.
+ *   - bf16 tensors are row-major, contiguous, 16-byte aligned.
+ *   - Supported dimension sets (others return DSA_ERR_UNSUPPORTED):
+ *       DeepSeek-V3.2 shapes: H=128, D=576, Dv=512, HI=64, DI=128, topk=2048
+ *       tiny shapes:          H=8,   D=64,  Dv=48,  HI=4,  DI=32,  topk=64
+ */
+#ifndef DSA_CP_H
+#define DSA_CP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_CP_ABI_VERSION 1
+
+typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,    /* null pointer, rank out of range, bad mode  */
+  DSA_ERR_SHAPE = 2,          /* sizes inconsistent or out of range         */
+  DSA_ERR_UNSUPPORTED = 3,    /* dimension set not compiled                 */
+  DSA_ERR_WORKSPACE = 4,      /* workspace too small                        */
+  DSA_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed          */
+  DSA_ERR_DEVICE_TIMEOUT = 6, /* a device wait ran past its limit           */
+  DSA_ERR_DEVICE_BOUNDS = 7,  /* a device-side index was out of range       */
+  DSA_ERR_DEVICE_PREFIX = 8   /* metadata: seq_lens != query lengths        */
+} dsa_status;
+
+typedef enum { DSA_CP_IN_SEQ_SPLIT = 0, DSA_CP_ROUND_ROBIN = 1 } dsa_cp_mode;
+
+/* Indices into dsa_cp_local_metadata.scalars. */
+enum {
+  DSA_MD_NUM_TOKENS_PAD = 0,
+  DSA_MD_TOKENS_PER_RANK = 1,
+  DSA_MD_LOCAL_START = 2,
+  DSA_MD_LOCAL_END = 3,
+  DSA_MD_LOCAL_BATCH = 4,
+  DSA_MD_LOCAL_NUM_TOKENS = 5,
+  DSA_MD_LOCAL_MAX_SEQLEN_Q = 6,
+  DSA_MD_LOCAL_MAX_SEQLEN_KV = 7,
+  DSA_MD_NUM_SCALARS = 8
+};
+
+/*
+ * Local view of one CP rank ([xLLM] "代码实现 / 2. CP 本地元数据",
+ * DSACPMetadata, without the RoPE tables).  All members are device int32
+ * arrays owned by the caller; dsa_cp_metadata_bind carves them out of one
+ * buffer of dsa_cp_metadata_sizes() ints.  B = global batch size,
+ * tpr = tokens_per_rank.
+ *   scalars[8]                  see DSA_MD_*; in round-robin mode the local
+ *                               rows are {local_start + i*cp_size < local_end}
+ *   local_query_start_loc[B+1]  cu-seqlens of the local queries (first
+ *                               local_batch+1 entries valid)
+ *   local_seq_lens[B]           KV extent seen by the local queries of each
+ *                               local request = last local position + 1
+ *                               (right-aligned, [xLLM] 单层前向数据流 (4))
+ *   local_kv_start_loc[B+1]     exclusive cumsum of local_seq_lens
+ *   local_req_id[B]             global request index of each local request
+ *   local_req_kv_base[B]        flat row of that request's first token (KV
+ *                               and index keys stay in full flat order)
+ *   local_token_pos[tpr]        flat token row of every local slot, -1 = pad
+ * Requests with no local row are not in the local batch.
+ */
+typedef struct {
+  int32_t *scalars;
+  int32_t *local_query_start_loc;
+  int32_t *local_seq_lens;
+  int32_t *local_kv_start_loc;
+  int32_t *local_req_id;
+  int32_t *local_req_kv_base;
+  int32_t *local_token_pos;
+} dsa_cp_local_metadata;
+
+/* Host only.  num_tokens_pad = ceil(num_tokens / cp_size) * cp_size and
+ * tokens_per_rank = num_tokens_pad / cp_size ([xLLM] 2).  Outputs are host
+ * pointers.  Errors: DSA_ERR_INVALID_ARG (null output, cp_size < 1),
+ * DSA_ERR_SHAPE (num_tokens < 0 or the padded count overflows int32). */
+dsa_status dsa_cp_geometry(int32_t num_tokens, int32_t cp_size, int32_t *num_tokens_pad,
+                           int32_t *tokens_per_rank);
+
+/* Host only.  Number of int32 elements one view's metadata needs:
+ * 8 + 2*(batch+1) + 3*batch + tokens_per_rank.  `ints_needed` is a host
+ * pointer. */
+dsa_status dsa_cp_metadata_sizes(int32_t batch, int32_t num_tokens, int32_t cp_size,
+                                 size_t *ints_needed);
+
+/* Host only.  Fill `out` (host struct) with pointers into `buffer` (device,
+ * at least dsa_cp_metadata_sizes() ints, 4-byte aligned); no memory access. */
+dsa_status dsa_cp_metadata_bind(int32_t *buffer, int32_t batch, int32_t num_tokens, int32_t cp_size,
+                                dsa_cp_local_metadata *out);
+
+/*
+ * build_cp_local_metadata ([xLLM] "代码实现 / 2", [blog] "2.B"): the local
+ * view of rank cp_rank.  query_start_loc [batch+1] and seq_lens [batch] are
+ * device arrays with query_start_loc[0] = 0, query_start_loc[batch] =
+ * num_tokens and seq_lens[b] = query length of request b (a prefix, i.e.
+ * chunked prefill, is reported as DSA_ERR_DEVICE_PREFIX through
+ * dsa_poll_device_error).  `out` is a host struct of device pointers.
+ * Split of the flat token stream (padded at the end to a multiple of
+ * cp_size):
+ *   DSA_CP_IN_SEQ_SPLIT: rank r holds rows [r*tpr, (r+1)*tpr)
+ *   DSA_CP_ROUND_ROBIN:  rank r holds rows g with g % cp_size == r, slot g / cp_size.
+ * cp_size == 1 gives the identity view.
+ */
+dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc, const int32_t *seq_lens,
+                                       int32_t batch, int32_t num_tokens, int32_t cp_size,
+                                       int32_t cp_rank, dsa_cp_mode mode,
+                                       const dsa_cp_local_metadata *out, dsa_stream_t stream);
+
+/*
+ * Split ([blog] "2.B" and "第三部分" step 1; [sglang] cp_split_and_rebuild):
+ * gather the rows of src [num_tokens][row_bytes] that rank cp_rank holds
+ * into dst [tpr][row_bytes] (cp_rank >= 0), or every rank's rows into the
+ * rank-major layout dst [cp_size][tpr][row_bytes] (cp_rank == -1; this is
+ * also the all-gathered order T0,T4,T1,T5,... of [blog] "第三部分" step B).
+ * Pad rows are zero.  A byte copy: results are bit-exact.  row_bytes > 0.
+ */
+dsa_status dsa_cp_split(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
+                        dsa_cp_mode mode, int32_t cp_rank, void *dst, dsa_stream_t stream);
+
+/*
+ * Rerange ([blog] "第三部分" step B, [sglang] "第一次 All-Gather",
+ * cp_all_gather_rerange_output): the inverse of the all-rank split, from
+ * the rank-major src [cp_size][tpr][row_bytes] back to logical token order
+ * dst [num_tokens][row_bytes]; pad rows are dropped.  Bit-exact.
+ */
+dsa_status dsa_cp_rerange(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
+                          dsa_cp_mode mode, void *dst, dsa_stream_t stream);
+
+/* Host only.  Recommended workspace bytes for dsa_indexer_topk: room for the
+ * fp32 indexer scores of a block of local rows (rows x round_up(max_kv_len, 4)
+ * x 4 bytes, at most 1 GiB, at least one 8-row tile).  Any size holding one
+ * tile works; smaller workspaces take more launches. */
+dsa_status dsa_indexer_topk_workspace_size(int32_t tokens_per_rank, int32_t max_kv_len, int32_t topk,
+                                           size_t *bytes);
+
+/*
+ * Lightning indexer + causal top-k for one CP view ([xLLM] 单层前向数据流
+ * (3) and "4. Indexer full/local 分离": local queries and weights, full
+ * index keys).  For every local slot i with flat row g in request b,
+ * position p = g - qs_b:
+ *   I[i, s] = sum_j w[i, j] * ReLU(q_idx[i, j, :] . k_idx[qs_b + s, :]),  s = 0..p
+ * and topk_idx[i, :] = the flat KV rows qs_b + s of the topk largest
+ * I[i, s], ties to the lower s, in ascending order; rows with p + 1 <= topk
+ * select every s; unused entries and pad slots are -1.
+ *   md           host struct of device pointers (dsa_cp_build_local_metadata)
+ *   batch        global batch size B (capacity of the md arrays)
+ *   tpr          tokens_per_rank
+ *   max_kv_len   host upper bound of every local_seq_lens entry (e.g. the
+ *                longest request); a larger extent on the device is a
+ *                DSA_ERR_DEVICE_BOUNDS
+ *   q_idx        bf16 [tpr][HI][DI]   (local, split)
+ *   k_idx        bf16 [num_tokens][DI] (full)
+ *   w            fp32 [tpr][HI]        (local, split)
+ *   topk_idx     int32 [tpr][topk]     output
+ *   workspace    device scratch of ws_bytes bytes (16-byte aligned)
+ * Scores accumulate in fp32 on the tensor cores (bf16 inputs).
+ */
+dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                            int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
+                            int32_t num_tokens, int32_t HI, int32_t DI, int32_t topk, int32_t *topk_idx,
+                            void *workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Test hook: the indexer scores themselves for local slots
+ * [row_begin, row_begin + row_count): scores [row_count][max_kv_len] fp32,
+ * entry s of a row = I[i, s] for s <= p, -inf for s > p and for pad slots.
+ * Same inputs and meaning as dsa_indexer_topk.
+ */
+dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                              int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
+                              int32_t num_tokens, int32_t HI, int32_t DI, int32_t row_begin,
+                              int32_t row_count, float *scores, dsa_stream_t stream);
+
+/*
+ * MLA sparse attention prefill for one CP view ([xLLM] 单层前向数据流 (4):
+ * local queries, full latent KV, output [T_local, num_heads_FULL, Dv]).
+ * For every local slot i and head h over the valid selected rows J of
+ * topk_idx[i, :]:
+ *   l_j = softmax_scale * q[i, h, :] . kv[j, :]            (D-wide latent)
+ *   out[i, h, :] = sum_j e^(l_j - m) kv[j, :Dv] / (sum_j e^(l_j - m) + e^(sink_h - m))
+ * with m any common shift and the sink term present only when attn_sink
+ * is non-NULL (a logit in scaled units that adds to the denominator only).
+ *   q          bf16 [tpr][H][D] (local, split)
+ *   kv         bf16 [num_tokens][D] (full); value = the first Dv columns
+ *   topk_idx   int32 [tpr][topk] flat KV rows, -1 = unused (as produced by
+ *              dsa_indexer_topk: the valid entries first)
+ *   attn_sink  fp32 [H] or NULL
+ *   out        bf16 [tpr][H][Dv]; pad slots are written as zeros
+ * QK and PV run on the tensor cores (bf16 operands, fp32 accumulate); the
+ * softmax is fp32.  Each view's per-token arithmetic is independent of the
+ * view, so reranged views reproduce the single-view result.
+ */
+dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                   const void *q, const void *kv, int32_t num_tokens,
+                                   const int32_t *topk_idx, int32_t topk, const float *attn_sink,
+                                   float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
+                                   dsa_stream_t stream);
+
+/* Synchronise `stream`, then return (and clear) the first error a kernel
+ * recorded on the current device since the last poll: DSA_OK, or
+ * DSA_ERR_DEVICE_TIMEOUT / _BOUNDS / _PREFIX; DSA_ERR_CUDA if the sync
+ * itself failed (the message is in dsa_last_cuda_error()). */
+dsa_status dsa_poll_device_error(dsa_stream_t stream);
+
+/* As dsa_poll_device_error, and when an error is returned, `detail` (host,
+ * 3 ints, may be NULL) receives where it was recorded: {site, site detail,
+ * linear CTA index}.  Site codes: 11-18 indexer waits, 21-31 attention waits
+ * (the detail is the key block), 41-46 bounds checks (indexer slot, top-k
+ * slot, top-k overflow, attention slot, attention index, metadata). */
+dsa_status dsa_poll_device_error_detail(dsa_stream_t stream, int32_t *detail);
+
+/* Static string for a status code. */
+const char *dsa_status_string(dsa_status status);
+
+/* Static string of the last CUDA error a call returned DSA_ERR_CUDA for
+ * (per thread; "" if none). */
+const char *dsa_last_cuda_error(void);
+
+/* DSA_CP_ABI_VERSION of the built library. */
+int32_t dsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_CP_H */

@@ -1,0 +1,230 @@
+"""GB300-native DeepSeek Sparse Attention (DSA) prefill on context-parallel views.
+
+Thin PyTorch binding of libdsa_cp.so (include/dsa_cp.h): each function has
+the C entry point's name, checks and marshals its tensors (device, dtype,
+contiguity) and passes raw pointers plus the current CUDA stream.  Every
+step of the path runs in the library's sm_103a kernels; if the library is
+missing it is built, and if it cannot be built or loaded the call raises.
+PyTorch only provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from ._lib import DSAError, LocalMetadata, check, load  # noqa: F401
+
+IN_SEQ_SPLIT = 0
+ROUND_ROBIN = 1
+
+__all__ = [
+    "IN_SEQ_SPLIT", "ROUND_ROBIN", "DSAError", "CPLocalMetadata", "load",
+    "dsa_cp_geometry", "dsa_cp_metadata_sizes", "dsa_cp_build_local_metadata", "dsa_cp_split",
+    "dsa_cp_rerange", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_indexer_scores",
+    "dsa_sparse_attn_prefill", "dsa_poll_device_error",
+]
+
+
+def _stream(stream) -> C.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> C.c_void_p | None:
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def dsa_cp_geometry(num_tokens: int, cp_size: int) -> tuple[int, int]:
+    """(num_tokens_pad, tokens_per_rank)."""
+    pad, tpr = C.c_int32(), C.c_int32()
+    check(load().dsa_cp_geometry(num_tokens, cp_size, C.byref(pad), C.byref(tpr)), "dsa_cp_geometry")
+    return pad.value, tpr.value
+
+
+def dsa_cp_metadata_sizes(batch: int, num_tokens: int, cp_size: int) -> int:
+    n = C.c_size_t()
+    check(load().dsa_cp_metadata_sizes(batch, num_tokens, cp_size, C.byref(n)), "dsa_cp_metadata_sizes")
+    return n.value
+
+
+class CPLocalMetadata:
+    """One CP view's local metadata: a device int32 buffer and the C struct
+    of pointers into it (dsa_cp_local_metadata)."""
+
+    FIELDS = ("local_query_start_loc", "local_seq_lens", "local_kv_start_loc", "local_req_id",
+              "local_req_kv_base", "local_token_pos")
+    SCALARS = ("num_tokens_pad", "tokens_per_rank", "local_start", "local_end", "local_batch",
+               "local_num_tokens", "local_max_seqlen_q", "local_max_seqlen_kv")
+
+    def __init__(self, batch: int, num_tokens: int, cp_size: int, device=None):
+        self.batch, self.num_tokens, self.cp_size = int(batch), int(num_tokens), int(cp_size)
+        self.num_tokens_pad, self.tokens_per_rank = dsa_cp_geometry(num_tokens, cp_size)
+        n = dsa_cp_metadata_sizes(batch, num_tokens, cp_size)
+        self.buffer = torch.zeros(n, dtype=torch.int32, device=device or torch.device("cuda"))
+        self.struct = LocalMetadata()
+        check(load().dsa_cp_metadata_bind(_ptr(self.buffer), batch, num_tokens, cp_size, C.byref(self.struct)),
+              "dsa_cp_metadata_bind")
+
+    def to_host(self) -> dict:
+        """Read the view back (synchronises); lists trimmed to their valid length."""
+        b = self.buffer.cpu().tolist()
+        B, tpr = self.batch, self.tokens_per_rank
+        out = dict(zip(self.SCALARS, b[:8]))
+        o = 8
+        nb = out["local_batch"]
+        for name, size, valid in (("local_query_start_loc", B + 1, nb + 1), ("local_seq_lens", B, nb),
+                                  ("local_kv_start_loc", B + 1, nb + 1), ("local_req_id", B, nb),
+                                  ("local_req_kv_base", B, nb), ("local_token_pos", tpr, tpr)):
+            out[name] = b[o:o + valid]
+            o += size
+        return out
+
+
+def dsa_cp_build_local_metadata(query_start_loc: torch.Tensor, seq_lens: torch.Tensor, num_tokens: int,
+                                cp_size: int, cp_rank: int, mode: int, md: CPLocalMetadata | None = None,
+                                stream=None) -> CPLocalMetadata:
+    _need(query_start_loc, torch.int32, "query_start_loc")
+    _need(seq_lens, torch.int32, "seq_lens")
+    batch = seq_lens.numel()
+    if query_start_loc.numel() != batch + 1:
+        raise ValueError("query_start_loc must have batch + 1 entries")
+    if md is None:
+        md = CPLocalMetadata(batch, num_tokens, cp_size, query_start_loc.device)
+    elif (md.batch, md.num_tokens, md.cp_size) != (batch, num_tokens, cp_size):
+        raise ValueError("metadata buffer was sized for another batch / token count / cp_size")
+    check(load().dsa_cp_build_local_metadata(_ptr(query_start_loc), _ptr(seq_lens), batch, num_tokens, cp_size,
+                                             cp_rank, mode, C.byref(md.struct), _stream(stream)),
+          "dsa_cp_build_local_metadata")
+    return md
+
+
+def _row_bytes(t: torch.Tensor) -> int:
+    return t[0].numel() * t.element_size() if t.dim() > 1 else t.element_size()
+
+
+def dsa_cp_split(src: torch.Tensor, cp_size: int, mode: int, cp_rank: int = -1, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """src [T, ...] -> [cp_size, tpr, ...] (cp_rank == -1) or [tpr, ...]."""
+    if not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    T = src.shape[0]
+    _, tpr = dsa_cp_geometry(T, cp_size)
+    shape = ((cp_size, tpr) if cp_rank < 0 else (tpr,)) + tuple(src.shape[1:])
+    if out is None:
+        out = torch.empty(shape, dtype=src.dtype, device=src.device)
+    elif tuple(out.shape) != shape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {src.dtype} tensor of shape {shape}")
+    check(load().dsa_cp_split(_ptr(src), _row_bytes(src), T, cp_size, mode, cp_rank, _ptr(out), _stream(stream)),
+          "dsa_cp_split")
+    return out
+
+
+def dsa_cp_rerange(src: torch.Tensor, num_tokens: int, cp_size: int, mode: int, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """src [cp_size, tpr, ...] -> [num_tokens, ...]."""
+    if not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    _, tpr = dsa_cp_geometry(num_tokens, cp_size)
+    if tuple(src.shape[:2]) != (cp_size, tpr):
+        raise ValueError(f"src must be [cp_size={cp_size}, tpr={tpr}, ...]")
+    shape = (num_tokens,) + tuple(src.shape[2:])
+    if out is None:
+        out = torch.empty(shape, dtype=src.dtype, device=src.device)
+    elif tuple(out.shape) != shape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {src.dtype} tensor of shape {shape}")
+    row = src[0, 0].numel() * src.element_size() if src.dim() > 2 else src.element_size()
+    check(load().dsa_cp_rerange(_ptr(src), row, num_tokens, cp_size, mode, _ptr(out), _stream(stream)),
+          "dsa_cp_rerange")
+    return out
+
+
+def dsa_indexer_topk_workspace_size(tokens_per_rank: int, max_kv_len: int, topk: int) -> int:
+    n = C.c_size_t()
+    check(load().dsa_indexer_topk_workspace_size(tokens_per_rank, max_kv_len, topk, C.byref(n)),
+          "dsa_indexer_topk_workspace_size")
+    return n.value
+
+
+def dsa_indexer_topk(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor, topk: int,
+                     max_kv_len: int, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """q_idx bf16 [tpr, HI, DI], k_idx bf16 [T, DI], w fp32 [tpr, HI] -> int32 [tpr, topk]."""
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(k_idx, torch.bfloat16, "k_idx")
+    _need(w, torch.float32, "w")
+    tpr, HI, DI = q_idx.shape
+    if tpr != md.tokens_per_rank or tuple(w.shape) != (tpr, HI) or k_idx.shape[1] != DI:
+        raise ValueError("q_idx / w / k_idx shapes do not match the view")
+    if out is None:
+        out = torch.empty((tpr, topk), dtype=torch.int32, device=q_idx.device)
+    _need(out, torch.int32, "out")
+    if workspace is None:
+        workspace = torch.empty(dsa_indexer_topk_workspace_size(tpr, max_kv_len, topk), dtype=torch.uint8,
+                                device=q_idx.device)
+    check(load().dsa_indexer_topk(C.byref(md.struct), md.batch, tpr, max_kv_len, _ptr(q_idx), _ptr(k_idx), _ptr(w),
+                                  k_idx.shape[0], HI, DI, topk, _ptr(out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+          "dsa_indexer_topk")
+    return out
+
+
+def dsa_indexer_scores(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor,
+                       max_kv_len: int, row_begin: int = 0, row_count: int | None = None,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Test hook: fp32 scores [row_count, max_kv_len], -inf beyond each row's causal extent."""
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(k_idx, torch.bfloat16, "k_idx")
+    _need(w, torch.float32, "w")
+    tpr, HI, DI = q_idx.shape
+    if row_count is None:
+        row_count = tpr - row_begin
+    if out is None:
+        out = torch.empty((row_count, max_kv_len), dtype=torch.float32, device=q_idx.device)
+    _need(out, torch.float32, "out")
+    check(load().dsa_indexer_scores(C.byref(md.struct), md.batch, tpr, max_kv_len, _ptr(q_idx), _ptr(k_idx),
+                                    _ptr(w), k_idx.shape[0], HI, DI, row_begin, row_count, _ptr(out),
+                                    _stream(stream)),
+          "dsa_indexer_scores")
+    return out
+
+
+def dsa_sparse_attn_prefill(md: CPLocalMetadata, q: torch.Tensor, kv: torch.Tensor, topk_idx: torch.Tensor,
+                            softmax_scale: float, Dv: int, attn_sink: torch.Tensor | None = None,
+                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q bf16 [tpr, H, D], kv bf16 [T, D], topk_idx int32 [tpr, topk] -> bf16 [tpr, H, Dv]."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv, torch.bfloat16, "kv")
+    _need(topk_idx, torch.int32, "topk_idx")
+    if attn_sink is not None:
+        _need(attn_sink, torch.float32, "attn_sink")
+    tpr, H, D = q.shape
+    if tpr != md.tokens_per_rank or kv.shape[1] != D or topk_idx.shape[0] != tpr:
+        raise ValueError("q / kv / topk_idx shapes do not match the view")
+    if out is None:
+        out = torch.empty((tpr, H, Dv), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    check(load().dsa_sparse_attn_prefill(C.byref(md.struct), md.batch, tpr, _ptr(q), _ptr(kv), kv.shape[0],
+                                         _ptr(topk_idx), topk_idx.shape[1], _ptr(attn_sink), float(softmax_scale),
+                                         H, D, Dv, _ptr(out), _stream(stream)),
+          "dsa_sparse_attn_prefill")
+    return out
+
+
+def dsa_poll_device_error(stream=None) -> None:
+    """Synchronise and raise DSAError if a kernel recorded a device-side error
+    (with the site that recorded it)."""
+    detail = (C.c_int32 * 3)()
+    status = load().dsa_poll_device_error_detail(_stream(stream), detail)
+    if status != 0:
+        raise DSAError(status, "dsa_poll_device_error", tuple(detail))

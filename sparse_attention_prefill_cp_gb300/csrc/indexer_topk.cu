@@ -1,0 +1,559 @@
+// Lightning indexer + causal top-k for one CP view.
+//
+// DeepSeek Sparse Attention (named in "feat: DeepSeek-V4 DSA context-parallel
+// on NPU", section 背景): I[t,s] = sum_j w[t,j] * ReLU(q_I[t,j] . k_I[s]) for
+// the view's local queries t against the full index keys s (same page,
+// 单层前向数据流 (2)(3) and 4. Indexer full/local 分离), then the topk
+// largest I[t,s] over s <= t with ties to the lower s.
+//
+// indexer_kernel (tcgen05, one CTA per 2 x (256/HI) local queries and up to
+// 2048 keys): the key block (128 keys) is the MMA's M side, the query tile's
+// (token, head) rows are N = 256, the indexer dim is K.  Each TMEM lane is
+// then one key holding every head of a token in its own columns, so the
+// weighted-ReLU head sum is a per-thread loop.  Two TMEM accumulators of
+// 256 columns alternate between the two token groups so the epilogue of one
+// overlaps the MMA of the other.  K tiles arrive by TMA (128B swizzle).
+// Scores (fp32) go to a workspace row per query, indexed by in-request key
+// position.
+//
+// topk_kernel (one CTA per query row): 4-pass 8-bit radix select of the
+// topk-th largest score (scores mapped to order-preserving uint32 keys, -0
+// folded into +0), then a block-scan compaction in ascending key order that
+// takes every score above the threshold and the lowest-index ties.
+#include "dsa_common.cuh"
+#include "internal.h"
+
+namespace dsa {
+namespace {
+
+template <int HI_, int DI_>
+struct IdxCfg {
+  static constexpr int HI = HI_, DI = DI_;
+  static constexpr int kTokPerGroup = 256 / HI;          // tokens in one N = 256 MMA
+  static constexpr int kTileTok = 2 * kTokPerGroup;      // two TMEM accumulators
+  static constexpr int kRowsQ = kTileTok * HI;           // 512 B-operand rows
+  static constexpr int kCW = DI >= 64 ? 64 : DI;         // elements per swizzle row
+  static constexpr int kCWB = kCW * 2;                   // 128 B (SW128) or 64 B (SW64)
+  static constexpr int kNCh = DI / kCW;
+  static constexpr uint32_t kLayout = kCWB == 128 ? kLayoutSW128 : kLayoutSW64;
+  static constexpr uint32_t kSBO = 8 * kCWB;             // 8-row swizzle atom
+  static constexpr int kBK = 128;                        // keys per block (M)
+  static constexpr int kStages = DI >= 128 ? 2 : 4;
+  static constexpr int kQBytes = kNCh * kRowsQ * kCWB;
+  static constexpr int kKStageBytes = kNCh * kBK * kCWB;
+  static constexpr int kKSteps = DI / 16;
+  static constexpr int kStepsPerChunk = kCW / 16;
+  static constexpr int kKeyChunk = 2048;                 // keys per CTA
+  static constexpr int kTokPerHalf = kTokPerGroup / 2;   // tokens per epilogue half
+  static constexpr int kThreads = 320;                   // 0 TMA, 1 MMA, 2..9 epilogue
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  // shared memory carve-up (offsets from a 1024-aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffW = kOffK + kStages * kKStageBytes;
+  static constexpr int kOffSlot = kOffW + kTileTok * HI * 4;
+  static constexpr int kOffBar = kOffSlot + kTileTok * 8;
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemUsed = kOffMisc + 64 + 1024;  // + alignment slack
+  // every CTA allocates all 512 TMEM columns: ask for enough smem to keep one CTA per SM
+  static constexpr int kSmemBytes = kSmemUsed < 120 * 1024 ? 120 * 1024 : kSmemUsed;
+  static_assert(HI * kTokPerGroup == 256, "HI must divide 256");
+  static_assert(kTokPerGroup % 2 == 0, "two epilogue halves");
+  static_assert((128 / HI) * HI == 128, "an epilogue half covers 128 columns");
+};
+
+struct IdxParams {
+  dsa_cp_local_metadata md;
+  const float *w;      // [tpr][HI]
+  float *scores;       // [rows][ld]
+  int64_t ld;          // score row stride (floats)
+  int32_t tpr, row_begin, row_end, max_kv_len, num_tokens;
+  int *err;
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const IdxParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *w_s = reinterpret_cast<float *>(smem + C::kOffW);
+  int32_t *s_base = reinterpret_cast<int32_t *>(smem + C::kOffSlot);
+  int32_t *s_p = s_base + C::kTileTok;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *q_full = bars;
+  uint64_t *k_full = bars + 1;
+  uint64_t *k_empty = k_full + C::kStages;
+  uint64_t *t_full = k_empty + C::kStages;
+  uint64_t *t_empty = t_full + 2;
+  uint64_t *mma_done = t_empty + 2;
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);  // [0] tmem base, [1] lo, [2] hi
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slot0 = P.row_begin + blockIdx.x * C::kTileTok;
+  const int local_batch = P.md.scalars[DSA_MD_LOCAL_BATCH];
+
+  if (tid == 0) {
+    misc[1] = 0x7fffffff;
+    misc[2] = 0;
+    misc[3] = 0;  // any valid slot
+  }
+  __syncthreads();
+  // per-slot causal extent: flat key rows [base, base + p]
+  for (int t = tid; t < C::kTileTok; t += C::kThreads) {
+    const int slot = slot0 + t;
+    int base = 0, p = -1;
+    if (slot < P.row_end) {
+      const int g = P.md.local_token_pos[slot];
+      if (g >= 0 && local_batch > 0) {
+        const int j = find_local_request(P.md.local_query_start_loc, local_batch, slot);
+        base = P.md.local_req_kv_base[j];
+        p = g - base;
+        if (p < 0 || p >= P.max_kv_len || g >= P.num_tokens) {
+          record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 41, slot);
+          p = -1;
+        }
+      }
+    }
+    s_base[t] = base;
+    s_p[t] = p;
+    if (p >= 0) {
+      atomicMin(reinterpret_cast<int *>(&misc[1]), base);
+      atomicMax(reinterpret_cast<int *>(&misc[2]), base + p);
+      misc[3] = 1;
+    }
+  }
+  for (int i = tid; i < C::kTileTok * C::HI; i += C::kThreads) {
+    const int slot = slot0 + i / C::HI;
+    w_s[i] = slot < P.row_end ? P.w[static_cast<int64_t>(slot) * C::HI + (i % C::HI)] : 0.f;
+  }
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&t_full[b], 1);
+      mbar_init(&t_empty[b], 256);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&misc[0], 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int lo = static_cast<int>(misc[1]), hi = static_cast<int>(misc[2]);
+  const int kstart = lo + static_cast<int>(blockIdx.y) * C::kKeyChunk;
+  const bool active = misc[3] != 0 && kstart <= hi;
+  const int kend = active ? min(hi + 1, kstart + C::kKeyChunk) : kstart;
+  const int nblk = active ? (kend - kstart + C::kBK - 1) / C::kBK : 0;
+
+  if (nblk > 0) {
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      mbar_arrive_expect_tx(q_full, C::kQBytes);
+      for (int c = 0; c < C::kNCh; ++c)
+        for (int h = 0; h < C::kRowsQ / 256; ++h)
+          tma_load_2d(smem + C::kOffQ + (c * C::kRowsQ + h * 256) * C::kCWB, &qmap, c * C::kCW,
+                      slot0 * C::HI + h * 256, q_full);
+      int issued = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % C::kStages;
+        if (!mbar_wait(&k_empty[s], ((j / C::kStages) & 1) ^ 1, P.err, 11, j)) break;
+        mbar_arrive_expect_tx(&k_full[s], C::kKStageBytes);
+        uint8_t *dst = smem + C::kOffK + s * C::kKStageBytes;
+        for (int c = 0; c < C::kNCh; ++c)
+          tma_load_2d(dst + c * C::kBK * C::kCWB, &kmap, c * C::kCW, kstart + j * C::kBK, &k_full[s]);
+        issued = j + 1;
+      }
+      // drain: every armed load has landed before the CTA can exit
+      mbar_wait(q_full, 0, P.err, 12);
+      for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
+        mbar_wait(&k_full[j % C::kStages], (j / C::kStages) & 1, P.err, 13, j);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
+      const uint32_t k_addr = smem_u32(smem + C::kOffK);
+      bool ok = mbar_wait(q_full, 0, P.err, 14);
+      for (int j = 0; ok && j < nblk; ++j) {
+        const int s = j % C::kStages;
+        if (!(ok = mbar_wait(&k_full[s], (j / C::kStages) & 1, P.err, 15, j))) break;
+        tc_fence_after();
+        for (int g = 0; g < 2; ++g) {
+          if (!(ok = mbar_wait(&t_empty[g], (j & 1) ^ 1, P.err, 16, j))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < C::kKSteps; ++k) {
+            const int ch = k / C::kStepsPerChunk, sub = k % C::kStepsPerChunk;
+            const uint64_t a = smem_desc(k_addr + s * C::kKStageBytes + ch * C::kBK * C::kCWB + sub * 32, 16,
+                                         C::kSBO, C::kLayout);
+            const uint64_t b = smem_desc(q_addr + ch * C::kRowsQ * C::kCWB + g * 256 * C::kCWB + sub * 32, 16,
+                                         C::kSBO, C::kLayout);
+            mma_ss(tmem + g * 256, a, b, C::kIdesc, k > 0 ? 1u : 0u);
+          }
+          mma_commit(&t_full[g]);
+        }
+        mma_commit(&k_empty[s]);
+      }
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, P.err, 17);
+    } else if (warp >= 2) {
+      // ---------------- epilogue: one TMEM lane (= one key) per thread
+      const int quad = warp & 3, half = (warp - 2) >> 2;
+      const int row_in_blk = quad * 32 + lane;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      for (int j = 0; j < nblk; ++j) {
+        const int key = kstart + j * C::kBK + row_in_blk;
+        bool ok = true;
+        for (int g = 0; g < 2; ++g) {
+          // tcgen05.ld is warp-collective: keep the exit decision warp-uniform
+          ok = __all_sync(0xffffffffu, mbar_wait(&t_full[g], j & 1, P.err, 18, j));
+          if (!ok) break;
+          tc_fence_after();
+          float acc[C::kTokPerHalf];
+#pragma unroll
+          for (int u = 0; u < C::kTokPerHalf; ++u) acc[u] = 0.f;
+          const int tok0 = g * C::kTokPerGroup + half * C::kTokPerHalf;
+          const float *wrow = w_s + tok0 * C::HI;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + g * 256 + half * 128 + c4 * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int col = c4 * 32 + c;
+              acc[col / C::HI] = fmaf(wrow[col], fmaxf(__uint_as_float(r[c]), 0.f), acc[col / C::HI]);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&t_empty[g]);
+#pragma unroll
+          for (int u = 0; u < C::kTokPerHalf; ++u) {
+            const int t = tok0 + u;
+            const int ks = key - s_base[t];
+            if (ks >= 0 && ks <= s_p[t])
+              P.scores[static_cast<int64_t>(slot0 - P.row_begin + t) * P.ld + ks] = acc[u];
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ top-k
+constexpr int kTopkThreads = 512;
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t b = __float_as_uint(x == 0.f ? 0.f : x);  // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Exclusive block scan of two counters (512 threads).
+__device__ __forceinline__ void scan2(int a, int b, int &ea, int &eb, int &ta, int &tb, int2 *warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int xa = __shfl_up_sync(0xffffffffu, ia, off), xb = __shfl_up_sync(0xffffffffu, ib, off);
+    if (lane >= off) {
+      ia += xa;
+      ib += xb;
+    }
+  }
+  if (lane == 31) warp_tot[warp] = make_int2(ia, ib);
+  __syncthreads();
+  int pa = 0, pb = 0;
+  ta = 0;
+  tb = 0;
+#pragma unroll
+  for (int w = 0; w < kTopkThreads / 32; ++w) {
+    const int2 v = warp_tot[w];
+    if (w < warp) {
+      pa += v.x;
+      pb += v.y;
+    }
+    ta += v.x;
+    tb += v.y;
+  }
+  __syncthreads();
+  ea = pa + ia - a;
+  eb = pb + ib - b;
+}
+
+template <int TOPK>
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_metadata md, int32_t row_begin,
+                                                            int32_t max_kv_len, const float *__restrict__ scores,
+                                                            int64_t ld, int32_t *__restrict__ topk_idx, int *err) {
+  __shared__ uint32_t hist[256];
+  __shared__ int2 warp_tot[kTopkThreads / 32];
+  __shared__ int s_base, s_p, s_digit, s_krem;
+  const int tid = threadIdx.x;
+  const int slot = row_begin + blockIdx.x;
+  int32_t *out = topk_idx + static_cast<int64_t>(slot) * TOPK;
+  if (tid == 0) {
+    int base = 0, p = -1;
+    const int g = md.local_token_pos[slot];
+    const int nb = md.scalars[DSA_MD_LOCAL_BATCH];
+    if (g >= 0 && nb > 0) {
+      const int j = find_local_request(md.local_query_start_loc, nb, slot);
+      base = md.local_req_kv_base[j];
+      p = g - base;
+      if (p < 0 || p >= max_kv_len) {
+        record_error(err, DSA_ERR_DEVICE_BOUNDS, 42, slot);
+        p = -1;
+      }
+    }
+    s_base = base;
+    s_p = p;
+  }
+  __syncthreads();
+  const int base = s_base, n = s_p + 1;
+  if (n <= TOPK) {  // pad slot or short row: every causal key, then -1
+    for (int i = tid; i < TOPK; i += kTopkThreads) out[i] = i < n ? base + i : -1;
+    return;
+  }
+  const float *row = scores + static_cast<int64_t>(blockIdx.x) * ld;
+
+  uint32_t prefix = 0, mask = 0;
+  int krem = TOPK;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint32_t key = order_key(row[i]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // warp 0 finds the digit holding the krem-th largest key: suffix sums over 8 digits per lane
+      uint32_t local[8], sum = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        local[k] = hist[255 - (tid * 8 + k)];
+        sum += local[k];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, off);
+        if (tid >= off) incl += x;
+      }
+      uint32_t cum = incl - sum;  // count of keys in higher digits than this lane's first
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (cum < static_cast<uint32_t>(krem) && cum + local[k] >= static_cast<uint32_t>(krem)) {
+          s_digit = 255 - (tid * 8 + k);
+          s_krem = krem - static_cast<int>(cum);
+        }
+        cum += local[k];
+      }
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(s_digit) << shift;
+    mask |= 255u << shift;
+    krem = s_krem;
+    __syncthreads();
+  }
+  // prefix is the threshold key; take every key above it and the first krem equal ones
+  const uint32_t thr = prefix;
+  int run_sel = 0, run_eq = 0;
+  for (int t0 = 0; t0 < n; t0 += kTopkThreads * 4) {
+    const int i0 = t0 + tid * 4;
+    uint32_t keys[4];
+    int c_eq = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      keys[k] = (i0 + k < n) ? order_key(row[i0 + k]) : 0u;
+      c_eq += (i0 + k < n && keys[k] == thr);
+    }
+    int e_eq, e_dummy, t_eq, t_dummy;
+    scan2(c_eq, 0, e_eq, e_dummy, t_eq, t_dummy, warp_tot);
+    int sel[4], c_sel = 0, r_eq = run_eq + e_eq;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool valid = i0 + k < n;
+      const bool eq = valid && keys[k] == thr;
+      sel[k] = valid && (keys[k] > thr || (eq && r_eq < krem));
+      r_eq += eq;
+      c_sel += sel[k];
+    }
+    int e_sel, t_sel;
+    scan2(c_sel, 0, e_sel, e_dummy, t_sel, t_dummy, warp_tot);
+    int pos = run_sel + e_sel;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (sel[k]) {
+        if (pos < TOPK) out[pos] = base + i0 + k;
+        else record_error(err, DSA_ERR_DEVICE_BOUNDS, 43, slot);
+        ++pos;
+      }
+    }
+    run_sel += t_sel;
+    run_eq += t_eq;
+  }
+}
+
+__global__ void fill_kernel(float *p, int64_t n, float v) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    p[i] = v;
+}
+
+// ------------------------------------------------------------------ host side
+template <class C>
+dsa_status make_maps(const void *q_idx, const void *k_idx, int32_t tpr, int32_t num_tokens, CUtensorMap *qmap,
+                     CUtensorMap *kmap) {
+  const CUtensorMapSwizzle sw = C::kCWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  uint64_t qdims[2] = {static_cast<uint64_t>(C::DI), static_cast<uint64_t>(tpr) * C::HI};
+  uint64_t qstr[1] = {static_cast<uint64_t>(C::DI) * 2};
+  uint32_t qbox[2] = {static_cast<uint32_t>(C::kCW), 256};
+  dsa_status st = encode_tensor_map(qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_idx, qdims, qstr, qbox, sw);
+  if (st != DSA_OK) return st;
+  uint64_t kdims[2] = {static_cast<uint64_t>(C::DI), static_cast<uint64_t>(num_tokens)};
+  uint32_t kbox[2] = {static_cast<uint32_t>(C::kCW), 128};
+  return encode_tensor_map(kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k_idx, kdims, qstr, kbox, sw);
+}
+
+template <class C>
+dsa_status launch_indexer(const CUtensorMap &qmap, const CUtensorMap &kmap, const IdxParams &P,
+                          cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int rows = P.row_end - P.row_begin;
+  dim3 grid((rows + C::kTileTok - 1) / C::kTileTok, (P.max_kv_len + C::kKeyChunk - 1) / C::kKeyChunk);
+  indexer_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(qmap, kmap, P);
+  return check_launch();
+}
+
+struct Args {
+  const dsa_cp_local_metadata *md;
+  int32_t batch, tpr, max_kv_len, num_tokens, HI, DI;
+  const void *q_idx, *k_idx;
+  const float *w;
+};
+
+dsa_status validate(const Args &a) {
+  if (!a.md || !a.q_idx || !a.k_idx || !a.w) return DSA_ERR_INVALID_ARG;
+  if (!a.md->scalars || !a.md->local_query_start_loc || !a.md->local_req_kv_base || !a.md->local_token_pos)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned16(a.q_idx) || !aligned16(a.k_idx)) return DSA_ERR_INVALID_ARG;
+  if (a.batch < 0 || a.tpr < 0 || a.max_kv_len < 1 || a.num_tokens < 1) return DSA_ERR_SHAPE;
+  if (static_cast<int64_t>(a.tpr) * a.HI > INT32_MAX) return DSA_ERR_SHAPE;
+  return DSA_OK;
+}
+
+using BigIdx = IdxCfg<64, 128>;
+using TinyIdx = IdxCfg<4, 32>;
+
+template <class C>
+dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *out, int64_t ld,
+                      cudaStream_t stream) {
+  CUtensorMap qmap, kmap;
+  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_tokens, &qmap, &kmap);
+  if (st != DSA_OK) return st;
+  int *err = device_error_word();
+  if (!err) return DSA_ERR_CUDA;
+  IdxParams P{*a.md, a.w, out, ld, a.tpr, row_begin, row_end, a.max_kv_len, a.num_tokens, err};
+  return launch_indexer<C>(qmap, kmap, P, stream);
+}
+
+template <class C, int TOPK>
+dsa_status run_topk(const Args &a, int32_t *topk_idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
+  const int64_t ld = (static_cast<int64_t>(a.max_kv_len) + 3) / 4 * 4;
+  int64_t rows_fit = static_cast<int64_t>(ws_bytes / (static_cast<size_t>(ld) * 4));
+  rows_fit = rows_fit / C::kTileTok * C::kTileTok;
+  if (rows_fit < C::kTileTok) return DSA_ERR_WORKSPACE;
+  CUtensorMap qmap, kmap;
+  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_tokens, &qmap, &kmap);
+  if (st != DSA_OK) return st;
+  int *err = device_error_word();
+  if (!err) return DSA_ERR_CUDA;
+  float *scores = static_cast<float *>(ws);
+  for (int64_t r0 = 0; r0 < a.tpr; r0 += rows_fit) {
+    const int32_t r1 = static_cast<int32_t>(r0 + rows_fit < a.tpr ? r0 + rows_fit : a.tpr);
+    IdxParams P{*a.md, a.w, scores, ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_tokens, err};
+    st = launch_indexer<C>(qmap, kmap, P, stream);
+    if (st != DSA_OK) return st;
+    topk_kernel<TOPK><<<static_cast<unsigned>(r1 - r0), kTopkThreads, 0, stream>>>(
+        *a.md, static_cast<int32_t>(r0), a.max_kv_len, scores, ld, topk_idx, err);
+    st = check_launch();
+    if (st != DSA_OK) return st;
+  }
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status dsa_indexer_topk_workspace_size(int32_t tokens_per_rank, int32_t max_kv_len, int32_t topk,
+                                                      size_t *bytes) {
+  if (!bytes) return DSA_ERR_INVALID_ARG;
+  if (tokens_per_rank < 0 || max_kv_len < 1 || topk < 1) return DSA_ERR_SHAPE;
+  const size_t row = static_cast<size_t>((static_cast<int64_t>(max_kv_len) + 3) / 4 * 4) * 4;
+  const size_t tile = topk <= 64 ? TinyIdx::kTileTok : BigIdx::kTileTok;
+  size_t rows = (static_cast<size_t>(tokens_per_rank) + tile - 1) / tile * tile;
+  const size_t cap = (size_t(1) << 30) / row / tile * tile;
+  if (rows > cap) rows = cap;
+  if (rows < tile) rows = tile;
+  *bytes = rows * row;
+  return DSA_OK;
+}
+
+extern "C" dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                       int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
+                                       int32_t num_tokens, int32_t HI, int32_t DI, int32_t topk,
+                                       int32_t *topk_idx, void *workspace, size_t ws_bytes,
+                                       dsa_stream_t stream) {
+  Args a{md, batch, tpr, max_kv_len, num_tokens, HI, DI, q_idx, k_idx, w};
+  dsa_status st = validate(a);
+  if (st != DSA_OK) return st;
+  if (!topk_idx || !workspace || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+  if (tpr == 0) return DSA_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (HI == 64 && DI == 128 && topk == 2048) return run_topk<BigIdx, 2048>(a, topk_idx, workspace, ws_bytes, s);
+  if (HI == 4 && DI == 32 && topk == 64) return run_topk<TinyIdx, 64>(a, topk_idx, workspace, ws_bytes, s);
+  return DSA_ERR_UNSUPPORTED;
+}
+
+extern "C" dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                         int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
+                                         int32_t num_tokens, int32_t HI, int32_t DI, int32_t row_begin,
+                                         int32_t row_count, float *scores, dsa_stream_t stream) {
+  Args a{md, batch, tpr, max_kv_len, num_tokens, HI, DI, q_idx, k_idx, w};
+  dsa_status st = validate(a);
+  if (st != DSA_OK) return st;
+  if (!scores) return DSA_ERR_INVALID_ARG;
+  if (row_begin < 0 || row_count < 0 || static_cast<int64_t>(row_begin) + row_count > tpr) return DSA_ERR_SHAPE;
+  if (row_count == 0) return DSA_OK;
+  const bool big = HI == 64 && DI == 128, tiny = HI == 4 && DI == 32;
+  if (!big && !tiny) return DSA_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t n = static_cast<int64_t>(row_count) * max_kv_len;
+  fill_kernel<<<static_cast<unsigned>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, s>>>(
+      scores, n, -__builtin_huge_valf());
+  st = check_launch();
+  if (st != DSA_OK) return st;
+  return big ? run_scores<BigIdx>(a, row_begin, row_begin + row_count, scores, max_kv_len, s)
+             : run_scores<TinyIdx>(a, row_begin, row_begin + row_count, scores, max_kv_len, s);
+}

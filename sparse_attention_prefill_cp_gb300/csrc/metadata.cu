@@ -1,0 +1,185 @@
+// build_cp_local_metadata on the device ("feat: DeepSeek-V4 DSA
+// context-parallel on NPU", section 代码实现 / 2; round-robin split of
+// "[DeepSeek v3.2] 上下文并行详解", section 2.B).
+//
+// One CTA per call.  Per request b the number of local rows and the last
+// local position come from closed forms (an interval intersection for
+// in-seq-split, an arithmetic progression for round-robin); a block-wide
+// exclusive scan compacts the requests that have local rows.
+#include "dsa_common.cuh"
+#include "internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct Triple {
+  int a, b, c;
+};
+
+// Exclusive scan of (a, b, c) over the block; returns the block totals in `tot`.
+__device__ Triple block_exclusive_scan(Triple v, Triple &tot) {
+  __shared__ Triple warp_tot[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  Triple inc = v;
+  for (int off = 1; off < 32; off <<= 1) {
+    int a = __shfl_up_sync(0xffffffffu, inc.a, off);
+    int b = __shfl_up_sync(0xffffffffu, inc.b, off);
+    int c = __shfl_up_sync(0xffffffffu, inc.c, off);
+    if (lane >= off) {
+      inc.a += a;
+      inc.b += b;
+      inc.c += c;
+    }
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  Triple before = {0, 0, 0};
+  tot = {0, 0, 0};
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) {
+      before.a += warp_tot[w].a;
+      before.b += warp_tot[w].b;
+      before.c += warp_tot[w].c;
+    }
+    tot.a += warp_tot[w].a;
+    tot.b += warp_tot[w].b;
+    tot.c += warp_tot[w].c;
+  }
+  __syncthreads();
+  return {before.a + inc.a - v.a, before.b + inc.b - v.b, before.c + inc.c - v.c};
+}
+
+__global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__restrict__ qsl,
+                                                               const int32_t *__restrict__ seq_lens, int B,
+                                                               int T, int cp, int rank, int mode,
+                                                               dsa_cp_local_metadata md, int *err) {
+  __shared__ int s_bad;
+  __shared__ int s_run[3];  // running local_batch, query total, kv total
+  __shared__ int s_maxq, s_maxkv;
+  const int tid = threadIdx.x;
+  const int64_t tpr = (static_cast<int64_t>(T) + cp - 1) / cp;
+
+  if (tid == 0) {
+    s_bad = 0;
+    s_run[0] = s_run[1] = s_run[2] = 0;
+    s_maxq = s_maxkv = 0;
+  }
+  __syncthreads();
+  // Inputs must describe a plain prefill: cu-seqlens from 0 to T, and
+  // seq_lens equal to the query lengths (no prefix KV).
+  for (int b = tid; b < B; b += kThreads) {
+    const int qs = __ldg(qsl + b), qe = __ldg(qsl + b + 1);
+    if (qe < qs || qs < 0 || qe > T) atomicOr(&s_bad, 1);
+    else if (__ldg(seq_lens + b) != qe - qs) atomicOr(&s_bad, 2);
+  }
+  if (tid == 0 && (__ldg(qsl) != 0 || __ldg(qsl + B) != T)) atomicOr(&s_bad, 1);
+  __syncthreads();
+  const int bad = s_bad;
+  if (bad && tid == 0) record_error(err, (bad & 1) ? DSA_ERR_DEVICE_BOUNDS : DSA_ERR_DEVICE_PREFIX, 46, bad);
+
+  // local slot -> flat token row
+  const int64_t lo_inseq = static_cast<int64_t>(rank) * tpr;
+  const int64_t hi_inseq = lo_inseq + tpr < T ? lo_inseq + tpr : T;
+  for (int64_t i = tid; i < tpr; i += kThreads) {
+    const int64_t g = (mode == DSA_CP_IN_SEQ_SPLIT) ? lo_inseq + i : rank + i * cp;
+    md.local_token_pos[i] = (!bad && g < T) ? static_cast<int32_t>(g) : -1;
+  }
+  if (tid == 0) {
+    md.local_query_start_loc[0] = 0;
+    md.local_kv_start_loc[0] = 0;
+  }
+
+  if (!bad) {
+    for (int base = 0; base < B; base += kThreads) {
+      const int b = base + tid;
+      Triple v = {0, 0, 0};
+      int qs = 0;
+      if (b < B) {
+        qs = __ldg(qsl + b);
+        const int qe = __ldg(qsl + b + 1);
+        int64_t q_len = 0, last = -1;
+        if (mode == DSA_CP_IN_SEQ_SPLIT) {
+          const int64_t lo = qs > lo_inseq ? qs : lo_inseq;
+          const int64_t hi = qe < hi_inseq ? qe : hi_inseq;
+          if (hi > lo) {
+            q_len = hi - lo;
+            last = hi - 1;
+          }
+        } else {
+          // first g >= qs with g % cp == rank
+          const int64_t g0 = qs + ((rank - qs % cp) % cp + cp) % cp;
+          if (g0 < qe) {
+            q_len = (qe - 1 - g0) / cp + 1;
+            last = g0 + (q_len - 1) * cp;
+          }
+        }
+        if (q_len > 0) v = {1, static_cast<int>(q_len), static_cast<int>(last - qs + 1)};
+      }
+      Triple tot;
+      Triple ex = block_exclusive_scan(v, tot);
+      if (v.a) {
+        const int j = s_run[0] + ex.a;
+        md.local_query_start_loc[j + 1] = s_run[1] + ex.b + v.b;
+        md.local_kv_start_loc[j + 1] = s_run[2] + ex.c + v.c;
+        md.local_seq_lens[j] = v.c;
+        md.local_req_id[j] = b;
+        md.local_req_kv_base[j] = qs;
+        atomicMax(&s_maxq, v.b);
+        atomicMax(&s_maxkv, v.c);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        s_run[0] += tot.a;
+        s_run[1] += tot.b;
+        s_run[2] += tot.c;
+      }
+      __syncthreads();
+    }
+  }
+
+  if (tid == 0) {
+    int32_t *s = md.scalars;
+    s[DSA_MD_NUM_TOKENS_PAD] = static_cast<int32_t>(tpr * cp);
+    s[DSA_MD_TOKENS_PER_RANK] = static_cast<int32_t>(tpr);
+    if (mode == DSA_CP_IN_SEQ_SPLIT) {
+      s[DSA_MD_LOCAL_START] = static_cast<int32_t>(lo_inseq < T ? lo_inseq : T);
+      s[DSA_MD_LOCAL_END] = static_cast<int32_t>(hi_inseq > lo_inseq ? hi_inseq : (lo_inseq < T ? lo_inseq : T));
+    } else {
+      s[DSA_MD_LOCAL_START] = rank < T ? rank : T;
+      s[DSA_MD_LOCAL_END] = T;
+    }
+    s[DSA_MD_LOCAL_BATCH] = s_run[0];
+    s[DSA_MD_LOCAL_NUM_TOKENS] = s_run[1];
+    s[DSA_MD_LOCAL_MAX_SEQLEN_Q] = s_maxq;
+    s[DSA_MD_LOCAL_MAX_SEQLEN_KV] = s_maxkv;
+  }
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc, const int32_t *seq_lens,
+                                                  int32_t batch, int32_t num_tokens, int32_t cp_size,
+                                                  int32_t cp_rank, dsa_cp_mode mode,
+                                                  const dsa_cp_local_metadata *out, dsa_stream_t stream) {
+  if (!query_start_loc || !seq_lens || !out) return DSA_ERR_INVALID_ARG;
+  if (cp_size < 1 || cp_rank < 0 || cp_rank >= cp_size) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (!out->scalars || !out->local_query_start_loc || !out->local_seq_lens || !out->local_kv_start_loc ||
+      !out->local_req_id || !out->local_req_kv_base || !out->local_token_pos)
+    return DSA_ERR_INVALID_ARG;
+  if (batch < 0 || num_tokens < 0) return DSA_ERR_SHAPE;
+  int32_t pad = 0, tpr = 0;
+  dsa_status st = dsa_cp_geometry(num_tokens, cp_size, &pad, &tpr);
+  if (st != DSA_OK) return st;
+  int *err = device_error_word();
+  if (!err) return DSA_ERR_CUDA;
+  cp_metadata_kernel<<<1, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      query_start_loc, seq_lens, batch, num_tokens, cp_size, cp_rank, static_cast<int>(mode), *out, err);
+  return check_launch();
+}

@@ -1,0 +1,131 @@
+// Split and rerange of the CP token layout ("[DeepSeek v3.2] 上下文并行详解",
+// sections 2.B and 第三部分; "NSA Prefill CP 中两次 All-Gather 的作用说明",
+// 第一次 All-Gather).  Both are row gathers: dst row d <- src row map(d), or
+// zeros when map(d) is a pad slot.  HBM-bound byte copies, bit-exact.
+//
+// Large rows (>= 2 KB, e.g. 147,456-byte attention-query rows): one CTA
+// copies a 16 KB piece of one row with 16-byte vectors, 8 loads in flight per
+// thread.  Small rows (e.g. 256-byte indexer-weight rows): one warp per row.
+#include "dsa_common.cuh"
+#include "internal.h"
+
+namespace dsa {
+namespace {
+
+struct SplitMap {  // dst [n_ranks][tpr] <- src [T]
+  int64_t tpr, T;
+  int32_t cp, rank, mode;  // rank < 0: all ranks
+  __device__ __forceinline__ int64_t operator()(int64_t d) const {
+    const int64_t r = rank < 0 ? d / tpr : rank;
+    const int64_t i = rank < 0 ? d - r * tpr : d;
+    const int64_t g = (mode == DSA_CP_IN_SEQ_SPLIT) ? r * tpr + i : r + i * cp;
+    return g < T ? g : -1;
+  }
+};
+
+struct RerangeMap {  // dst [T] <- src [cp][tpr]
+  int64_t tpr;
+  int32_t cp, mode;
+  __device__ __forceinline__ int64_t operator()(int64_t g) const {
+    const int64_t r = (mode == DSA_CP_IN_SEQ_SPLIT) ? g / tpr : g % cp;
+    const int64_t i = (mode == DSA_CP_IN_SEQ_SPLIT) ? g - r * tpr : g / cp;
+    return r * tpr + i;
+  }
+};
+
+constexpr int kBigThreads = 128;
+constexpr int kBigUnroll = 8;
+constexpr int64_t kBigChunk = kBigThreads * kBigUnroll;  // elements per CTA
+
+template <class T, class Map>
+__global__ void __launch_bounds__(kBigThreads) copy_rows_big(const T *__restrict__ src, T *__restrict__ dst,
+                                                             int64_t elems_per_row, Map map) {
+  const int64_t row = blockIdx.x;
+  const int64_t s = map(row);
+  const int64_t e0 = static_cast<int64_t>(blockIdx.y) * kBigChunk + threadIdx.x;
+  const T *sp = src + s * elems_per_row;
+  T *dp = dst + row * elems_per_row;
+  T v[kBigUnroll];
+#pragma unroll
+  for (int k = 0; k < kBigUnroll; ++k) {
+    const int64_t e = e0 + k * kBigThreads;
+    if (s >= 0 && e < elems_per_row) v[k] = __ldcs(sp + e);
+    else v[k] = T{};
+  }
+#pragma unroll
+  for (int k = 0; k < kBigUnroll; ++k) {
+    const int64_t e = e0 + k * kBigThreads;
+    if (e < elems_per_row) __stcs(dp + e, v[k]);
+  }
+}
+
+template <class T, class Map>
+__global__ void __launch_bounds__(256) copy_rows_small(const T *__restrict__ src, T *__restrict__ dst,
+                                                       int64_t elems_per_row, int64_t n_rows, Map map) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= n_rows) return;
+  const int64_t s = map(row);
+  for (int64_t e = threadIdx.x & 31; e < elems_per_row; e += 32)
+    dst[row * elems_per_row + e] = s >= 0 ? src[s * elems_per_row + e] : T{};
+}
+
+template <class Map>
+dsa_status launch_copy(const void *src, void *dst, int64_t row_bytes, int64_t n_rows, Map map,
+                       cudaStream_t stream) {
+  if (n_rows == 0) return DSA_OK;
+  const bool a16 = aligned16(src) && aligned16(dst) && (row_bytes % 16 == 0);
+  const bool a4 = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) % 4 == 0) &&
+                  (row_bytes % 4 == 0);
+  auto go = [&](auto tag) -> dsa_status {
+    using T = decltype(tag);
+    const int64_t elems = row_bytes / static_cast<int64_t>(sizeof(T));
+    if (row_bytes >= 2048) {
+      const int64_t chunks = (elems + kBigChunk - 1) / kBigChunk;
+      if (chunks > 65535 || n_rows > INT32_MAX) return DSA_ERR_SHAPE;
+      dim3 grid(static_cast<unsigned>(n_rows), static_cast<unsigned>(chunks));
+      copy_rows_big<T, Map><<<grid, kBigThreads, 0, stream>>>(static_cast<const T *>(src), static_cast<T *>(dst),
+                                                             elems, map);
+    } else {
+      const int64_t blocks = (n_rows + 7) / 8;
+      if (blocks > INT32_MAX) return DSA_ERR_SHAPE;
+      copy_rows_small<T, Map><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+          static_cast<const T *>(src), static_cast<T *>(dst), elems, n_rows, map);
+    }
+    return check_launch();
+  };
+  if (a16) return go(uint4{});
+  if (a4) return go(uint32_t{});
+  return go(uint8_t{});
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status dsa_cp_split(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
+                                   dsa_cp_mode mode, int32_t cp_rank, void *dst, dsa_stream_t stream) {
+  if (!src || !dst) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (cp_size < 1 || cp_rank < -1 || cp_rank >= cp_size) return DSA_ERR_INVALID_ARG;
+  if (row_bytes <= 0 || num_tokens < 0) return DSA_ERR_SHAPE;
+  int32_t pad = 0, tpr = 0;
+  dsa_status st = dsa_cp_geometry(num_tokens, cp_size, &pad, &tpr);
+  if (st != DSA_OK) return st;
+  const int64_t n_rows = cp_rank < 0 ? static_cast<int64_t>(pad) : tpr;
+  SplitMap map{tpr, num_tokens, cp_size, cp_rank, static_cast<int32_t>(mode)};
+  return launch_copy(src, dst, row_bytes, n_rows, map, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsa_status dsa_cp_rerange(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
+                                     dsa_cp_mode mode, void *dst, dsa_stream_t stream) {
+  if (!src || !dst) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (cp_size < 1) return DSA_ERR_INVALID_ARG;
+  if (row_bytes <= 0 || num_tokens < 0) return DSA_ERR_SHAPE;
+  int32_t pad = 0, tpr = 0;
+  dsa_status st = dsa_cp_geometry(num_tokens, cp_size, &pad, &tpr);
+  if (st != DSA_OK) return st;
+  RerangeMap map{tpr, cp_size, static_cast<int32_t>(mode)};
+  return launch_copy(src, dst, row_bytes, num_tokens, map, reinterpret_cast<cudaStream_t>(stream));
+}

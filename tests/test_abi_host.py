@@ -1,0 +1,93 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+function include/dsa_cp.h declares, and its host-side logic (geometry,
+metadata sizing, argument validation) answers without touching a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+import sparse_attention_prefill_cp_gb300 as dsa
+from sparse_attention_prefill_cp_gb300 import _lib
+from oracle import dsa_oracle as O
+
+HEADER = os.path.join(ROOT, "include", "dsa_cp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(dsa_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.dsa_abi_version() == 1
+    for code, name in _lib.STATUS.items():
+        assert lib.dsa_status_string(code).decode().startswith(name)
+
+
+@pytest.mark.parametrize("T,cp", [(0, 1), (1, 1), (12, 3), (13, 4), (11805, 4), (184265, 16), (65536, 8)])
+def test_geometry_matches_oracle(T, cp):
+    assert dsa.dsa_cp_geometry(T, cp) == O.padded_geometry(T, cp)
+
+
+def test_metadata_sizes_and_bind(lib):
+    B, T, cp = 4, 11805, 4
+    n = dsa.dsa_cp_metadata_sizes(B, T, cp)
+    tpr = O.padded_geometry(T, cp)[1]
+    assert n == 8 + 2 * (B + 1) + 3 * B + tpr
+    md = _lib.LocalMetadata()
+    base = 0x10000
+    assert lib.dsa_cp_metadata_bind(C.c_void_p(base), B, T, cp, C.byref(md)) == 0
+    offs = [md.scalars, md.local_query_start_loc, md.local_seq_lens, md.local_kv_start_loc, md.local_req_id,
+            md.local_req_kv_base, md.local_token_pos]
+    assert [(o - base) // 4 for o in offs] == [0, 8, 8 + B + 1, 8 + 2 * B + 1, 8 + 3 * B + 2, 8 + 4 * B + 2,
+                                                8 + 5 * B + 2]
+
+
+def test_workspace_size_holds_a_tile():
+    big = dsa.dsa_indexer_topk_workspace_size(1024, 8192, 2048)
+    assert big == 1024 * 8192 * 4
+    assert dsa.dsa_indexer_topk_workspace_size(8192, 65536, 2048) <= (1 << 30)
+    assert dsa.dsa_indexer_topk_workspace_size(1, 3, 2048) == 8 * 4 * 4  # one 8-row tile, ld rounded to 4
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    md = _lib.LocalMetadata()
+    assert lib.dsa_cp_metadata_bind(C.c_void_p(0x10000), 1, 16, 2, C.byref(md)) == 0
+    p = C.c_void_p(0x10000)
+    # null pointers, bad rank / mode / sizes
+    assert lib.dsa_cp_split(None, 16, 10, 2, 0, -1, p, None) == 1
+    assert lib.dsa_cp_split(p, 16, 10, 2, 7, -1, p, None) == 1
+    assert lib.dsa_cp_split(p, 16, 10, 2, 0, 2, p, None) == 1
+    assert lib.dsa_cp_split(p, 0, 10, 2, 0, -1, p, None) == 2
+    assert lib.dsa_cp_rerange(p, 16, -1, 2, 1, p, None) == 2
+    assert lib.dsa_cp_build_local_metadata(p, p, 1, 16, 2, 2, 0, C.byref(md), None) == 1
+    assert lib.dsa_cp_build_local_metadata(p, p, 1, 16, 0, 0, 0, C.byref(md), None) == 1
+    assert lib.dsa_cp_geometry(5, 0, C.byref(C.c_int32()), C.byref(C.c_int32())) == 1
+    # dimension sets that are not compiled
+    assert lib.dsa_indexer_topk(C.byref(md), 1, 8, 16, p, p, p, 16, 32, 128, 2048, p, p, 1 << 20, None) == 3
+    assert lib.dsa_indexer_topk(C.byref(md), 1, 8, 16, p, p, p, 16, 64, 128, 1024, p, p, 1 << 20, None) == 3
+    assert lib.dsa_sparse_attn_prefill(C.byref(md), 1, 8, p, p, 16, p, 2048, None, C.c_float(0.07), 64, 576,
+                                       512, p, None) == 3
+    # misaligned tensors and a non-positive scale
+    q = C.c_void_p(0x10008)
+    assert lib.dsa_sparse_attn_prefill(C.byref(md), 1, 8, q, p, 16, p, 2048, None, C.c_float(0.07), 128, 576,
+                                       512, p, None) == 1
+    assert lib.dsa_sparse_attn_prefill(C.byref(md), 1, 8, p, p, 16, p, 2048, None, C.c_float(-1.0), 128, 576,
+                                       512, p, None) == 1
+    assert lib.dsa_indexer_topk(None, 1, 8, 16, p, p, p, 16, 64, 128, 2048, p, p, 1 << 20, None) == 1
