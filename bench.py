@@ -1,0 +1,400 @@
+"""Benchmark: DSA prefill query-tokens/s on one GB300 (or N, as weak-scaling
+replicas), with the dominant kernel's roofline fraction and the fp64 oracle
+timed on the host cores beside it.
+
+A step is one pass of the whole path over one batch: local metadata for
+every CP view, split of q / q_idx / w, then per view the indexer + top-k and
+the sparse attention, then the rerange of the outputs.  Inputs are resident
+in HBM before the timed region (``value``); ``e2e`` repeats the step through
+pinned host buffers with the copies inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--mode in-seq|round-robin]
+Under torchrun each rank runs its own batch (weak scaling); rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "DSA prefill query-tokens/s (indexer+top-k+sparse attn), % of roofline"
+UNIT = "query-tokens/s"
+DEFAULT_WORKLOAD = W.LONG_8K.name
+L2_BYTES = 126 * 1024 * 1024
+PROFILE_FILE = os.path.join(ROOT, "profiles", "sparse_attn_kernel_long8k.md")
+ATTN_SRC = os.path.join(ROOT, "sparse_attention_prefill_cp_gb300", "csrc", "sparse_attn.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
+    ap.add_argument("--mode", choices=["in-seq", "round-robin"], default=None)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ work model
+
+def positions(wl):
+    """in-request position of every flat token"""
+    return np.concatenate([np.arange(n) for n in wl.lengths])
+
+
+def algorithmic(wl):
+    """FLOPs (indexer, attention) and bytes per batch of the a3-a5 core, as
+    counted for the roofline: indexer sum over causal pairs of HI*DI*2,
+    attention sum over tokens of min(p+1, topk)*H*(D+Dv)*2; bytes = q, q_idx,
+    w, kv, k_idx read once, output written once, top-k indices written and read."""
+    p = positions(wl).astype(np.float64)
+    f_idx = float(np.sum(p + 1) * wl.HI * wl.DI * 2)
+    f_att = float(np.sum(np.minimum(p + 1, wl.topk)) * wl.H * (wl.D + wl.Dv) * 2)
+    T = wl.num_tokens
+    per_tok = (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4 + wl.D * 2 + wl.DI * 2 + wl.H * wl.Dv * 2
+               + 2 * wl.topk * 4)
+    return f_idx, f_att, float(T * per_tok)
+
+
+def view_attention_flops(wl, cp, mode):
+    """attention FLOPs of each CP view (one kernel launch per view)"""
+    p = positions(wl)
+    _, tpr = (-(-wl.num_tokens // cp) * cp, -(-wl.num_tokens // cp))
+    out = []
+    for r in range(cp):
+        if mode == W.IN_SEQ_SPLIT:
+            g = np.arange(r * tpr, min((r + 1) * tpr, wl.num_tokens))
+        else:
+            g = np.arange(r, wl.num_tokens, cp)
+        out.append(float(np.sum(np.minimum(p[g] + 1, wl.topk)) * wl.H * (wl.D + wl.Dv) * 2))
+    return out
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def profiled_traffic():
+    """dram bytes per attention launch from the committed ncu summary, only if
+    it was taken on the current kernel source (same hash)."""
+    try:
+        h = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+        txt = open(PROFILE_FILE).read()
+        kv = dict(l.split(":", 1) for l in txt.splitlines() if l.startswith(("traffic_bytes_per_launch:",
+                                                                              "kernel_source_sha256_16:")))
+        if kv.get("kernel_source_sha256_16", "").strip() == h:
+            return float(kv["traffic_bytes_per_launch"].strip())
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+
+def oracle_rows(wl, mode, n_seconds, seed=123, max_rows=None):
+    """Time the fp64 oracle on a seeded sample of query rows drawn uniformly
+    from all CP views of the workload; returns (rows, seconds, description)."""
+    from oracle import dsa_oracle as O
+    T = wl.num_tokens
+    rng = np.random.default_rng(seed)
+    # inputs: the oracle needs every key row but only the sampled query rows
+    gen = torch.Generator().manual_seed(wl.seed + 1000)
+    kv = torch.randn((T, wl.D), generator=gen).to(torch.bfloat16).to(torch.float64).numpy()
+    k_idx = torch.randn((T, wl.DI), generator=gen).to(torch.bfloat16).to(torch.float64).numpy()
+    sink = torch.randn(wl.H, generator=gen).numpy().astype(np.float64) if wl.sink else None
+    qsl = wl.query_start_loc()
+    cp = wl.cp_size
+    mds = [O.build_local_metadata(qsl, wl.seq_lens(), cp, r, mode) for r in range(cp)]
+    rows, t_total = 0, 0.0
+    order = rng.permutation(T)
+    for g in order:
+        g = int(g)
+        q = torch.randn((wl.H, wl.D), generator=gen).to(torch.bfloat16).to(torch.float64).numpy()
+        qi = torch.randn((wl.HI, wl.DI), generator=gen).to(torch.bfloat16).to(torch.float64).numpy()
+        w = (torch.randn(wl.HI, generator=gen) * wl.w_std).numpy().astype(np.float64)
+        r = next(rr for rr in range(cp) if g in mds[rr]["local_token_pos"])
+        i = mds[r]["local_token_pos"].index(g)
+        t0 = time.perf_counter()
+        md = mds[r]
+        q_loc = {i: q}
+        qi_loc = {i: qi}
+        w_loc = {i: w}
+        O.view_row(md, i, q_loc, qi_loc, w_loc, kv, k_idx, wl.topk, wl.scale, wl.Dv, sink)
+        t_total += time.perf_counter() - t0
+        rows += 1
+        if t_total >= n_seconds or (max_rows and rows >= max_rows):
+            break
+    desc = (f"{rows} query rows drawn uniformly from all {cp} views of {wl.name}; per row: indexer over its "
+            f"causal keys, top-{wl.topk}, attention of {wl.H} heads, fp64 numpy")
+    return rows, t_total, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl, mode, rank):
+    if rank != 0:
+        return
+    per_step = []
+    rows_total = 0
+    for s in range(args.warmup + args.steps):
+        rows, secs, desc = oracle_rows(wl, mode, n_seconds=max(2.0, args.cpu_seconds / max(1, args.steps)),
+                                       seed=1000 + s)
+        if s >= args.warmup:
+            per_step.append(secs)
+            rows_total += rows
+    value = rows_total / sum(per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(per_step),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, mode),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, mode):
+    return {"workload": wl.name, "lengths": list(wl.lengths) if len(wl.lengths) <= 16 else len(wl.lengths),
+            "num_tokens": wl.num_tokens, "cp_size": wl.cp_size, "mode": W.MODE_NAMES[mode], "heads": wl.H,
+            "latent_dim": wl.D, "value_dim": wl.Dv, "indexer_heads": wl.HI, "indexer_dim": wl.DI, "topk": wl.topk,
+            "sink": wl.sink, "l2": "flushed between steps (256 MiB write) and per-step inputs > L2"}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, wl, mode, rank, world):
+    import sparse_attention_prefill_cp_gb300 as dsa
+    from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dsa.load()
+    x = W.draw_inputs(wl, device=dev, seed_offset=rank)
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # attention launches timed live with events on the launching stream
+    attn_events = []
+    orig_view = pipe.view
+
+    def timed_view(r, kv, k_idx, sink=None, stream=None):
+        dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], k_idx, pipe.w_split[r], pipe.topk, pipe.max_kv_len,
+                             pipe.topk_idx[r], pipe.workspace, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(torch.cuda.current_stream())
+        dsa.dsa_sparse_attn_prefill(pipe.md[r], pipe.q_split[r], kv, pipe.topk_idx[r], pipe.scale, pipe.Dv, sink,
+                                    pipe.out_split[r], stream)
+        e1.record(torch.cuda.current_stream())
+        if recording[0]:
+            attn_events.append((r, e0, e1))
+
+    recording = [False]
+    pipe.view = timed_view
+
+    def step(events=None):
+        return pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"], events=events)
+
+    for _ in range(args.warmup):
+        step()
+    dsa.dsa_poll_device_error()
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    recording[0] = True
+    step_ms, core_ms = [], []
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()  # evict L2 between steps (outside the timed events)
+        ev = {k: torch.cuda.Event(enable_timing=True) for k in ("start", "core_start", "core_end", "end")}
+        step(ev)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    recording[0] = False
+    for ev in evs:
+        step_ms.append(ev["start"].elapsed_time(ev["end"]))
+        core_ms.append(ev["core_start"].elapsed_time(ev["core_end"]))
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    dsa.dsa_poll_device_error()
+    t_rank = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([t_rank], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_rank = float(t.item())
+
+    # dominant kernel: the attention launches
+    per_view_flops = view_attention_flops(wl, wl.cp_size, mode)
+    attn_ms = [e0.elapsed_time(e1) for (_, e0, e1) in attn_events]
+    attn_flops = [per_view_flops[r] for (r, _, _) in attn_events]
+    pk = peaks()
+    achieved = (sum(attn_flops) / (sum(attn_ms) / 1e3)) / 1e12
+
+    # end to end: pinned host inputs in, output out, through the same public calls
+    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
+    out_host = torch.empty((wl.num_tokens, wl.H, wl.Dv), dtype=torch.bfloat16).pin_memory()
+    dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = []
+    for s in range(1 + args.e2e_steps):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k, v in host.items():
+            if v is not None:
+                dev_in[k].copy_(v, non_blocking=True)
+        out = pipe.run(dev_in["q"], dev_in["kv"], dev_in["q_idx"], dev_in["k_idx"], dev_in["w"], dev_in["sink"])
+        out_host.copy_(out, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if s > 0:
+            e2e_ms.append(e0.elapsed_time(e1))
+    dsa.dsa_poll_device_error()
+
+    launches = pipe.launches_per_step() * args.steps
+    if rank != 0:
+        return
+    f_idx, f_att, bytes_core = algorithmic(wl)
+    total_tokens = world * args.steps * wl.num_tokens
+    value = total_tokens / t_rank
+    roof_s = max((f_idx + f_att) / (pk["bf16_tflops_sustained"] * 1e12), bytes_core / (pk["hbm_gbs"] * 1e9))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_rank / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 inputs, shapes of the workload)",
+        "config": config_of(wl, mode),
+        "roofline": {"bound": "tensor", "kernel": "sparse_attn_kernel", "achieved": achieved,
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
+                     "peak_source": f"{pk['source']} bf16 sustained", "traffic": profiled_traffic(),
+                     "launch_ms": statistics.mean(attn_ms), "flops_per_launch": statistics.mean(attn_flops)},
+        "core": {"what": "a3-a5 (indexer + top-k + sparse attention, all views)",
+                 "ms_per_step": statistics.mean(core_ms), "value": wl.num_tokens / (statistics.mean(core_ms) / 1e3),
+                 "roofline_frac": roof_s / (statistics.mean(core_ms) / 1e3),
+                 "roofline_ms": roof_s * 1e3, "flops": f_idx + f_att},
+        "e2e": {"value": wl.num_tokens / (statistics.mean(e2e_ms) / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+        "clocks": clocks,
+        "gpu_launches": launches,
+    }
+    if not args.no_cpu_baseline:
+        rows, secs, desc = oracle_rows(wl, mode, n_seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rows / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    wl = W.ALL[args.workload]
+    mode = wl.modes[0] if args.mode is None else (W.IN_SEQ_SPLIT if args.mode == "in-seq" else W.ROUND_ROBIN)
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, wl, mode, rank)
+        else:
+            run_ours(args, wl, mode, rank, world)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -48,6 +48,15 @@ class DSAPrefill:
         ws = workspace_bytes or dsa_indexer_topk_workspace_size(tpr, self.max_kv_len, topk)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
+    def launches_per_step(self) -> int:
+        """Kernel launches of one ``run``: metadata per view, 3 splits, per view
+        (indexer + top-k) per workspace chunk and one attention, 1 rerange."""
+        ld = (self.max_kv_len + 3) // 4 * 4
+        tile = 8 if self.HI == 64 else 128
+        rows_fit = (self.workspace.numel() // (ld * 4)) // tile * tile
+        chunks = -(-self.tpr // rows_fit)
+        return self.cp_size + 3 + self.cp_size * (2 * chunks + 1) + 1
+
     def metadata(self, stream=None):                                     # a1
         for r in range(self.cp_size):
             dsa_cp_build_local_metadata(self.query_start_loc, self.seq_lens, self.T, self.cp_size, r, self.mode,
