@@ -192,6 +192,35 @@ dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int3
                             void *workspace, size_t ws_bytes, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_topk without a workspace argument, for callers that cannot
+ * allocate device memory where they call it (inside an allocator or memory
+ * pool callback, in a runtime whose memory is all owned by a pool, or from
+ * a framework hook that must not call cudaMalloc).  The pages have no
+ * counterpart; this is a deployment convenience.  Same inputs, outputs and
+ * results as dsa_indexer_topk; the score workspace is a fixed 32 MiB array
+ * inside the library (static device memory, held by every GPU that loads the
+ * library until the process exits).  It allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library call.
+ *   - Limit: the array must hold one query tile of scores, so
+ *     max_kv_len <= 1,048,576 for the DeepSeek-V3.2 shapes (8-query tiles)
+ *     and <= 65,536 for the tiny shapes (128-query tiles); larger values
+ *     return DSA_ERR_WORKSPACE without launching.  Rows beyond what fits in
+ *     one pass are processed in several passes over the same array.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps whatever the
+ *     last call left in it.  Nothing needs to start at zero: each pass writes
+ *     every score it later reads.  Calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race on the array and give wrong
+ *     results: serialise them.
+ */
+dsa_status dsa_indexer_topk_noalloc(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                    int32_t max_kv_len, const void *q_idx, const void *k_idx,
+                                    const float *w, int32_t num_tokens, int32_t HI, int32_t DI,
+                                    int32_t topk, int32_t *topk_idx, dsa_stream_t stream);
+
+/*
  * Test hook: the indexer scores themselves for local slots
  * [row_begin, row_begin + row_count): scores [row_count][max_kv_len] fp32,
  * entry s of a row = I[i, s] for s <= p, -inf for s > p and for pad slots.

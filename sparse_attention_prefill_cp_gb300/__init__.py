@@ -179,6 +179,31 @@ def dsa_indexer_topk(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Tens
     return out
 
 
+def dsa_indexer_topk_noalloc(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor,
+                             topk: int, max_kv_len: int, out: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """dsa_indexer_topk for callers that cannot allocate device memory at the
+    call site: the score workspace is the library's fixed 32 MiB device array.
+    ``out`` should be passed pre-allocated by such callers (when omitted it is
+    allocated here, for convenience in tests).  Calls that overlap on the GPU
+    share that array and race; the first call on a device should come before
+    any stream capture."""
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(k_idx, torch.bfloat16, "k_idx")
+    _need(w, torch.float32, "w")
+    tpr, HI, DI = q_idx.shape
+    if tpr != md.tokens_per_rank or tuple(w.shape) != (tpr, HI) or k_idx.shape[1] != DI:
+        raise ValueError("q_idx / w / k_idx shapes do not match the view")
+    if out is None:
+        out = torch.empty((tpr, topk), dtype=torch.int32, device=q_idx.device)
+    _need(out, torch.int32, "out")
+    check(load().dsa_indexer_topk_noalloc(C.byref(md.struct), md.batch, tpr, max_kv_len, _ptr(q_idx),
+                                          _ptr(k_idx), _ptr(w), k_idx.shape[0], HI, DI, topk, _ptr(out),
+                                          _stream(stream)),
+          "dsa_indexer_topk_noalloc")
+    return out
+
+
 def dsa_indexer_scores(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor,
                        max_kv_len: int, row_begin: int = 0, row_count: int | None = None,
                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -38,6 +38,9 @@ SIGNATURES = {
     "dsa_indexer_topk": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                    C.c_void_p, C.c_size_t, c_stream]),
+    "dsa_indexer_topk_noalloc": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+                                           C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                           C.c_void_p, c_stream]),
     "dsa_indexer_scores": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                      C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                      C.c_void_p, c_stream]),

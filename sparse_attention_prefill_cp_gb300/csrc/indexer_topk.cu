@@ -20,6 +20,8 @@
 // topk-th largest score (scores mapped to order-preserving uint32 keys, -0
 // folded into +0), then a block-scan compaction in ascending key order that
 // takes every score above the threshold and the lowest-index ties.
+#include <mutex>
+
 #include "dsa_common.cuh"
 #include "internal.h"
 
@@ -556,4 +558,67 @@ extern "C" dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_
   if (st != DSA_OK) return st;
   return big ? run_scores<BigIdx>(a, row_begin, row_begin + row_count, scores, max_kv_len, s)
              : run_scores<TinyIdx>(a, row_begin, row_begin + row_count, scores, max_kv_len, s);
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+// Some callers cannot allocate device memory at the point where they run the
+// indexer: code inside a custom allocator or memory-pool callback, a runtime
+// that has already handed all its memory to a pool, or a framework hook that
+// must not call cudaMalloc.  For them dsa_indexer_topk_noalloc takes its score
+// workspace from this fixed array instead of a caller buffer.  The array is
+// part of the library image: every GPU that loads the library holds these
+// 32 MiB until the process exits.
+namespace dsa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+static void *s_scratch_ptr[kMaxScratchDevices];
+static std::mutex s_scratch_mutex;
+
+// Device address of g_static_scratch on the current device.  In host code the
+// symbol's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached; no memory is allocated.
+dsa_status static_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxScratchDevices) return cuda_fail_msg("device index beyond the scratch table");
+  std::lock_guard<std::mutex> lock(s_scratch_mutex);
+  if (!s_scratch_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    s_scratch_ptr[dev] = p;
+  }
+  *out = s_scratch_ptr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_indexer_topk_noalloc(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                               int32_t max_kv_len, const void *q_idx, const void *k_idx,
+                                               const float *w, int32_t num_tokens, int32_t HI, int32_t DI,
+                                               int32_t topk, int32_t *topk_idx, dsa_stream_t stream) {
+  Args a{md, batch, tpr, max_kv_len, num_tokens, HI, DI, q_idx, k_idx, w};
+  dsa_status st = validate(a);
+  if (st != DSA_OK) return st;
+  if (!topk_idx) return DSA_ERR_INVALID_ARG;
+  const bool big = HI == 64 && DI == 128 && topk == 2048, tiny = HI == 4 && DI == 32 && topk == 64;
+  if (!big && !tiny) return DSA_ERR_UNSUPPORTED;
+  // the fixed array must hold the scores of at least one query tile
+  const size_t row_bytes = static_cast<size_t>((static_cast<int64_t>(max_kv_len) + 3) / 4 * 4) * 4;
+  const size_t tile = big ? BigIdx::kTileTok : TinyIdx::kTileTok;
+  if (row_bytes * tile > kStaticScratchBytes) return DSA_ERR_WORKSPACE;
+  if (tpr == 0) return DSA_OK;
+  void *scratch = nullptr;
+  st = static_scratch(&scratch);
+  if (st != DSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return big ? run_topk<BigIdx, 2048>(a, topk_idx, scratch, kStaticScratchBytes, s)
+             : run_topk<TinyIdx, 64>(a, topk_idx, scratch, kStaticScratchBytes, s);
 }
