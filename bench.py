@@ -249,6 +249,15 @@ def config_of(wl, mode):
 
 # ------------------------------------------------------------------ GPU arm
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, wl, mode, rank, world):
     import sparse_attention_prefill_cp_gb300 as dsa
     from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill
@@ -310,11 +319,7 @@ def run_ours(args, wl, mode, rank, world):
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
     dsa.dsa_poll_device_error()
-    t_rank = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([t_rank], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_rank = float(t.item())
+    t_rank = max_over_ranks(sum(step_ms) / 1e3, world, dev)
 
     # dominant kernel: the attention launches
     per_view_flops = view_attention_flops(wl, wl.cp_size, mode)
@@ -330,7 +335,7 @@ def run_ours(args, wl, mode, rank, world):
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = out_host.numel() * out_host.element_size()
     e2e_ms = []
-    for s in range(1 + args.e2e_steps):
+    for s in range(1 + max(1, args.e2e_steps)):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
