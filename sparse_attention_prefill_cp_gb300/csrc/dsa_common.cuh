@@ -90,48 +90,53 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+// try_wait with an explicit suspend-time hint: the thread may sleep until the
+// phase completes or about 20 us pass, whichever comes first.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_hint_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Polls with
-// the non-blocking test_wait; after a short spin it backs off with
-// nanosleep and checks the error record every iteration, so a stuck pipeline
-// anywhere on the GPU drains quickly.  Returns false (after recording
-// DSA_ERR_DEVICE_TIMEOUT with `site` / `detail`, or when another thread
-// already recorded an error) instead of spinning forever.
+// Bounded wait for the phase with the given parity to complete.  The fast
+// path is the hardware try_wait; only every ~100K cycles does the loop look at
+// the error record (another thread gave up: return) and at its own time
+// limit (record DSA_ERR_DEVICE_TIMEOUT with `site` / `detail` and return
+// false), so a waiter notices its phase completing without a memory round
+// trip, and a stuck pipeline still drains within about a second.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int site = 0,
                                           int detail = 0) {
-  for (int n = 0; n < 256; ++n)
-    if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
+  if (kCluster ? mbar_try_wait_hint_cluster(bar, parity) : mbar_try_wait_hint(bar, parity)) return true;
   const long long t0 = clock64();
+  long long t_check = t0;
   while (true) {
-    if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
-    if (error_set(err)) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      record_error(err, DSA_ERR_DEVICE_TIMEOUT, site, detail);
-      return false;
+    if (kCluster ? mbar_try_wait_hint_cluster(bar, parity) : mbar_try_wait_hint(bar, parity)) return true;
+    const long long now = clock64();
+    if (now - t_check > 100000) {
+      if (error_set(err)) return false;
+      if (now - t0 > kWaitLimitCycles) {
+        record_error(err, DSA_ERR_DEVICE_TIMEOUT, site, detail);
+        return false;
+      }
+      t_check = now;
     }
-    __nanosleep(64);
   }
 }
 
@@ -179,6 +184,69 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       "%4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+// tile::gather4: four arbitrary rows (y0..y3) of a 2D tensor map whose box is
+// one row high, written to smem as four consecutive box rows (swizzled by the
+// destination address like a 4-row box).
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int32_t x, int4 rows,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4_b32(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   raddr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
+               : "memory");
+}
+
+// Arrive (relaxed) on the barrier at the same smem offset in CTA `cta_rank`:
+// for signals that carry no data (e.g. "buffer consumed" after the loads'
+// values were already used).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint64_t *bar, uint32_t cta_rank) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
+      "r"(cta_rank)
+      : "memory");
+}
+
+// Bulk copy from this CTA's shared memory to a peer CTA's shared memory,
+// completing `bytes` of transaction count on the peer's mbarrier (both peer
+// addresses are shared::cluster addresses from mapa).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Asynchronous 16-byte store into a peer CTA's shared memory that signals the
+// peer's mbarrier (complete_tx) when it lands; both addresses are
+// shared::cluster addresses (mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   raddr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+               : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

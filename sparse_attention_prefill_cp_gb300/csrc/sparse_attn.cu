@@ -14,16 +14,27 @@
 // [256c, 256c + 256) + [512 + 32c, 512 + 32c + 32): the gathered rows split
 // evenly (576 bytes per CTA per row, no row read twice) and the value
 // columns are exactly the CTA's main QK chunks, so one smem tile serves as
-// QK's K-major B and PV's MN-major B.  The partial S tiles are exchanged
-// through distributed shared memory and summed (a + b == b + a bitwise, so
-// both CTAs hold the same S and take the same softmax decisions).
+// QK's K-major B and PV's MN-major B.
 //
-// Per CTA, 10 warps: 0-3 softmax (one head row = one TMEM lane per thread),
-// 4 MMA issue + TMEM owner, 5 Q TMA, 6-9 row gather (cp.async, 128B/64B
-// swizzle written directly).  Key blocks of 64 rows, 3 smem stages; two S
-// buffers in TMEM, P (bf16) written over its S buffer and fed to the PV MMA
-// from TMEM.  The running max is rescaled lazily: O and l are rescaled only
-// when a block's max exceeds the max in use by more than 2^8.
+// Tensor memory per CTA (512 columns): O (256), two S buffers (2 x 64) and
+// the CTA's 256 main Q dims as bf16 (128), so the QK MMA reads A from TMEM
+// and only the 64-row key block from shared memory.
+//
+// Per CTA, 14 warps: 0-7 softmax in two warpgroups (one head row = one TMEM
+// lane per thread; warpgroup w owns columns [32w, 32w + 32) of each block),
+// 8 MMA issue + TMEM owner, 9 TMA for Q and the index row, then exchange agent,
+// 10-13 gather of the selected rows with 16-byte cp.async straight into the
+// 128B / 64B swizzled tiles (two groups on alternate blocks).  Key blocks of
+// 64 rows, 3 smem stages.  The partial S tiles are exchanged rounded to bf16:
+// the softmax threads stage their rows locally and warp 9 ships each tile to
+// the peer's double-buffered receive tiles with one bulk copy that completes
+// the peer's mbarrier transaction count, one block ahead of the softmax that
+// needs it.  Each CTA softmaxes its own
+// fp32 partial plus the peer's bf16 one and normalises its own O half.  P (bf16) goes to a shared-memory
+// tile, so an S buffer is free as soon as it has been read and QK runs two
+// blocks ahead of PV.  The running max is rescaled lazily: O and l change
+// only when some row of a warp sees its block max exceed the max in use by
+// more than 2^8.
 //
 // The tiny shapes (H = 8, D = 64, Dv = 48) run the same kernel on one CTA
 // with Q rows 8..127 zero-filled by the TMA.
@@ -40,32 +51,48 @@ struct AttnCfg {
   static constexpr int DVC = DVC_;      // value columns per CTA
   static constexpr bool SPLIT = SPLIT_; // 2-CTA cluster per token
   static constexpr int kBN = 64;        // selected rows per block
+  static constexpr int kHalf = kBN / 2; // columns per softmax warpgroup
   static constexpr int kStages = 3;
-  static constexpr int kThreads = 320;
+  // warps: 0-7 softmax (two warpgroups), 8 MMA + TMEM, 9 TMA (Q, index row), 10-13 row gather
+  static constexpr int kThreads = 448;
   static constexpr int kQMain = NMAIN * 128 * 128;
   static constexpr int kQTail = TAIL ? 128 * 64 : 0;
   static constexpr int kStageMain = NMAIN * kBN * 128;
   static constexpr int kStageBytes = kStageMain + (TAIL ? kBN * 64 : 0);
-  static constexpr int kUnitsPerRow = NMAIN * 8 + (TAIL ? 4 : 0);  // 16-byte pieces
-  static constexpr int kQKSteps = NMAIN * 4 + (TAIL ? 2 : 0);
+  static constexpr int kUnitsPerRow = NMAIN * 8 + (TAIL ? 4 : 0);  // 16-byte pieces per gathered row
+  static constexpr int kQKMainSteps = NMAIN * 4;
+  static constexpr int kQKSteps = kQKMainSteps + (TAIL ? 2 : 0);
   static constexpr int kPVSteps = kBN / 16;
+  // tensor memory columns
   static constexpr int kOCols = (DVC + 63) / 64 * 64;
-  static constexpr int kSCol = kOCols;  // S / P buffers after O
-  static constexpr int kTmemCols = (kOCols + 2 * kBN) <= 256 ? 256 : 512;
-  static constexpr int kRecvStride = 68;  // floats per head row (padded against bank conflicts)
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffStage = kOffQ + kQMain + kQTail;
-  static constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
-  static constexpr int kOffBar = kOffRecv + (SPLIT ? 128 * kRecvStride * 4 : 0);
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2;
+  static constexpr int kSCol = kOCols;              // two S buffers
+  static constexpr int kQCol = kSCol + 2 * kBN;     // Q main dims, bf16 pairs
+  static constexpr int kTmemCols = (kQCol + NMAIN * 32) <= 256 ? 256 : 512;
+  // shared memory
+  static constexpr int kRecvBytes = SPLIT ? 128 * kBN * 2 : 0;  // one partial-S tile (bf16), rows swizzled
+  static constexpr int kPBytes = 128 * 128;                     // P tile [128 heads][64 keys] bf16, SW128
+  static constexpr int kIdxBytes = 2048 * 4;
+  static constexpr int kOffStage = 0;
+  static constexpr int kOffQStage = kOffStage + kStageBytes;  // Q main staged in stages 1..2 at start
+  static constexpr int kOffQTail = kOffStage + kStages * kStageBytes;
+  static constexpr int kOffRecv = kOffQTail + kQTail;
+  static constexpr int kOffStg = kOffRecv + 2 * kRecvBytes;   // our partial-S tiles on their way out
+  static constexpr int kOffP = kOffStg + 2 * kRecvBytes;
+  static constexpr int kOffIdx = kOffP + 2 * kPBytes;
+  static constexpr int kOffRed = kOffIdx + kIdxBytes;         // [3][2 warpgroups][128] floats
+  static constexpr int kOffBar = kOffRed + 3 * 2 * 128 * 4;
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 * 10 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 32 + 1024;
   // the tiny variant asks for enough smem that at most two CTAs share an SM's TMEM
   static constexpr int kSmemBytes = kSmemUsed < 100 * 1024 && !SPLIT ? 100 * 1024 : kSmemUsed;
   static constexpr uint32_t kIdescQK = idesc_bf16(128, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(128, DVC, false, true);
-  static_assert(kOCols + 2 * kBN <= kTmemCols, "TMEM budget");
+  static constexpr uint32_t kRecvTx = 128 * kBN * 2;
+  static_assert(kQCol + NMAIN * 32 <= kTmemCols, "TMEM budget");
   static_assert(DVC % 16 == 0 && DVC <= NMAIN * 64, "value columns inside the main chunks");
+  static_assert(kQMain <= 2 * kStageBytes, "Q staging fits in stages 1..2");
+  static_assert(kStageBytes % 1024 == 0 && kOffQTail % 1024 == 0 && kOffP % 1024 == 0, "alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -96,16 +123,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-  uint64_t *q_full = bars;
-  uint64_t *kv_full = q_full + 1;
-  uint64_t *kv_empty = kv_full + C::kStages;
-  uint64_t *s_full = kv_empty + C::kStages;
-  uint64_t *p_full = s_full + 2;
-  uint64_t *pv_done = p_full + 2;
-  uint64_t *recv_full = pv_done + 2;
-  uint64_t *recv_empty = recv_full + 1;
+  uint64_t *q_full = bars;                     // Q staged + tail + index row landed (TMA)
+  uint64_t *q_ready = bars + 1;                // Q main copied into TMEM, staging free (256 softmax threads)
+  uint64_t *kv_full = bars + 2;                // [kStages] gathered rows landed (64 gather threads)
+  uint64_t *kv_empty = kv_full + C::kStages;   // [kStages] PV done with the stage (MMA commit)
+  uint64_t *s_full = kv_empty + C::kStages;    // [2] QK done (MMA commit)
+  uint64_t *s_free = s_full + 2;               // [2] S read out of TMEM (256 softmax threads)
+  uint64_t *p_full = s_free + 2;               // [2] P tile written (256 softmax threads)
+  uint64_t *pv_done = p_full + 2;              // [2] PV done, P tile free (MMA commit)
+  uint64_t *recv_full = pv_done + 2;           // [2] the peer's partial S landed (st.async tx)
+  uint64_t *recv_empty = recv_full + 2;        // [2] the peer consumed what we sent (peer's agent)
+  uint64_t *red_full = recv_empty + 2;         // [2] both warpgroups' block maxima written (256)
+  uint64_t *staged = red_full + 2;             // [2] our partial-S tile written (256 softmax threads)
+  uint64_t *stg_free = staged + 2;             // [2] the bulk copy has read our tile (sender)
+  uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (256 softmax threads)
+  uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (256)
   int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p
-  float *recv = reinterpret_cast<float *>(smem + C::kOffRecv);
+  const int32_t *idx_s = reinterpret_cast<const int32_t *>(smem + C::kOffIdx);
+  float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = C::SPLIT ? cluster_ctarank() : 0u;
@@ -117,9 +152,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (tid == 0) {
     int base = 0, p = -1;
     const int g = P.md.local_token_pos[slot];
-    const int nb = P.md.scalars[DSA_MD_LOCAL_BATCH];
-    if (g >= 0 && nb > 0) {
-      const int j = find_local_request(P.md.local_query_start_loc, nb, slot);
+    const int nbatch = P.md.scalars[DSA_MD_LOCAL_BATCH];
+    if (g >= 0 && nbatch > 0) {
+      const int j = find_local_request(P.md.local_query_start_loc, nbatch, slot);
       base = P.md.local_req_kv_base[j];
       p = g - base;
       if (p < 0 || g >= P.num_tokens) {
@@ -130,20 +165,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     misc[1] = base;
     misc[2] = p;
     mbar_init(q_full, 1);
+    mbar_init(q_ready, 256);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&kv_full[s], 64);
       mbar_init(&kv_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 128);
+      mbar_init(&s_free[b], 256);
+      mbar_init(&p_full[b], 256);
       mbar_init(&pv_done[b], 1);
+      mbar_init(&recv_full[b], 1);
+      mbar_init(&recv_empty[b], 1);
+      mbar_init(&red_full[b], 256);
+      mbar_init(&staged[b], 256);
+      mbar_init(&stg_free[b], 1);
+      mbar_init(&consumed[b], 256);
     }
-    mbar_init(recv_full, 128);
-    mbar_init(recv_empty, 128);
+    mbar_init(fin_full, 256);
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(reinterpret_cast<uint32_t *>(&misc[0]), C::kTmemCols);
     tmem_relinquish();
   }
@@ -162,91 +204,125 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // pad slot: zero output rows
     if (warp < 4 && tid < P.H) {
       __nv_bfloat16 *o = out_row + static_cast<int64_t>(tid) * P.Dv;
-      for (int c = 0; c < C::DVC; ++c) o[c] = __float2bfloat16(0.f);
+      for (int c = 0; c < C::DVC; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
     }
-  } else if (warp == 5) {
-    // ---------------- Q tile by TMA (rows beyond H arrive as zeros)
+  } else if (warp == 9) {
+    // ---------------- TMA: Q (main dims to a staging tile, tail dims in place) and the index row
     if (lane == 0) {
       tma_prefetch_desc(&qmain_map);
-      mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail);
+      const uint32_t idx_bytes = static_cast<uint32_t>(P.topk) * 4;
+      mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail + idx_bytes);
       for (int i = 0; i < C::NMAIN; ++i)
-        tma_load_3d(smem + C::kOffQ + i * 128 * 128, &qmain_map, main_dim0 + 64 * i, 0, slot, q_full);
-      if (C::TAIL) tma_load_3d(smem + C::kOffQ + C::kQMain, &qtail_map, tail_dim0, 0, slot, q_full);
-      mbar_wait(q_full, 0, P.err, 21);
-    }
-  } else if (warp >= 6) {
-    // ---------------- gather of the selected rows: two groups of 64 threads take
-    // alternate blocks, one selected row per thread
-    const int ptid = tid - 192;
-    const int group = ptid >> 6, r = ptid & 63;
-    const int32_t *idx_row = P.topk_idx + static_cast<int64_t>(slot) * P.topk;
-    for (int j = group; j < nb; j += 2) {
-      const int s = j % C::kStages;
-      if (!mbar_wait(&kv_empty[s], ((j / C::kStages) & 1) ^ 1, P.err, 22, j)) break;
-      const int k = j * C::kBN + r;
-      int row = k < n_valid ? __ldg(idx_row + k) : -1;
-      if (k < n_valid && (row < 0 || row >= P.num_tokens)) {
-        record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, k);
-        row = -1;
-      }
-      const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
-      const uint32_t nbytes = row < 0 ? 0u : 16u;
-      const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-#pragma unroll
-      for (int u = 0; u < C::kUnitsPerRow; ++u) {
-        if (u < C::NMAIN * 8) {
-          const int i = u >> 3, v = u & 7;
-          cp_async_16(sb + i * (C::kBN * 128) + r * 128 + ((v ^ (r & 7)) << 4), src + main_dim0 + i * 64 + v * 8,
-                      nbytes);
-        } else {
-          const int v = u - C::NMAIN * 8;
-          cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + tail_dim0 + v * 8, nbytes);
+        tma_load_3d(smem + C::kOffQStage + i * 16384, &qmain_map, main_dim0 + 64 * i, 0, slot, q_full);
+      if (C::TAIL) tma_load_3d(smem + C::kOffQTail, &qtail_map, tail_dim0, 0, slot, q_full);
+      bulk_load(smem + C::kOffIdx, P.topk_idx + static_cast<int64_t>(slot) * P.topk, idx_bytes, q_full);
+      bool ok = mbar_wait(q_full, 0, P.err, 21);
+      if (C::SPLIT) {
+        // ---------------- exchange agent: ships each staged partial-S tile to the
+        // peer with one bulk copy, and tells the peer when its tiles have been read
+        const uint32_t peer_recv = map_to_cta(smem_u32(smem + C::kOffRecv), peer);
+        const uint32_t peer_full = map_to_cta(smem_u32(recv_full), peer);
+        for (int t = 0; ok && t <= nb; ++t) {
+          if (t < nb) {
+            const int b = t & 1;
+            if (!(ok = mbar_wait(&staged[b], (t >> 1) & 1, P.err, 35, t))) break;
+            if (t >= 2 && !(ok = mbar_wait<true>(&recv_empty[b], ((t >> 1) & 1) ^ 1, P.err, 28, t))) break;
+            bulk_copy_to_peer(peer_recv + b * C::kRecvBytes, smem + C::kOffStg + b * C::kRecvBytes, C::kRecvBytes,
+                              peer_full + b * 8);
+            bulk_commit();
+            bulk_wait_read0();
+            mbar_arrive(&stg_free[b]);
+          }
+          if (t >= 1) {
+            const int b = (t - 1) & 1;
+            if (!(ok = mbar_wait(&consumed[b], ((t - 1) >> 1) & 1, P.err, 36, t - 1))) break;
+            mbar_arrive_remote_relaxed(&recv_empty[b], peer);
+          }
         }
+        bulk_wait_read0();
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(&kv_full[s]);
+    }
+  } else if (warp >= 10) {
+    // ---------------- gather of the selected rows: two groups of 64 threads take
+    // alternate blocks, one selected row per thread, 16-byte cp.async pieces
+    // written straight into the 128B / 64B swizzled tiles
+    const int ptid = tid - 320;
+    const int group = ptid >> 6, r = ptid & 63;
+    if (mbar_wait(q_full, 0, P.err, 21)) {
+      for (int j = group; j < nb; j += 2) {
+        const int s = j % C::kStages;
+        if (!mbar_wait(&kv_empty[s], ((j / C::kStages) & 1) ^ 1, P.err, 22, j)) break;
+        // stages 1 and 2 held the staged Q until the softmax warps moved it to TMEM
+        if ((j == 1 || j == 2) && !mbar_wait(q_ready, 0, P.err, 20, j)) break;
+        const int k = j * C::kBN + r;
+        int row = k < n_valid ? idx_s[k] : -1;
+        if (k < n_valid && (row < 0 || row >= P.num_tokens)) {
+          record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, k);
+          row = -1;
+        }
+        const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
+        const uint32_t nbytes = row < 0 ? 0u : 16u;
+        const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+#pragma unroll
+        for (int u = 0; u < C::kUnitsPerRow; ++u) {
+          if (u < C::NMAIN * 8) {
+            const int i = u >> 3, v = u & 7;
+            cp_async_16(sb + i * (C::kBN * 128) + r * 128 + ((v ^ (r & 7)) << 4), src + main_dim0 + i * 64 + v * 8,
+                        nbytes);
+          } else {
+            const int v = u - C::NMAIN * 8;
+            cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + tail_dim0 + v * 8,
+                        nbytes);
+          }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(&kv_full[s]);
+      }
     }
     cp_async_wait<0>();
-  } else if (warp == 4) {
-    // ---------------- MMA issuer
+  } else if (warp == 8) {
+    // ---------------- MMA issuer (one thread): QK runs two blocks ahead of PV
     if (lane == 0) {
-      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
       const uint32_t st_addr = smem_u32(smem + C::kOffStage);
-      bool ok = mbar_wait(q_full, 0, P.err, 23);
-      for (int j = 0; ok && j <= nb; ++j) {
+      const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
+      const uint32_t p_addr = smem_u32(smem + C::kOffP);
+      bool ok = mbar_wait(q_full, 0, P.err, 23) && mbar_wait(q_ready, 0, P.err, 23);
+      tc_fence_after();
+      for (int j = 0; ok && j < nb + 2; ++j) {
         if (j < nb) {
           const int s = j % C::kStages, b = j & 1;
           if (!(ok = mbar_wait(&kv_full[s], (j / C::kStages) & 1, P.err, 24, j))) break;
-          if (j >= 2 && !(ok = mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, P.err, 25, j))) break;
+          if (j >= 2 && !(ok = mbar_wait(&s_free[b], ((j - 2) >> 1) & 1, P.err, 25, j))) break;
           tc_fence_after();
           const uint32_t kb = st_addr + s * C::kStageBytes;
 #pragma unroll
           for (int k = 0; k < C::kQKSteps; ++k) {
-            uint64_t a, bd;
-            if (k < C::NMAIN * 4) {
+            if (k < C::kQKMainSteps) {
               const int i = k >> 2, sub = k & 3;
-              a = smem_desc(q_addr + i * 16384 + sub * 32, 16, 1024, kLayoutSW128);
-              bd = smem_desc(kb + i * (C::kBN * 128) + sub * 32, 16, 1024, kLayoutSW128);
+              const uint64_t bd = smem_desc(kb + i * (C::kBN * 128) + sub * 32, 16, 1024, kLayoutSW128);
+              mma_ts(tmem + C::kSCol + b * C::kBN, tmem + C::kQCol + k * 8, bd, C::kIdescQK, k > 0 ? 1u : 0u);
             } else {
-              const int t = k - C::NMAIN * 4;
-              a = smem_desc(q_addr + C::kQMain + t * 32, 16, 512, kLayoutSW64);
-              bd = smem_desc(kb + C::kStageMain + t * 32, 16, 512, kLayoutSW64);
+              const int t = k - C::kQKMainSteps;
+              const uint64_t a = smem_desc(qt_addr + t * 32, 16, 512, kLayoutSW64);
+              const uint64_t bd = smem_desc(kb + C::kStageMain + t * 32, 16, 512, kLayoutSW64);
+              mma_ss(tmem + C::kSCol + b * C::kBN, a, bd, C::kIdescQK, 1u);
             }
-            mma_ss(tmem + C::kSCol + b * C::kBN, a, bd, C::kIdescQK, k > 0 ? 1u : 0u);
           }
           mma_commit(&s_full[b]);
         }
-        if (j >= 1) {
-          const int i = j - 1, si = i % C::kStages, bi = i & 1;
+        if (j >= 2) {
+          const int i = j - 2, si = i % C::kStages, bi = i & 1;
           if (!(ok = mbar_wait(&p_full[bi], (i >> 1) & 1, P.err, 26, i))) break;
           tc_fence_after();
           const uint32_t vb = st_addr + si * C::kStageBytes;
+          const uint32_t pb = p_addr + bi * C::kPBytes;
 #pragma unroll
           for (int k = 0; k < C::kPVSteps; ++k) {
+            const uint64_t a = smem_desc(pb + k * 32, 16, 1024, kLayoutSW128);
             const uint64_t bd = smem_desc(vb + k * 2048, C::kBN * 128, 1024, kLayoutSW128);
-            mma_ts(tmem, tmem + C::kSCol + bi * C::kBN + k * 8, bd, C::kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
+            mma_ss(tmem, a, bd, C::kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&pv_done[bi]);
           mma_commit(&kv_empty[si]);
@@ -254,68 +330,143 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
     }
   } else {
-    // ---------------- softmax: thread = head row h = TMEM lane
-    const int h = tid;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float m_used = -__builtin_huge_valf(), l = 0.f;
-    float *my_recv = recv + h * C::kRecvStride;
-    const uint32_t peer_recv = C::SPLIT ? map_to_cta(smem_u32(my_recv), peer) : 0u;
-    bool ok = true;
-    for (int i = 0; i < nb; ++i) {
-      const int b = i & 1;
-      // tcgen05.ld/st are warp-collective (.sync.aligned): every decision that
-      // guards one is made warp-uniform, including the error path
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (i >> 1) & 1, P.err, 27, i));
-      if (!ok) break;
-      tc_fence_after();
-      float x[C::kBN];
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(lane_base + C::kSCol + b * C::kBN, r0);
-        tmem_ld32(lane_base + C::kSCol + b * C::kBN + 32, r1);
-        tmem_ld_wait();
+    // ---------------- softmax: two warpgroups; thread = head row h = TMEM lane,
+    // warpgroup w owns columns [32w, 32w + 32) of every 64-row block.
+    // tcgen05.ld/st are warp-collective (.sync.aligned): every decision that
+    // guards one is made warp-uniform, including the error path.
+    const int h = tid & 127, w = tid >> 7;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, P.err, 27, -1));
+    if (ok) {
+      // Q main dims: staged rows (128B swizzle) -> TMEM as bf16 pairs, chunks split by warpgroup
+      const uint8_t *qs = smem + C::kOffQStage;
+#pragma unroll 1
+      for (int i = w; i < C::NMAIN; i += 2) {
+        uint32_t r[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          x[k] = __uint_as_float(r0[k]);
-          x[k + 32] = __uint_as_float(r1[k]);
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(qs + i * 16384 + h * 128 + ((u ^ (h & 7)) << 4));
+          r[4 * u + 0] = v.x;
+          r[4 * u + 1] = v.y;
+          r[4 * u + 2] = v.z;
+          r[4 * u + 3] = v.w;
         }
+        tmem_st32(lane_base + C::kQCol + 32 * i, r);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(q_ready);
+
+    // partial-S tile rows: 64 bf16 (128 bytes), 16-byte unit u stored at u ^ (h & 7)
+    uint8_t *recv0 = smem + C::kOffRecv;
+    // stage our 32 columns of block j's partial S row, rounded to bf16, for the
+    // exchange agent (SPLIT only).  Each CTA softmaxes its own fp32 partial plus
+    // the peer's bf16 partial and normalises its own O half with its own sum,
+    // so the two CTAs need not agree bitwise.
+    auto stage = [&](int j) {
+      const int b = j & 1;
+      uint32_t r[32];
+      tmem_ld32(lane_base + C::kSCol + b * C::kBN + w * C::kHalf, r);
+      tmem_ld_wait();
+      uint8_t *row = smem + C::kOffStg + b * C::kRecvBytes + h * 128;
+#pragma unroll
+      for (int k = 0; k < 32; k += 8) {
+        const int u = (w * C::kHalf + k) >> 3;
+        *reinterpret_cast<uint4 *>(row + ((u ^ (h & 7)) << 4)) =
+            make_uint4(pack_bf16x2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                       pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
+                       pack_bf16x2(__uint_as_float(r[k + 4]), __uint_as_float(r[k + 5])),
+                       pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
+      }
+      fence_proxy_async_smem();  // the bulk copy reads the tile through the async proxy
+      mbar_arrive(&staged[b]);
+    };
+
+    float m_used = -__builtin_huge_valf(), l = 0.f;  // m in log2 units; l over this warpgroup's columns
+    if (C::SPLIT && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[0], 0, P.err, 27, 0));
+      if (ok) {
+        tc_fence_after();
+        stage(0);
+      }
+    }
+    for (int i = 0; ok && i < nb; ++i) {
+      const int b = i & 1;
+      if (C::SPLIT && i + 1 < nb) {
+        // send block i+1 ahead: the peer has it by the time it starts block i+1
+        const int b1 = (i + 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b1], ((i + 1) >> 1) & 1, P.err, 27, i + 1) &&
+                                         mbar_wait(&stg_free[b1], (((i + 1) >> 1) & 1) ^ 1, P.err, 28, i + 1));
+        if (!ok) break;
+        tc_fence_after();
+        stage(i + 1);
       }
       if (C::SPLIT) {
-        ok = __all_sync(0xffffffffu, i == 0 || mbar_wait<true>(recv_empty, (i - 1) & 1, P.err, 28, i));
-        if (!ok) break;
+        if (tid == 0) mbar_arrive_expect_tx(&recv_full[b], C::kRecvTx);
+        ok = __all_sync(0xffffffffu, mbar_wait<true>(&recv_full[b], (i >> 1) & 1, P.err, 29, i));
+      } else {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (i >> 1) & 1, P.err, 27, i));
+      }
+      if (!ok) break;
+      tc_fence_after();
+      float x[C::kHalf];
+      {
+        uint32_t r[32];
+        tmem_ld32(lane_base + C::kSCol + b * C::kBN + w * C::kHalf, r);
+        tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < C::kBN; k += 4) st_cluster_v4(peer_recv + k * 4, x[k], x[k + 1], x[k + 2], x[k + 3]);
-        mbar_arrive_remote(recv_full, peer);
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(recv_full, i & 1, P.err, 29, i));
-        if (!ok) break;
+        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r[k]);
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[b]);  // the MMA may compute QK(i+2) into this buffer
+      if (C::SPLIT) {
+        const uint8_t *my_recv = recv0 + b * C::kRecvBytes + h * 128;
 #pragma unroll
-        for (int k = 0; k < C::kBN; k += 4) {
-          const float4 v = *reinterpret_cast<const float4 *>(my_recv + k);
-          x[k] += v.x;
-          x[k + 1] += v.y;
-          x[k + 2] += v.z;
-          x[k + 3] += v.w;
+        for (int k = 0; k < 32; k += 8) {
+          const int u = (w * C::kHalf + k) >> 3;
+          const uint4 v = *reinterpret_cast<const uint4 *>(my_recv + ((u ^ (h & 7)) << 4));
+          const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[k + 2 * e] += __uint_as_float(pv[e] << 16);
+            x[k + 2 * e + 1] += __uint_as_float(pv[e] & 0xffff0000u);
+          }
         }
-        mbar_arrive_remote(recv_empty, peer);
+        mbar_arrive(&consumed[b]);  // the agent tells the peer that recv[b] may be refilled
       }
-      float mblk = -__builtin_huge_valf();
+      // row max over the whole block: this warpgroup's half, then the other's through smem
+      const bool full = (i + 1) * C::kBN <= n_valid;
+      if (!full) {
 #pragma unroll
-      for (int k = 0; k < C::kBN; ++k) {
-        x[k] = (i * C::kBN + k < n_valid) ? x[k] * P.scale_log2 : -__builtin_huge_valf();
-        mblk = fmaxf(mblk, x[k]);
+        for (int k = 0; k < 32; ++k)
+          if (i * C::kBN + w * C::kHalf + k >= n_valid) x[k] = -__builtin_huge_valf();
       }
+      float m01[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        m01[q4] = fmaxf(fmaxf(x[8 * q4], x[8 * q4 + 1]), fmaxf(x[8 * q4 + 2], x[8 * q4 + 3]));
+        m01[q4] = fmaxf(m01[q4], fmaxf(fmaxf(x[8 * q4 + 4], x[8 * q4 + 5]), fmaxf(x[8 * q4 + 6], x[8 * q4 + 7])));
+      }
+      red[(b * 2 + w) * 128 + h] = fmaxf(fmaxf(m01[0], m01[1]), fmaxf(m01[2], m01[3]));
+      mbar_arrive(&red_full[b]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&red_full[b], (i >> 1) & 1, P.err, 33, i));
+      if (!ok) break;
+      const float mraw = fmaxf(red[(b * 2) * 128 + h], red[(b * 2 + 1) * 128 + h]);
+      const float mblk = mraw * P.scale_log2;  // scale > 0: the max commutes with it
       // lazy rescale: only when some row of the warp saw its max grow by more
-      // than 2^8; rows whose max did not grow get alpha = 1 (exact)
+      // than 2^8; rows whose max did not grow get alpha = 1 (exact).  Both
+      // warpgroups see the same row maxima, so they decide alike.
       if (__any_sync(0xffffffffu, mblk > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, mblk);
         const float alpha = ex2(m_used - m_new);
         if (i >= 1) {
-          // O holds PV(i-1): rescale it before PV(i) accumulates
+          // O holds PV(i-1): rescale this warpgroup's half of it before PV(i) accumulates
           ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, P.err, 30, i));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < C::kOCols; c += 32) {
+          for (int c = w * (C::kOCols / 2); c < (w + 1) * (C::kOCols / 2); c += 32) {
             uint32_t r[32];
             tmem_ld32(lane_base + c, r);
             tmem_ld_wait();
@@ -328,28 +479,45 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         l *= alpha;
         m_used = m_new;
       }
-      uint32_t packed[32];
-      float lsum = 0.f;
+      // P tile: wait until PV(i-2) has consumed this buffer
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((i - 2) >> 1) & 1, P.err, 32, i));
+        if (!ok) break;
+      }
+      uint32_t packed[16];
+      float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < C::kBN; k += 2) {
-        const float a = ex2(x[k] - m_used), c = ex2(x[k + 1] - m_used);
-        lsum += a + c;
+      for (int k = 0; k < 32; k += 2) {
+        const float a = ex2(fmaf(x[k], P.scale_log2, -m_used));
+        const float c = ex2(fmaf(x[k + 1], P.scale_log2, -m_used));
+        ls0 += a;
+        ls1 += c;
         packed[k >> 1] = pack_bf16x2(a, c);
       }
-      l += lsum;
-      tmem_st32(lane_base + C::kSCol + b * C::kBN, packed);
-      tmem_st_wait();
-      tc_fence_before();
+      l += ls0 + ls1;
+      uint8_t *prow = smem + C::kOffP + b * C::kPBytes + h * 128;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int uu = w * 4 + u;
+        *reinterpret_cast<uint4 *>(prow + ((uu ^ (h & 7)) << 4)) =
+            make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
       mbar_arrive(&p_full[b]);
     }
     ok = __all_sync(0xffffffffu, ok && mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, P.err, 31, nb));
+    // the two warpgroups' partial sums of the softmax denominator
+    red[(4 + w) * 128 + h] = l;
+    mbar_arrive(fin_full);
+    ok = __all_sync(0xffffffffu, mbar_wait(fin_full, 0, P.err, 34) && ok);
+    l = red[4 * 128 + h] + red[5 * 128 + h];
     if (ok) {
       tc_fence_after();
       if (P.sink && h < P.H) l += ex2(P.sink[h] * 1.4426950408889634f - m_used);
       const float inv = 1.f / l;
       __nv_bfloat16 *o = out_row + static_cast<int64_t>(h) * P.Dv;
 #pragma unroll 1
-      for (int c = 0; c < C::kOCols; c += 32) {
+      for (int c = w * (C::kOCols / 2); c < (w + 1) * (C::kOCols / 2); c += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + c, r);
         tmem_ld_wait();
@@ -371,7 +539,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -428,7 +596,7 @@ extern "C" dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, i
   if (!md || !q || !kv || !topk_idx || !out) return DSA_ERR_INVALID_ARG;
   if (!md->scalars || !md->local_query_start_loc || !md->local_req_kv_base || !md->local_token_pos)
     return DSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(topk_idx)) return DSA_ERR_INVALID_ARG;
   if (batch < 0 || tpr < 0 || num_tokens < 1 || topk < 1) return DSA_ERR_SHAPE;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return DSA_ERR_INVALID_ARG;
   if (tpr == 0) return DSA_OK;
