@@ -264,7 +264,7 @@ dsa_status dsa_poll_device_error(dsa_stream_t stream);
 
 /* As dsa_poll_device_error, and when an error is returned, `detail` (host,
  * 3 ints, may be NULL) receives where it was recorded: {site, site detail,
- * linear CTA index}.  Site codes: 11-18 indexer waits, 19-34 attention waits
+ * linear CTA index}.  Site codes: 11-18 indexer waits, 19-37 attention waits
  * (the detail is the key block), 41-46 bounds checks (indexer slot, top-k
  * slot, top-k overflow, attention slot, attention index, metadata). */
 dsa_status dsa_poll_device_error_detail(dsa_stream_t stream, int32_t *detail);

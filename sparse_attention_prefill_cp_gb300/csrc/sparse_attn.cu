@@ -20,11 +20,11 @@
 // the CTA's 256 main Q dims as bf16 (128), so the QK MMA reads A from TMEM
 // and only the 64-row key block from shared memory.
 //
-// Per CTA, 14 warps: 0-7 softmax in two warpgroups (one head row = one TMEM
+// Per CTA, 16 warps: 0-7 softmax in two warpgroups (one head row = one TMEM
 // lane per thread; warpgroup w owns columns [32w, 32w + 32) of each block),
-// 8 MMA issue + TMEM owner, 9 TMA for Q and the index row, then exchange agent,
-// 10-13 gather of the selected rows with 16-byte cp.async straight into the
-// 128B / 64B swizzled tiles (two groups on alternate blocks).  Key blocks of
+// 8 TMA for Q and the index row then event-driven MMA issue (TMEM owner), 9
+// the exchange agent, 10-15 gather of the selected rows with 16-byte cp.async
+// straight into the 128B / 64B swizzled tiles (two warps per stage).  Key blocks of
 // 64 rows, 3 smem stages.  The partial S tiles are exchanged rounded to bf16:
 // the softmax threads stage their rows locally and warp 9 ships each tile to
 // the peer's double-buffered receive tiles with one bulk copy that completes
@@ -53,8 +53,9 @@ struct AttnCfg {
   static constexpr int kBN = 64;        // selected rows per block
   static constexpr int kHalf = kBN / 2; // columns per softmax warpgroup
   static constexpr int kStages = 3;
-  // warps: 0-7 softmax (two warpgroups), 8 MMA + TMEM, 9 TMA (Q, index row), 10-13 row gather
-  static constexpr int kThreads = 448;
+  // warps: 0-7 softmax (two warpgroups); 8 TMEM owner, TMA (Q, index row) then MMA issue;
+  // 9 exchange agent; 10-15 row gather, warps 10 + 2g and 11 + 2g owning stage g
+  static constexpr int kThreads = 512;
   static constexpr int kQMain = NMAIN * 128 * 128;
   static constexpr int kQTail = TAIL ? 128 * 64 : 0;
   static constexpr int kStageMain = NMAIN * kBN * 128;
@@ -206,9 +207,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       __nv_bfloat16 *o = out_row + static_cast<int64_t>(tid) * P.Dv;
       for (int c = 0; c < C::DVC; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
     }
-  } else if (warp == 9) {
-    // ---------------- TMA: Q (main dims to a staging tile, tail dims in place) and the index row
+  } else if (warp == 8) {
     if (lane == 0) {
+      // ---------------- TMA: Q (main dims to a staging tile, tail dims in place) and the index row
       tma_prefetch_desc(&qmain_map);
       const uint32_t idx_bytes = static_cast<uint32_t>(P.topk) * 4;
       mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail + idx_bytes);
@@ -216,6 +217,72 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tma_load_3d(smem + C::kOffQStage + i * 16384, &qmain_map, main_dim0 + 64 * i, 0, slot, q_full);
       if (C::TAIL) tma_load_3d(smem + C::kOffQTail, &qtail_map, tail_dim0, 0, slot, q_full);
       bulk_load(smem + C::kOffIdx, P.topk_idx + static_cast<int64_t>(slot) * P.topk, idx_bytes, q_full);
+      // ---------------- MMA issuer: QK runs two blocks ahead of PV
+      const uint32_t st_addr = smem_u32(smem + C::kOffStage);
+      const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
+      const uint32_t p_addr = smem_u32(smem + C::kOffP);
+      bool ok = mbar_wait(q_full, 0, P.err, 23) && mbar_wait(q_ready, 0, P.err, 23);
+      tc_fence_after();
+      // event-driven issue: QK(j) as soon as its rows have landed and its S
+      // buffer is free, PV(i) as soon as P(i) is written; each stream in order
+      int qk = 0, pv = 0;
+      long long t_prog = clock64(), t_check = t_prog;
+      while (ok && pv < nb) {
+        bool progressed = false;
+        if (qk < nb && mbar_test(&kv_full[qk % C::kStages], (qk / C::kStages) & 1) &&
+            (qk < 2 || mbar_test(&s_free[qk & 1], ((qk - 2) >> 1) & 1))) {
+          tc_fence_after();
+          const int b = qk & 1;
+          const uint32_t kb = st_addr + (qk % C::kStages) * C::kStageBytes;
+#pragma unroll
+          for (int k = 0; k < C::kQKSteps; ++k) {
+            if (k < C::kQKMainSteps) {
+              const int i = k >> 2, sub = k & 3;
+              const uint64_t bd = smem_desc(kb + i * (C::kBN * 128) + sub * 32, 16, 1024, kLayoutSW128);
+              mma_ts(tmem + C::kSCol + b * C::kBN, tmem + C::kQCol + k * 8, bd, C::kIdescQK, k > 0 ? 1u : 0u);
+            } else {
+              const int t = k - C::kQKMainSteps;
+              const uint64_t a = smem_desc(qt_addr + t * 32, 16, 512, kLayoutSW64);
+              const uint64_t bd = smem_desc(kb + C::kStageMain + t * 32, 16, 512, kLayoutSW64);
+              mma_ss(tmem + C::kSCol + b * C::kBN, a, bd, C::kIdescQK, 1u);
+            }
+          }
+          mma_commit(&s_full[b]);
+          ++qk;
+          progressed = true;
+        }
+        if (pv < qk && mbar_test(&p_full[pv & 1], (pv >> 1) & 1)) {
+          tc_fence_after();
+          const int bi = pv & 1, si = pv % C::kStages;
+          const uint32_t vb = st_addr + si * C::kStageBytes;
+          const uint32_t pb = p_addr + bi * C::kPBytes;
+#pragma unroll
+          for (int k = 0; k < C::kPVSteps; ++k) {
+            const uint64_t a = smem_desc(pb + k * 32, 16, 1024, kLayoutSW128);
+            const uint64_t bd = smem_desc(vb + k * 2048, C::kBN * 128, 1024, kLayoutSW128);
+            mma_ss(tmem, a, bd, C::kIdescPV, (pv > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&pv_done[bi]);
+          mma_commit(&kv_empty[si]);
+          ++pv;
+          progressed = true;
+        }
+        const long long now = clock64();
+        if (progressed) {
+          t_prog = now;
+        } else if (now - t_check > 100000) {
+          t_check = now;
+          if (error_set(P.err)) {
+            ok = false;
+          } else if (now - t_prog > kWaitLimitCycles) {
+            record_error(P.err, DSA_ERR_DEVICE_TIMEOUT, 37, qk * 10000 + pv);
+            ok = false;
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, P.err, 21);
       if (C::SPLIT) {
         // ---------------- exchange agent: ships each staged partial-S tile to the
@@ -243,17 +310,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
     }
   } else if (warp >= 10) {
-    // ---------------- gather of the selected rows: two groups of 64 threads take
-    // alternate blocks, one selected row per thread, 16-byte cp.async pieces
-    // written straight into the 128B / 64B swizzled tiles
-    const int ptid = tid - 320;
-    const int group = ptid >> 6, r = ptid & 63;
+    // ---------------- gather of the selected rows: warps 10 + 2g and 11 + 2g
+    // take the blocks j = g (mod 3), which all use stage g; one selected row
+    // per thread, 16-byte cp.async pieces written straight into the 128B / 64B
+    // swizzled tiles
+    const int g = (warp - 10) >> 1, r = ((warp - 10) & 1) * 32 + lane;
     if (mbar_wait(q_full, 0, P.err, 21)) {
-      for (int j = group; j < nb; j += 2) {
-        const int s = j % C::kStages;
+      for (int j = g; j < nb; j += C::kStages) {
+        const int s = g;
         if (!mbar_wait(&kv_empty[s], ((j / C::kStages) & 1) ^ 1, P.err, 22, j)) break;
         // stages 1 and 2 held the staged Q until the softmax warps moved it to TMEM
         if ((j == 1 || j == 2) && !mbar_wait(q_ready, 0, P.err, 20, j)) break;
+        const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
         const int k = j * C::kBN + r;
         int row = k < n_valid ? idx_s[k] : -1;
         if (k < n_valid && (row < 0 || row >= P.num_tokens)) {
@@ -262,7 +330,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
         const uint32_t nbytes = row < 0 ? 0u : 16u;
-        const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
 #pragma unroll
         for (int u = 0; u < C::kUnitsPerRow; ++u) {
           if (u < C::NMAIN * 8) {
@@ -282,53 +349,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
     }
     cp_async_wait<0>();
-  } else if (warp == 8) {
-    // ---------------- MMA issuer (one thread): QK runs two blocks ahead of PV
-    if (lane == 0) {
-      const uint32_t st_addr = smem_u32(smem + C::kOffStage);
-      const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
-      const uint32_t p_addr = smem_u32(smem + C::kOffP);
-      bool ok = mbar_wait(q_full, 0, P.err, 23) && mbar_wait(q_ready, 0, P.err, 23);
-      tc_fence_after();
-      for (int j = 0; ok && j < nb + 2; ++j) {
-        if (j < nb) {
-          const int s = j % C::kStages, b = j & 1;
-          if (!(ok = mbar_wait(&kv_full[s], (j / C::kStages) & 1, P.err, 24, j))) break;
-          if (j >= 2 && !(ok = mbar_wait(&s_free[b], ((j - 2) >> 1) & 1, P.err, 25, j))) break;
-          tc_fence_after();
-          const uint32_t kb = st_addr + s * C::kStageBytes;
-#pragma unroll
-          for (int k = 0; k < C::kQKSteps; ++k) {
-            if (k < C::kQKMainSteps) {
-              const int i = k >> 2, sub = k & 3;
-              const uint64_t bd = smem_desc(kb + i * (C::kBN * 128) + sub * 32, 16, 1024, kLayoutSW128);
-              mma_ts(tmem + C::kSCol + b * C::kBN, tmem + C::kQCol + k * 8, bd, C::kIdescQK, k > 0 ? 1u : 0u);
-            } else {
-              const int t = k - C::kQKMainSteps;
-              const uint64_t a = smem_desc(qt_addr + t * 32, 16, 512, kLayoutSW64);
-              const uint64_t bd = smem_desc(kb + C::kStageMain + t * 32, 16, 512, kLayoutSW64);
-              mma_ss(tmem + C::kSCol + b * C::kBN, a, bd, C::kIdescQK, 1u);
-            }
-          }
-          mma_commit(&s_full[b]);
-        }
-        if (j >= 2) {
-          const int i = j - 2, si = i % C::kStages, bi = i & 1;
-          if (!(ok = mbar_wait(&p_full[bi], (i >> 1) & 1, P.err, 26, i))) break;
-          tc_fence_after();
-          const uint32_t vb = st_addr + si * C::kStageBytes;
-          const uint32_t pb = p_addr + bi * C::kPBytes;
-#pragma unroll
-          for (int k = 0; k < C::kPVSteps; ++k) {
-            const uint64_t a = smem_desc(pb + k * 32, 16, 1024, kLayoutSW128);
-            const uint64_t bd = smem_desc(vb + k * 2048, C::kBN * 128, 1024, kLayoutSW128);
-            mma_ss(tmem, a, bd, C::kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(&pv_done[bi]);
-          mma_commit(&kv_empty[si]);
-        }
-      }
-    }
   } else {
     // ---------------- softmax: two warpgroups; thread = head row h = TMEM lane,
     // warpgroup w owns columns [32w, 32w + 32) of every 64-row block.
@@ -360,67 +380,65 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
     // partial-S tile rows: 64 bf16 (128 bytes), 16-byte unit u stored at u ^ (h & 7)
     uint8_t *recv0 = smem + C::kOffRecv;
-    // stage our 32 columns of block j's partial S row, rounded to bf16, for the
-    // exchange agent (SPLIT only).  Each CTA softmaxes its own fp32 partial plus
-    // the peer's bf16 partial and normalises its own O half with its own sum,
-    // so the two CTAs need not agree bitwise.
-    auto stage = [&](int j) {
+    // stage our 32 columns of a partial S row (fp32 registers), rounded to bf16,
+    // for the exchange agent (SPLIT only).  Each CTA softmaxes its own fp32
+    // partial plus the peer's bf16 partial and normalises its own O half with
+    // its own sum, so the two CTAs need not agree bitwise.
+    auto stage = [&](int j, const float (&v)[32]) {
       const int b = j & 1;
-      uint32_t r[32];
-      tmem_ld32(lane_base + C::kSCol + b * C::kBN + w * C::kHalf, r);
-      tmem_ld_wait();
       uint8_t *row = smem + C::kOffStg + b * C::kRecvBytes + h * 128;
 #pragma unroll
       for (int k = 0; k < 32; k += 8) {
         const int u = (w * C::kHalf + k) >> 3;
         *reinterpret_cast<uint4 *>(row + ((u ^ (h & 7)) << 4)) =
-            make_uint4(pack_bf16x2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
-                       pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
-                       pack_bf16x2(__uint_as_float(r[k + 4]), __uint_as_float(r[k + 5])),
-                       pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
+            make_uint4(pack_bf16x2(v[k], v[k + 1]), pack_bf16x2(v[k + 2], v[k + 3]),
+                       pack_bf16x2(v[k + 4], v[k + 5]), pack_bf16x2(v[k + 6], v[k + 7]));
       }
       fence_proxy_async_smem();  // the bulk copy reads the tile through the async proxy
       mbar_arrive(&staged[b]);
     };
+    // load our 32 columns of S(j) from TMEM once; the buffer is then free for QK(j+2)
+    auto load_s = [&](int j, float (&v)[32]) {
+      uint32_t r[32];
+      tmem_ld32(lane_base + C::kSCol + (j & 1) * C::kBN + w * C::kHalf, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+      tc_fence_before();
+      mbar_arrive(&s_free[j & 1]);
+    };
 
     float m_used = -__builtin_huge_valf(), l = 0.f;  // m in log2 units; l over this warpgroup's columns
-    if (C::SPLIT && ok) {
+    float nxt[32];  // our partial S of the next block, carried across iterations
+    if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[0], 0, P.err, 27, 0));
       if (ok) {
         tc_fence_after();
-        stage(0);
+        load_s(0, nxt);
+        if (C::SPLIT) stage(0, nxt);
       }
     }
     for (int i = 0; ok && i < nb; ++i) {
       const int b = i & 1;
-      if (C::SPLIT && i + 1 < nb) {
-        // send block i+1 ahead: the peer has it by the time it starts block i+1
+      float x[C::kHalf];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) x[k] = nxt[k];
+      if (i + 1 < nb) {
+        // fetch (and for the pair, ship) block i+1 ahead: the peer has it by the
+        // time it starts block i+1
         const int b1 = (i + 1) & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b1], ((i + 1) >> 1) & 1, P.err, 27, i + 1) &&
-                                         mbar_wait(&stg_free[b1], (((i + 1) >> 1) & 1) ^ 1, P.err, 28, i + 1));
+                                         (!C::SPLIT || mbar_wait(&stg_free[b1], (((i + 1) >> 1) & 1) ^ 1, P.err,
+                                                                 28, i + 1)));
         if (!ok) break;
         tc_fence_after();
-        stage(i + 1);
+        load_s(i + 1, nxt);
+        if (C::SPLIT) stage(i + 1, nxt);
       }
       if (C::SPLIT) {
         if (tid == 0) mbar_arrive_expect_tx(&recv_full[b], C::kRecvTx);
         ok = __all_sync(0xffffffffu, mbar_wait<true>(&recv_full[b], (i >> 1) & 1, P.err, 29, i));
-      } else {
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (i >> 1) & 1, P.err, 27, i));
-      }
-      if (!ok) break;
-      tc_fence_after();
-      float x[C::kHalf];
-      {
-        uint32_t r[32];
-        tmem_ld32(lane_base + C::kSCol + b * C::kBN + w * C::kHalf, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r[k]);
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);  // the MMA may compute QK(i+2) into this buffer
-      if (C::SPLIT) {
+        if (!ok) break;
         const uint8_t *my_recv = recv0 + b * C::kRecvBytes + h * 128;
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
