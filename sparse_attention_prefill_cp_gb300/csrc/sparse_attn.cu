@@ -24,7 +24,8 @@
 // lane per thread; warpgroup w owns columns [32w, 32w + 32) of each block),
 // 8 TMA for Q and the index row then event-driven MMA issue (TMEM owner), 9
 // the exchange agent, 10-15 gather of the selected rows with 16-byte cp.async
-// straight into the 128B / 64B swizzled tiles (two warps per stage).  Key blocks of
+// straight into the 128B / 64B swizzled tiles (two warps per stage, eight
+// threads per 128-byte chunk so that loads coalesce into whole lines).  Key blocks of
 // 64 rows, 3 smem stages.  The partial S tiles are exchanged rounded to bf16:
 // the softmax threads stage their rows locally and warp 9 ships each tile to
 // the peer's double-buffered receive tiles with one bulk copy that completes
@@ -311,10 +312,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   } else if (warp >= 10) {
     // ---------------- gather of the selected rows: warps 10 + 2g and 11 + 2g
-    // take the blocks j = g (mod 3), which all use stage g; one selected row
-    // per thread, 16-byte cp.async pieces written straight into the 128B / 64B
-    // swizzled tiles
-    const int g = (warp - 10) >> 1, r = ((warp - 10) & 1) * 32 + lane;
+    // take the blocks j = g (mod 3), which all use stage g.  Eight consecutive
+    // threads copy one 128-byte chunk of a row (one 16-byte cp.async each, the
+    // 128B swizzle applied on the destination), so each warp instruction reads
+    // four whole lines; a thread covers rows r0, r0 + 8, ..., r0 + 56.
+    const int g = (warp - 10) >> 1, t = ((warp - 10) & 1) * 32 + lane;
+    const int v = t & 7, r0 = t >> 3;
     if (mbar_wait(q_full, 0, P.err, 21)) {
       for (int j = g; j < nb; j += C::kStages) {
         const int s = g;
@@ -322,25 +325,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // stages 1 and 2 held the staged Q until the softmax warps moved it to TMEM
         if ((j == 1 || j == 2) && !mbar_wait(q_ready, 0, P.err, 20, j)) break;
         const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        const int k = j * C::kBN + r;
-        int row = k < n_valid ? idx_s[k] : -1;
-        if (k < n_valid && (row < 0 || row >= P.num_tokens)) {
-          record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, k);
-          row = -1;
-        }
-        const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
-        const uint32_t nbytes = row < 0 ? 0u : 16u;
 #pragma unroll
-        for (int u = 0; u < C::kUnitsPerRow; ++u) {
-          if (u < C::NMAIN * 8) {
-            const int i = u >> 3, v = u & 7;
+        for (int rr = 0; rr < C::kBN / 8; ++rr) {
+          const int r = r0 + 8 * rr;
+          const int k = j * C::kBN + r;
+          int row = k < n_valid ? idx_s[k] : -1;
+          if (k < n_valid && (row < 0 || row >= P.num_tokens)) {
+            record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, k);
+            row = -1;
+          }
+          const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
+          const uint32_t nbytes = row < 0 ? 0u : 16u;
+#pragma unroll
+          for (int i = 0; i < C::NMAIN; ++i)
             cp_async_16(sb + i * (C::kBN * 128) + r * 128 + ((v ^ (r & 7)) << 4), src + main_dim0 + i * 64 + v * 8,
                         nbytes);
-          } else {
-            const int v = u - C::NMAIN * 8;
-            cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + tail_dim0 + v * 8,
-                        nbytes);
-          }
+          if (C::TAIL && v < 4)
+            cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + tail_dim0 + v * 8, nbytes);
         }
         cp_async_commit();
         cp_async_wait<0>();
