@@ -26,7 +26,7 @@
 // the exchange agent, 10-15 gather of the selected rows with 16-byte cp.async
 // straight into the 128B / 64B swizzled tiles (two warps per stage, eight
 // threads per 128-byte chunk so that loads coalesce into whole lines).  Key blocks of
-// 64 rows, 3 smem stages.  The partial S tiles are exchanged rounded to bf16:
+// 64 rows, 4 smem stages.  The partial S tiles are exchanged rounded to bf16:
 // the softmax threads stage their rows locally and warp 9 ships each tile to
 // the peer's double-buffered receive tiles with one bulk copy that completes
 // the peer's mbarrier transaction count, one block ahead of the softmax that
@@ -53,9 +53,9 @@ struct AttnCfg {
   static constexpr bool SPLIT = SPLIT_; // 2-CTA cluster per token
   static constexpr int kBN = 64;        // selected rows per block
   static constexpr int kHalf = kBN / 2; // columns per softmax warpgroup
-  static constexpr int kStages = 3;
-  // warps: 0-7 softmax (two warpgroups); 8 TMEM owner, TMA (Q, index row) then MMA issue;
-  // 9 exchange agent; 10-15 row gather, warps 10 + 2g and 11 + 2g owning stage g
+  static constexpr int kStages = 4;
+  // warps: 0-7 softmax (two warpgroups); 8 TMEM owner, TMA (Q) then MMA issue;
+  // 9 exchange agent; 10-15 row gather, warps 10 + 2g and 11 + 2g taking blocks j = g (mod 3)
   static constexpr int kThreads = 512;
   static constexpr int kQMain = NMAIN * 128 * 128;
   static constexpr int kQTail = TAIL ? 128 * 64 : 0;
@@ -73,15 +73,13 @@ struct AttnCfg {
   // shared memory
   static constexpr int kRecvBytes = SPLIT ? 128 * kBN * 2 : 0;  // one partial-S tile (bf16), rows swizzled
   static constexpr int kPBytes = 128 * 128;                     // P tile [128 heads][64 keys] bf16, SW128
-  static constexpr int kIdxBytes = 2048 * 4;
   static constexpr int kOffStage = 0;
   static constexpr int kOffQStage = kOffStage + kStageBytes;  // Q main staged in stages 1..2 at start
   static constexpr int kOffQTail = kOffStage + kStages * kStageBytes;
   static constexpr int kOffRecv = kOffQTail + kQTail;
-  static constexpr int kOffStg = kOffRecv + 2 * kRecvBytes;   // our partial-S tiles on their way out
-  static constexpr int kOffP = kOffStg + 2 * kRecvBytes;
-  static constexpr int kOffIdx = kOffP + 2 * kPBytes;
-  static constexpr int kOffRed = kOffIdx + kIdxBytes;         // [3][2 warpgroups][128] floats
+  static constexpr int kOffStg = kOffRecv + 2 * kRecvBytes;   // our partial-S tile on its way out
+  static constexpr int kOffP = kOffStg + kRecvBytes;
+  static constexpr int kOffRed = kOffP + kPBytes;             // [3][2 warpgroups][128] floats
   static constexpr int kOffBar = kOffRed + 3 * 2 * 128 * 4;
   static constexpr int kNumBars = 2 + 2 * kStages + 2 * 10 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -94,6 +92,7 @@ struct AttnCfg {
   static_assert(kQCol + NMAIN * 32 <= kTmemCols, "TMEM budget");
   static_assert(DVC % 16 == 0 && DVC <= NMAIN * 64, "value columns inside the main chunks");
   static_assert(kQMain <= 2 * kStageBytes, "Q staging fits in stages 1..2");
+  static_assert(kBN % 8 == 0, "gather covers rows in groups of 8");
   static_assert(kStageBytes % 1024 == 0 && kOffQTail % 1024 == 0 && kOffP % 1024 == 0, "alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -141,7 +140,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (256 softmax threads)
   uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (256)
   int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p
-  const int32_t *idx_s = reinterpret_cast<const int32_t *>(smem + C::kOffIdx);
   float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -210,14 +208,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   } else if (warp == 8) {
     if (lane == 0) {
-      // ---------------- TMA: Q (main dims to a staging tile, tail dims in place) and the index row
+      // ---------------- TMA: Q (main dims to a staging tile, tail dims in place)
       tma_prefetch_desc(&qmain_map);
-      const uint32_t idx_bytes = static_cast<uint32_t>(P.topk) * 4;
-      mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail + idx_bytes);
+      mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail);
       for (int i = 0; i < C::NMAIN; ++i)
         tma_load_3d(smem + C::kOffQStage + i * 16384, &qmain_map, main_dim0 + 64 * i, 0, slot, q_full);
       if (C::TAIL) tma_load_3d(smem + C::kOffQTail, &qtail_map, tail_dim0, 0, slot, q_full);
-      bulk_load(smem + C::kOffIdx, P.topk_idx + static_cast<int64_t>(slot) * P.topk, idx_bytes, q_full);
       // ---------------- MMA issuer: QK runs two blocks ahead of PV
       const uint32_t st_addr = smem_u32(smem + C::kOffStage);
       const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
@@ -256,7 +252,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_after();
           const int bi = pv & 1, si = pv % C::kStages;
           const uint32_t vb = st_addr + si * C::kStageBytes;
-          const uint32_t pb = p_addr + bi * C::kPBytes;
+          const uint32_t pb = p_addr;
 #pragma unroll
           for (int k = 0; k < C::kPVSteps; ++k) {
             const uint64_t a = smem_desc(pb + k * 32, 16, 1024, kLayoutSW128);
@@ -295,8 +291,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const int b = t & 1;
             if (!(ok = mbar_wait(&staged[b], (t >> 1) & 1, P.err, 35, t))) break;
             if (t >= 2 && !(ok = mbar_wait<true>(&recv_empty[b], ((t >> 1) & 1) ^ 1, P.err, 28, t))) break;
-            bulk_copy_to_peer(peer_recv + b * C::kRecvBytes, smem + C::kOffStg + b * C::kRecvBytes, C::kRecvBytes,
-                              peer_full + b * 8);
+            bulk_copy_to_peer(peer_recv + b * C::kRecvBytes, smem + C::kOffStg, C::kRecvBytes, peer_full + b * 8);
             bulk_commit();
             bulk_wait_read0();
             mbar_arrive(&stg_free[b]);
@@ -312,42 +307,52 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   } else if (warp >= 10) {
     // ---------------- gather of the selected rows: warps 10 + 2g and 11 + 2g
-    // take the blocks j = g (mod 3), which all use stage g.  Eight consecutive
-    // threads copy one 128-byte chunk of a row (one 16-byte cp.async each, the
-    // 128B swizzle applied on the destination), so each warp instruction reads
-    // four whole lines; a thread covers rows r0, r0 + 8, ..., r0 + 56.
+    // take the blocks j = g (mod 3), block j going to stage j % 4.  Eight
+    // consecutive threads copy one 128-byte chunk of a row (one 16-byte
+    // cp.async each, the 128B swizzle applied on the destination), so each warp
+    // instruction reads four whole lines; a thread covers rows r0, r0 + 8, ...
+    // The row indices of the group's next block are fetched while this one lands.
+    constexpr int kGroups = 3, kRowsPerThread = C::kBN / 8;
     const int g = (warp - 10) >> 1, t = ((warp - 10) & 1) * 32 + lane;
     const int v = t & 7, r0 = t >> 3;
-    if (mbar_wait(q_full, 0, P.err, 21)) {
-      for (int j = g; j < nb; j += C::kStages) {
-        const int s = g;
-        if (!mbar_wait(&kv_empty[s], ((j / C::kStages) & 1) ^ 1, P.err, 22, j)) break;
-        // stages 1 and 2 held the staged Q until the softmax warps moved it to TMEM
-        if ((j == 1 || j == 2) && !mbar_wait(q_ready, 0, P.err, 20, j)) break;
-        const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+    const int32_t *idx_row = P.topk_idx + static_cast<int64_t>(slot) * P.topk;
+    int rows[kRowsPerThread];
+    auto fetch = [&](int j) {
 #pragma unroll
-        for (int rr = 0; rr < C::kBN / 8; ++rr) {
-          const int r = r0 + 8 * rr;
-          const int k = j * C::kBN + r;
-          int row = k < n_valid ? idx_s[k] : -1;
-          if (k < n_valid && (row < 0 || row >= P.num_tokens)) {
-            record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, k);
-            row = -1;
-          }
-          const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
-          const uint32_t nbytes = row < 0 ? 0u : 16u;
-#pragma unroll
-          for (int i = 0; i < C::NMAIN; ++i)
-            cp_async_16(sb + i * (C::kBN * 128) + r * 128 + ((v ^ (r & 7)) << 4), src + main_dim0 + i * 64 + v * 8,
-                        nbytes);
-          if (C::TAIL && v < 4)
-            cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + tail_dim0 + v * 8, nbytes);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&kv_full[s]);
+      for (int rr = 0; rr < kRowsPerThread; ++rr) {
+        const int k = j * C::kBN + r0 + 8 * rr;
+        rows[rr] = k < n_valid ? __ldg(idx_row + k) : -1;
       }
+    };
+    if (g < nb) fetch(g);
+    for (int j = g; j < nb; j += kGroups) {
+      const int s = j % C::kStages;
+      if (!mbar_wait(&kv_empty[s], ((j / C::kStages) & 1) ^ 1, P.err, 22, j)) break;
+      // stages 1 and 2 held the staged Q until the softmax warps moved it to TMEM
+      if ((j == 1 || j == 2) && !mbar_wait(q_ready, 0, P.err, 20, j)) break;
+      const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerThread; ++rr) {
+        const int r = r0 + 8 * rr;
+        int row = rows[rr];
+        if (j * C::kBN + r < n_valid && (row < 0 || row >= P.num_tokens)) {
+          record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, j * C::kBN + r);
+          row = -1;
+        }
+        const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
+        const uint32_t nbytes = row < 0 ? 0u : 16u;
+#pragma unroll
+        for (int i = 0; i < C::NMAIN; ++i)
+          cp_async_16(sb + i * (C::kBN * 128) + r * 128 + ((v ^ (r & 7)) << 4), src + main_dim0 + i * 64 + v * 8,
+                      nbytes);
+        if (C::TAIL && v < 4)
+          cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + tail_dim0 + v * 8, nbytes);
+      }
+      cp_async_commit();
+      if (j + kGroups < nb) fetch(j + kGroups);
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(&kv_full[s]);
     }
     cp_async_wait<0>();
   } else {
@@ -387,7 +392,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // its own sum, so the two CTAs need not agree bitwise.
     auto stage = [&](int j, const float (&v)[32]) {
       const int b = j & 1;
-      uint8_t *row = smem + C::kOffStg + b * C::kRecvBytes + h * 128;
+      uint8_t *row = smem + C::kOffStg + h * 128;
 #pragma unroll
       for (int k = 0; k < 32; k += 8) {
         const int u = (w * C::kHalf + k) >> 3;
@@ -429,8 +434,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // time it starts block i+1
         const int b1 = (i + 1) & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b1], ((i + 1) >> 1) & 1, P.err, 27, i + 1) &&
-                                         (!C::SPLIT || mbar_wait(&stg_free[b1], (((i + 1) >> 1) & 1) ^ 1, P.err,
-                                                                 28, i + 1)));
+                                         (!C::SPLIT || mbar_wait(&stg_free[b], (i >> 1) & 1, P.err, 28, i + 1)));
         if (!ok) break;
         tc_fence_after();
         load_s(i + 1, nxt);
@@ -498,9 +502,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         l *= alpha;
         m_used = m_new;
       }
-      // P tile: wait until PV(i-2) has consumed this buffer
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((i - 2) >> 1) & 1, P.err, 32, i));
+      // P tile: wait until PV(i-1) has consumed it
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, P.err, 32, i));
         if (!ok) break;
       }
       uint32_t packed[16];
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         packed[k >> 1] = pack_bf16x2(a, c);
       }
       l += ls0 + ls1;
-      uint8_t *prow = smem + C::kOffP + b * C::kPBytes + h * 128;
+      uint8_t *prow = smem + C::kOffP + h * 128;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int uu = w * 4 + u;
