@@ -111,6 +111,13 @@ struct AttnParams {
   int *err;
 };
 
+// One arrival per warp: the warp's threads synchronise (ordering their prior
+// memory and fenced tcgen05 operations) and lane 0 arrives for all of them.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -125,20 +132,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint64_t *q_full = bars;                     // Q staged + tail + index row landed (TMA)
-  uint64_t *q_ready = bars + 1;                // Q main copied into TMEM, staging free (256 softmax threads)
+  uint64_t *q_ready = bars + 1;                // Q main copied into TMEM, staging free (8 softmax warps)
   uint64_t *kv_full = bars + 2;                // [kStages] gathered rows landed (64 gather threads)
   uint64_t *kv_empty = kv_full + C::kStages;   // [kStages] PV done with the stage (MMA commit)
   uint64_t *s_full = kv_empty + C::kStages;    // [2] QK done (MMA commit)
-  uint64_t *s_free = s_full + 2;               // [2] S read out of TMEM (256 softmax threads)
-  uint64_t *p_full = s_free + 2;               // [2] P tile written (256 softmax threads)
+  uint64_t *s_free = s_full + 2;               // [2] S read out of TMEM (8 softmax warps)
+  uint64_t *p_full = s_free + 2;               // [2] P tile written (8 softmax warps)
   uint64_t *pv_done = p_full + 2;              // [2] PV done, P tile free (MMA commit)
   uint64_t *recv_full = pv_done + 2;           // [2] the peer's partial S landed (st.async tx)
   uint64_t *recv_empty = recv_full + 2;        // [2] the peer consumed what we sent (peer's agent)
-  uint64_t *red_full = recv_empty + 2;         // [2] both warpgroups' block maxima written (256)
-  uint64_t *staged = red_full + 2;             // [2] our partial-S tile written (256 softmax threads)
+  uint64_t *red_full = recv_empty + 2;         // [2] both warpgroups' block maxima written (8 warps)
+  uint64_t *staged = red_full + 2;             // [2] our partial-S tile written (8 softmax warps)
   uint64_t *stg_free = staged + 2;             // [2] the bulk copy has read our tile (sender)
-  uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (256 softmax threads)
-  uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (256)
+  uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (8 softmax warps)
+  uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (8 warps)
   int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p
   float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
@@ -165,24 +172,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     misc[1] = base;
     misc[2] = p;
     mbar_init(q_full, 1);
-    mbar_init(q_ready, 256);
+    mbar_init(q_ready, 8);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&kv_full[s], 64);
       mbar_init(&kv_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 256);
-      mbar_init(&p_full[b], 256);
+      mbar_init(&s_free[b], 8);
+      mbar_init(&p_full[b], 8);
       mbar_init(&pv_done[b], 1);
       mbar_init(&recv_full[b], 1);
       mbar_init(&recv_empty[b], 1);
-      mbar_init(&red_full[b], 256);
-      mbar_init(&staged[b], 256);
+      mbar_init(&red_full[b], 8);
+      mbar_init(&staged[b], 8);
       mbar_init(&stg_free[b], 1);
-      mbar_init(&consumed[b], 256);
+      mbar_init(&consumed[b], 8);
     }
-    mbar_init(fin_full, 256);
+    mbar_init(fin_full, 8);
     fence_mbar_init();
   }
   if (warp == 8) {
@@ -382,7 +389,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tmem_st_wait();
     }
     tc_fence_before();
-    mbar_arrive(q_ready);
+    warp_arrive(q_ready, lane);
 
     // partial-S tile rows: 64 bf16 (128 bytes), 16-byte unit u stored at u ^ (h & 7)
     uint8_t *recv0 = smem + C::kOffRecv;
@@ -401,7 +408,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                        pack_bf16x2(v[k + 4], v[k + 5]), pack_bf16x2(v[k + 6], v[k + 7]));
       }
       fence_proxy_async_smem();  // the bulk copy reads the tile through the async proxy
-      mbar_arrive(&staged[b]);
+      warp_arrive(&staged[b], lane);
     };
     // load our 32 columns of S(j) from TMEM once; the buffer is then free for QK(j+2)
     auto load_s = [&](int j, float (&v)[32]) {
@@ -411,7 +418,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
       tc_fence_before();
-      mbar_arrive(&s_free[j & 1]);
+      warp_arrive(&s_free[j & 1], lane);
     };
 
     float m_used = -__builtin_huge_valf(), l = 0.f;  // m in log2 units; l over this warpgroup's columns
@@ -456,7 +463,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             x[k + 2 * e + 1] += __uint_as_float(pv[e] & 0xffff0000u);
           }
         }
-        mbar_arrive(&consumed[b]);  // the agent tells the peer that recv[b] may be refilled
+        warp_arrive(&consumed[b], lane);  // the agent tells the peer that recv[b] may be refilled
       }
       // row max over the whole block: this warpgroup's half, then the other's through smem
       const bool full = (i + 1) * C::kBN <= n_valid;
@@ -472,7 +479,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         m01[q4] = fmaxf(m01[q4], fmaxf(fmaxf(x[8 * q4 + 4], x[8 * q4 + 5]), fmaxf(x[8 * q4 + 6], x[8 * q4 + 7])));
       }
       red[(b * 2 + w) * 128 + h] = fmaxf(fmaxf(m01[0], m01[1]), fmaxf(m01[2], m01[3]));
-      mbar_arrive(&red_full[b]);
+      warp_arrive(&red_full[b], lane);
       ok = __all_sync(0xffffffffu, mbar_wait(&red_full[b], (i >> 1) & 1, P.err, 33, i));
       if (!ok) break;
       const float mraw = fmaxf(red[(b * 2) * 128 + h], red[(b * 2 + 1) * 128 + h]);
@@ -526,12 +533,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&p_full[b]);
+      warp_arrive(&p_full[b], lane);
     }
     ok = __all_sync(0xffffffffu, ok && mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, P.err, 31, nb));
     // the two warpgroups' partial sums of the softmax denominator
     red[(4 + w) * 128 + h] = l;
-    mbar_arrive(fin_full);
+    warp_arrive(fin_full, lane);
     ok = __all_sync(0xffffffffu, mbar_wait(fin_full, 0, P.err, 34) && ok);
     l = red[4 * 128 + h] + red[5 * 128 + h];
     if (ok) {
