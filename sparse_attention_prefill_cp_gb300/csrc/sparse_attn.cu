@@ -458,10 +458,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           const uint4 v = *reinterpret_cast<const uint4 *>(my_recv + ((u ^ (h & 7)) << 4));
           const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[k + 2 * e] += __uint_as_float(pv[e] << 16);
-            x[k + 2 * e + 1] += __uint_as_float(pv[e] & 0xffff0000u);
-          }
+          for (int e = 0; e < 4; ++e)
+            f2_unpack(f2_add(f2_pack(x[k + 2 * e], x[k + 2 * e + 1]),
+                             f2_pack(__uint_as_float(pv[e] << 16), __uint_as_float(pv[e] & 0xffff0000u))),
+                      x[k + 2 * e], x[k + 2 * e + 1]);
         }
         warp_arrive(&consumed[b], lane);  // the agent tells the peer that recv[b] may be refilled
       }
@@ -472,13 +472,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int k = 0; k < 32; ++k)
           if (i * C::kBN + w * C::kHalf + k >= n_valid) x[k] = -__builtin_huge_valf();
       }
-      float m01[4];
+      float m3[4];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        m01[q4] = fmaxf(fmaxf(x[8 * q4], x[8 * q4 + 1]), fmaxf(x[8 * q4 + 2], x[8 * q4 + 3]));
-        m01[q4] = fmaxf(m01[q4], fmaxf(fmaxf(x[8 * q4 + 4], x[8 * q4 + 5]), fmaxf(x[8 * q4 + 6], x[8 * q4 + 7])));
-      }
-      red[(b * 2 + w) * 128 + h] = fmaxf(fmaxf(m01[0], m01[1]), fmaxf(m01[2], m01[3]));
+      for (int q = 0; q < 4; ++q)
+        m3[q] = fmax3(fmax3(x[8 * q], x[8 * q + 1], x[8 * q + 2]), fmax3(x[8 * q + 3], x[8 * q + 4], x[8 * q + 5]),
+                      fmaxf(x[8 * q + 6], x[8 * q + 7]));
+      red[(b * 2 + w) * 128 + h] = fmaxf(fmax3(m3[0], m3[1], m3[2]), m3[3]);
       warp_arrive(&red_full[b], lane);
       ok = __all_sync(0xffffffffu, mbar_wait(&red_full[b], (i >> 1) & 1, P.err, 33, i));
       if (!ok) break;
@@ -515,16 +514,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!ok) break;
       }
       uint32_t packed[16];
-      float ls0 = 0.f, ls1 = 0.f;
+      const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2), nm2 = f2_pack(-m_used, -m_used);
+      uint64_t acc[2] = {0, 0};  // +0.0f pairs
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
-        const float a = ex2(fmaf(x[k], P.scale_log2, -m_used));
-        const float c = ex2(fmaf(x[k + 1], P.scale_log2, -m_used));
-        ls0 += a;
-        ls1 += c;
+        float t0, t1;
+        f2_unpack(f2_fma(f2_pack(x[k], x[k + 1]), sc2, nm2), t0, t1);
+        const float a = ex2(t0), c = ex2(t1);
+        acc[(k >> 1) & 1] = f2_add(acc[(k >> 1) & 1], f2_pack(a, c));
         packed[k >> 1] = pack_bf16x2(a, c);
       }
-      l += ls0 + ls1;
+      float s0, s1, s2, s3;
+      f2_unpack(acc[0], s0, s1);
+      f2_unpack(acc[1], s2, s3);
+      l += (s0 + s1) + (s2 + s3);
       uint8_t *prow = smem + C::kOffP + h * 128;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
