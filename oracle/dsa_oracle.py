@@ -44,6 +44,11 @@ design notes):
       the softmax denominator only; absent means no term.
   R8  KV rows stay in full flat order; request b's key s is flat row qs_b + s.
   R9  a prefix (seq_len != query length, i.e. chunked prefill) is rejected.
+  R10 the head/token all-to-all after the attention ([xLLM] 单层前向数据流 (6))
+      leaves rank r' with heads r'*H/cp .. (r'+1)*H/cp - 1 of every real token,
+      tokens in flat order for both split modes (for in-seq-split the
+      rank-major order already is the flat order; for round-robin the rows are
+      put back in flat order as by rerange); H must divide by cp.
 
 parity pins: every function here is pinned by tests/test_oracle_pins.py
 against worked examples from the pages (tests/golden/), closed forms,
@@ -209,6 +214,30 @@ def rerange(y: np.ndarray, num_tokens: int, cp_size: int, mode: int) -> np.ndarr
         for i, g in enumerate(local_rows(num_tokens, cp_size, r, mode)):
             if g >= 0:
                 out[g] = y[r, i]
+    return out
+
+
+def all_to_all_heads(y: np.ndarray, num_tokens: int, cp_size: int, mode: int) -> np.ndarray:
+    """Head/token transpose of the views' attention outputs (R10).
+
+    [xLLM] 单层前向数据流 (6) and "3. DSAttention 前向": each rank holds its
+    attention output [T_local padded to tokens_per_rank, num_heads_full,
+    head_dim]; an all_to_all that scatters the head dimension and gathers the
+    token dimension leaves rank r' with [tokens, num_heads_full / cp_size,
+    head_dim], the pad rows sliced off, ready for the tensor-parallel o_proj.
+    y [cp][tpr][H][Dv] -> [cp][num_tokens][H / cp][Dv].
+    """
+    H = y.shape[2]
+    if H % cp_size:
+        raise ValueError("the head count must divide by cp_size")
+    hc = H // cp_size
+    out = np.zeros((cp_size, num_tokens, hc) + y.shape[3:], dtype=y.dtype)
+    for r in range(cp_size):  # the view that computed the token
+        for i, g in enumerate(local_rows(num_tokens, cp_size, r, mode)):
+            if g < 0:
+                continue
+            for rd in range(cp_size):  # the rank that receives heads rd*hc ..
+                out[rd, g] = y[r, i, rd * hc:(rd + 1) * hc]
     return out
 
 

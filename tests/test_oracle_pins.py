@@ -66,6 +66,54 @@ def test_round_robin_counts_differ_by_at_most_one(T, cp):
     assert sum(counts) == T and max(counts) - min(counts) <= 1
 
 
+# ---------------------------------------------------------------- head/token all-to-all
+
+def test_all_to_all_hand_example():
+    # 3 tokens, cp 2, 2 heads, head_dim 2; y[r][i][h][d] = 1000r + 100i + 10h + d
+    y = np.zeros((2, 2, 2, 2), dtype=np.int64)
+    for r in range(2):
+        for i in range(2):
+            for h in range(2):
+                for d in range(2):
+                    y[r, i, h, d] = 1000 * r + 100 * i + 10 * h + d
+    names = {"in_seq": IN_SEQ_SPLIT, "round_robin": ROUND_ROBIN}
+    outs = {m: O.all_to_all_heads(y, 3, 2, mode) for m, mode in names.items()}
+    lines = read_golden_lines("all_to_all_hand_example.txt")
+    assert len(lines) == 12
+    for line in lines:
+        m, rank, tok, d0, d1 = line.split()
+        assert list(outs[m][int(rank), int(tok), 0]) == [int(d0), int(d1)], line
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T,cp,H", [(1, 1, 4), (7, 2, 4), (13, 4, 8), (5, 8, 8), (33, 4, 128)])
+def test_all_to_all_of_split_is_a_head_transpose(T, cp, H, mode):
+    # split then all-to-all == reshaping the full [T][H][Dv] tensor into
+    # [T][cp][H/cp][Dv] and moving the rank axis first (plain numpy)
+    rng = np.random.default_rng(T * 100 + cp)
+    x = rng.integers(-1000, 1000, size=(T, H, 3))
+    out = O.all_to_all_heads(O.split(x, cp, mode), T, cp, mode)
+    assert np.array_equal(out, np.moveaxis(x.reshape(T, cp, H // cp, 3), 1, 0))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_all_to_all_is_a_permutation_of_the_real_rows(mode):
+    T, cp, H = 10, 4, 8
+    _, tpr = O.padded_geometry(T, cp)
+    y = np.arange(1, cp * tpr * H * 2 + 1, dtype=np.int64).reshape(cp, tpr, H, 2)
+    out = O.all_to_all_heads(y, T, cp, mode)
+    real = np.concatenate([y[r, O.local_rows(T, cp, r, mode) >= 0].ravel() for r in range(cp)])
+    assert out.shape == (cp, T, H // cp, 2)
+    assert np.array_equal(np.sort(out.ravel()), np.sort(real))
+
+
+def test_all_to_all_cp1_is_identity_and_rejects_indivisible_heads():
+    x = np.arange(5 * 6 * 2).reshape(5, 6, 2)
+    assert np.array_equal(O.all_to_all_heads(x[None], 5, 1, IN_SEQ_SPLIT)[0], x)
+    with pytest.raises(ValueError):
+        O.all_to_all_heads(O.split(x, 4, ROUND_ROBIN), 5, 4, ROUND_ROBIN)
+
+
 # ---------------------------------------------------------------- metadata
 
 _CASES = {"A": [5, 3, 4], "B": [3, 4], "C": [5, 1]}
