@@ -350,6 +350,47 @@ def run_ours(args, wl, mode, rank, world):
             e2e_ms.append(e0.elapsed_time(e1))
     dsa.dsa_poll_device_error()
 
+    # data-movement steps and the head-sharded output, each timed on its own
+    # (cold L2, outside the timed step): a2 split, a6 rerange, the head/token
+    # all-to-all as a separate pass, and a3-a5 with the all-to-all fused into
+    # the attention's stores
+    def timed(fn, reps=5):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def fused_core():
+        hs = pipe._head_sharded_buffer()
+        for r in range(wl.cp_size):
+            dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], x["k_idx"], pipe.w_split[r], pipe.topk,
+                                 pipe.max_kv_len, pipe.topk_idx[r], pipe.workspace)
+            dsa.dsa_sparse_attn_prefill_headsharded(pipe.md[r], pipe.q_split[r], x["kv"], pipe.topk_idx[r],
+                                                    pipe.scale, pipe.Dv, wl.cp_size, hs, x["sink"])
+
+    pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
+    T, pad = wl.num_tokens, pipe.pad
+    split_bytes = (T + pad) * (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4)
+    out_bytes = 2 * T * wl.H * wl.Dv * 2
+    aux = {}
+    for name, fn, nbytes in (("a2_split", lambda: pipe.split(x["q"], x["q_idx"], x["w"]), split_bytes),
+                             ("a6_rerange", pipe.rerange, out_bytes),
+                             ("a2a_heads", pipe.all_to_all_heads, out_bytes)):
+        ms = timed(fn)
+        aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+                     "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
+    aux["note"] = ("a2a_heads: all views' [tpr][H][Dv] outputs -> [cp][T][H/cp][Dv] head-sharded; "
+                   "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores")
+    dsa.dsa_poll_device_error()
+
     launches = pipe.launches_per_step() * args.steps
     if rank != 0:
         return
@@ -374,6 +415,7 @@ def run_ours(args, wl, mode, rank, world):
                 "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
         "clocks": clocks,
         "gpu_launches": launches,
+        "aux": aux,
     }
     if not args.no_cpu_baseline:
         rows, secs, desc = oracle_rows(wl, mode, n_seconds=args.cpu_seconds)

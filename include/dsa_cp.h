@@ -157,6 +157,23 @@ dsa_status dsa_cp_split(const void *src, int64_t row_bytes, int32_t num_tokens, 
 dsa_status dsa_cp_rerange(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
                           dsa_cp_mode mode, void *dst, dsa_stream_t stream);
 
+/*
+ * Head/token all-to-all of the attention outputs ([xLLM] 单层前向数据流 (6)
+ * and "3. DSAttention 前向": all_to_all_4D with the head dimension scattered
+ * and the token dimension gathered, pad rows sliced off), emulated for all
+ * views on one device: from every view's output src [cp_size][tpr][num_heads]
+ * [head_bytes] (the rank-major layout, pad slots ignored) to
+ * dst [cp_size][num_tokens][num_heads / cp_size][head_bytes], where rank rd
+ * holds heads rd * num_heads / cp_size .. (rd + 1) * num_heads / cp_size - 1
+ * of every real token, tokens in flat order for both split modes (for
+ * round-robin the rows are put back in flat order as by dsa_cp_rerange).
+ * num_heads must divide by cp_size (else DSA_ERR_SHAPE).  A byte copy:
+ * results are bit-exact.  The caller owns both buffers; the call is
+ * asynchronous on `stream`.
+ */
+dsa_status dsa_cp_all_to_all_heads(const void *src, int32_t num_heads, int64_t head_bytes, int32_t num_tokens,
+                                   int32_t cp_size, dsa_cp_mode mode, void *dst, dsa_stream_t stream);
+
 /* Host only.  Recommended workspace bytes for dsa_indexer_topk: room for the
  * fp32 indexer scores of a block of local rows (rows x round_up(max_kv_len, 4)
  * x 4 bytes, at most 1 GiB, at least one 8-row tile).  Any size holding one
@@ -255,6 +272,23 @@ dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batc
                                    const int32_t *topk_idx, int32_t topk, const float *attn_sink,
                                    float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
                                    dsa_stream_t stream);
+
+/*
+ * dsa_sparse_attn_prefill with the head/token all-to-all fused into the
+ * output stores ([xLLM] 单层前向数据流 (4) then (6)): same inputs and
+ * arithmetic (the results are bit-identical to dsa_sparse_attn_prefill
+ * followed by dsa_cp_all_to_all_heads), but each head row is written
+ * straight to its place in out bf16 [cp_size][num_tokens][H / cp_size][Dv]:
+ * rank h / (H / cp_size), token local_token_pos[i], head h % (H / cp_size).
+ * Pad slots write nothing.  Every view of a batch writes into the same out;
+ * their rows do not overlap.  cp_size >= 1 (else DSA_ERR_INVALID_ARG) and H
+ * must divide by cp_size (else DSA_ERR_SHAPE).
+ */
+dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                               const void *q, const void *kv, int32_t num_tokens,
+                                               const int32_t *topk_idx, int32_t topk, const float *attn_sink,
+                                               float softmax_scale, int32_t H, int32_t D, int32_t Dv,
+                                               int32_t cp_size, void *out, dsa_stream_t stream);
 
 /* Synchronise `stream`, then return (and clear) the first error a kernel
  * recorded on the current device since the last poll: DSA_OK, or

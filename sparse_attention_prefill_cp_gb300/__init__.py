@@ -21,8 +21,8 @@ ROUND_ROBIN = 1
 __all__ = [
     "IN_SEQ_SPLIT", "ROUND_ROBIN", "DSAError", "CPLocalMetadata", "load",
     "dsa_cp_geometry", "dsa_cp_metadata_sizes", "dsa_cp_build_local_metadata", "dsa_cp_split",
-    "dsa_cp_rerange", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_indexer_scores",
-    "dsa_sparse_attn_prefill", "dsa_poll_device_error",
+    "dsa_cp_rerange", "dsa_cp_all_to_all_heads", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk",
+    "dsa_indexer_scores", "dsa_sparse_attn_prefill", "dsa_sparse_attn_prefill_headsharded", "dsa_poll_device_error",
 ]
 
 
@@ -149,6 +149,26 @@ def dsa_cp_rerange(src: torch.Tensor, num_tokens: int, cp_size: int, mode: int, 
     return out
 
 
+def dsa_cp_all_to_all_heads(src: torch.Tensor, num_tokens: int, cp_size: int, mode: int,
+                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """src [cp_size, tpr, H, ...] (every view's output) -> [cp_size, num_tokens, H / cp_size, ...]."""
+    if not src.is_cuda or not src.is_contiguous() or src.dim() < 3:
+        raise ValueError("src must be a contiguous CUDA tensor [cp_size, tpr, H, ...]")
+    _, tpr = dsa_cp_geometry(num_tokens, cp_size)
+    H = src.shape[2]
+    if tuple(src.shape[:2]) != (cp_size, tpr) or H % cp_size:
+        raise ValueError(f"src must be [cp_size={cp_size}, tpr={tpr}, H divisible by cp_size, ...]")
+    shape = (cp_size, num_tokens, H // cp_size) + tuple(src.shape[3:])
+    if out is None:
+        out = torch.empty(shape, dtype=src.dtype, device=src.device)
+    elif tuple(out.shape) != shape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {src.dtype} tensor of shape {shape}")
+    head = src[0, 0, 0].numel() * src.element_size()
+    check(load().dsa_cp_all_to_all_heads(_ptr(src), H, head, num_tokens, cp_size, mode, _ptr(out),
+                                         _stream(stream)), "dsa_cp_all_to_all_heads")
+    return out
+
+
 def dsa_indexer_topk_workspace_size(tokens_per_rank: int, max_kv_len: int, topk: int) -> int:
     n = C.c_size_t()
     check(load().dsa_indexer_topk_workspace_size(tokens_per_rank, max_kv_len, topk, C.byref(n)),
@@ -243,6 +263,31 @@ def dsa_sparse_attn_prefill(md: CPLocalMetadata, q: torch.Tensor, kv: torch.Tens
                                          _ptr(topk_idx), topk_idx.shape[1], _ptr(attn_sink), float(softmax_scale),
                                          H, D, Dv, _ptr(out), _stream(stream)),
           "dsa_sparse_attn_prefill")
+    return out
+
+
+def dsa_sparse_attn_prefill_headsharded(md: CPLocalMetadata, q: torch.Tensor, kv: torch.Tensor,
+                                        topk_idx: torch.Tensor, softmax_scale: float, Dv: int, cp_size: int,
+                                        out: torch.Tensor, attn_sink: torch.Tensor | None = None,
+                                        stream=None) -> torch.Tensor:
+    """As dsa_sparse_attn_prefill, writing into the head-sharded out bf16 [cp_size, T, H / cp_size, Dv]
+    (shared by every view of the batch; each view fills the rows of its own tokens)."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv, torch.bfloat16, "kv")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(out, torch.bfloat16, "out")
+    if attn_sink is not None:
+        _need(attn_sink, torch.float32, "attn_sink")
+    tpr, H, D = q.shape
+    if tpr != md.tokens_per_rank or kv.shape[1] != D or topk_idx.shape[0] != tpr:
+        raise ValueError("q / kv / topk_idx shapes do not match the view")
+    if cp_size < 1 or H % cp_size or tuple(out.shape) != (cp_size, kv.shape[0], H // cp_size, Dv):
+        raise ValueError("out must be [cp_size, T, H / cp_size, Dv] with H divisible by cp_size")
+    check(load().dsa_sparse_attn_prefill_headsharded(C.byref(md.struct), md.batch, tpr, _ptr(q), _ptr(kv),
+                                                     kv.shape[0], _ptr(topk_idx), topk_idx.shape[1],
+                                                     _ptr(attn_sink), float(softmax_scale), H, D, Dv, cp_size,
+                                                     _ptr(out), _stream(stream)),
+          "dsa_sparse_attn_prefill_headsharded")
     return out
 
 

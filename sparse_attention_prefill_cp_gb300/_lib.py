@@ -34,6 +34,8 @@ SIGNATURES = {
     "dsa_cp_split": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_int32, C.c_void_p,
                                c_stream]),
     "dsa_cp_rerange": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_void_p, c_stream]),
+    "dsa_cp_all_to_all_heads": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int,
+                                          C.c_void_p, c_stream]),
     "dsa_indexer_topk_workspace_size": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_size_t)]),
     "dsa_indexer_topk": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
@@ -47,6 +49,10 @@ SIGNATURES = {
     "dsa_sparse_attn_prefill": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                                           C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_float, C.c_int32,
                                           C.c_int32, C.c_int32, C.c_void_p, c_stream]),
+    "dsa_sparse_attn_prefill_headsharded": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_void_p,
+                                                      C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
+                                                      C.c_float, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                                      C.c_void_p, c_stream]),
     "dsa_poll_device_error": (C.c_int, [c_stream]),
     "dsa_poll_device_error_detail": (C.c_int, [c_stream, c_i32p]),
     "dsa_status_string": (C.c_char_p, [C.c_int]),

@@ -1,7 +1,9 @@
 // Split and rerange of the CP token layout ("[DeepSeek v3.2] 上下文并行详解",
 // sections 2.B and 第三部分; "NSA Prefill CP 中两次 All-Gather 的作用说明",
-// 第一次 All-Gather).  Both are row gathers: dst row d <- src row map(d), or
-// zeros when map(d) is a pad slot.  HBM-bound byte copies, bit-exact.
+// 第一次 All-Gather) and the head/token all-to-all of the attention outputs
+// ("feat: DeepSeek-V4 DSA context-parallel on NPU", 单层前向数据流 (6)).  All
+// are row gathers: dst row d <- the source row that map(d) points at, or zeros
+// when map(d) is a pad slot.  HBM-bound byte copies, bit-exact.
 //
 // Large rows (>= 2 KB, e.g. 147,456-byte attention-query rows): one CTA
 // copies a 16 KB piece of one row with 16-byte vectors, 8 loads in flight per
@@ -12,24 +14,41 @@
 namespace dsa {
 namespace {
 
+// Each map gives, for destination row d, the element offset of its source row
+// (in units of the copy's vector type; rows are `e` units long), or -1 for a
+// pad row that is written as zeros.
 struct SplitMap {  // dst [n_ranks][tpr] <- src [T]
   int64_t tpr, T;
   int32_t cp, rank, mode;  // rank < 0: all ranks
-  __device__ __forceinline__ int64_t operator()(int64_t d) const {
+  __device__ __forceinline__ int64_t operator()(int64_t d, int64_t e) const {
     const int64_t r = rank < 0 ? d / tpr : rank;
     const int64_t i = rank < 0 ? d - r * tpr : d;
     const int64_t g = (mode == DSA_CP_IN_SEQ_SPLIT) ? r * tpr + i : r + i * cp;
-    return g < T ? g : -1;
+    return g < T ? g * e : -1;
   }
 };
 
 struct RerangeMap {  // dst [T] <- src [cp][tpr]
   int64_t tpr;
   int32_t cp, mode;
-  __device__ __forceinline__ int64_t operator()(int64_t g) const {
+  __device__ __forceinline__ int64_t operator()(int64_t g, int64_t e) const {
     const int64_t r = (mode == DSA_CP_IN_SEQ_SPLIT) ? g / tpr : g % cp;
     const int64_t i = (mode == DSA_CP_IN_SEQ_SPLIT) ? g - r * tpr : g / cp;
-    return r * tpr + i;
+    return (r * tpr + i) * e;
+  }
+};
+
+// dst [cp][T][H / cp] head slices <- src [cp][tpr][H]: destination row
+// d = rd * T + g is heads rd * H / cp .. of token g, taken from the view that
+// computed g (its slot there as in RerangeMap); a row is H / cp heads long.
+struct HeadA2AMap {
+  int64_t tpr, T;
+  int32_t cp, mode;
+  __device__ __forceinline__ int64_t operator()(int64_t d, int64_t e) const {
+    const int64_t rd = d / T, g = d - rd * T;
+    const int64_t r = (mode == DSA_CP_IN_SEQ_SPLIT) ? g / tpr : g % cp;
+    const int64_t i = (mode == DSA_CP_IN_SEQ_SPLIT) ? g - r * tpr : g / cp;
+    return ((r * tpr + i) * cp + rd) * e;  // a token row is cp slices of e units
   }
 };
 
@@ -41,9 +60,9 @@ template <class T, class Map>
 __global__ void __launch_bounds__(kBigThreads) copy_rows_big(const T *__restrict__ src, T *__restrict__ dst,
                                                              int64_t elems_per_row, Map map) {
   const int64_t row = blockIdx.x;
-  const int64_t s = map(row);
+  const int64_t s = map(row, elems_per_row);
   const int64_t e0 = static_cast<int64_t>(blockIdx.y) * kBigChunk + threadIdx.x;
-  const T *sp = src + s * elems_per_row;
+  const T *sp = src + s;
   T *dp = dst + row * elems_per_row;
   T v[kBigUnroll];
 #pragma unroll
@@ -64,9 +83,9 @@ __global__ void __launch_bounds__(256) copy_rows_small(const T *__restrict__ src
                                                        int64_t elems_per_row, int64_t n_rows, Map map) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (row >= n_rows) return;
-  const int64_t s = map(row);
+  const int64_t s = map(row, elems_per_row);
   for (int64_t e = threadIdx.x & 31; e < elems_per_row; e += 32)
-    dst[row * elems_per_row + e] = s >= 0 ? src[s * elems_per_row + e] : T{};
+    dst[row * elems_per_row + e] = s >= 0 ? src[s + e] : T{};
 }
 
 template <class Map>
@@ -128,4 +147,21 @@ extern "C" dsa_status dsa_cp_rerange(const void *src, int64_t row_bytes, int32_t
   if (st != DSA_OK) return st;
   RerangeMap map{tpr, cp_size, static_cast<int32_t>(mode)};
   return launch_copy(src, dst, row_bytes, num_tokens, map, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsa_status dsa_cp_all_to_all_heads(const void *src, int32_t num_heads, int64_t head_bytes,
+                                              int32_t num_tokens, int32_t cp_size, dsa_cp_mode mode, void *dst,
+                                              dsa_stream_t stream) {
+  if (!src || !dst) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (cp_size < 1) return DSA_ERR_INVALID_ARG;
+  if (num_heads < 1 || num_heads % cp_size != 0 || head_bytes <= 0 || num_tokens < 0) return DSA_ERR_SHAPE;
+  int32_t pad = 0, tpr = 0;
+  dsa_status st = dsa_cp_geometry(num_tokens, cp_size, &pad, &tpr);
+  if (st != DSA_OK) return st;
+  const int64_t slice_bytes = head_bytes * (num_heads / cp_size);
+  if (slice_bytes > (int64_t{1} << 40) / cp_size) return DSA_ERR_SHAPE;
+  HeadA2AMap map{tpr, num_tokens, cp_size, static_cast<int32_t>(mode)};
+  return launch_copy(src, dst, slice_bytes, static_cast<int64_t>(cp_size) * num_tokens, map,
+                     reinterpret_cast<cudaStream_t>(stream));
 }

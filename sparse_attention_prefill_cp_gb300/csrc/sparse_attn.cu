@@ -39,6 +39,12 @@
 //
 // The tiny shapes (H = 8, D = 64, Dv = 48) run the same kernel on one CTA
 // with Q rows 8..127 zero-filled by the TMA.
+//
+// Output layouts: the view's [tpr][H][Dv] (pad rows zero), or, fused into the
+// epilogue's stores, the head-sharded layout that the head/token all-to-all
+// after the attention produces (单层前向数据流 (6)): [cp][T][H / cp][Dv], rank
+// rd holding heads rd * H / cp .. of every real token (pad slots write
+// nothing).
 #include "dsa_common.cuh"
 #include "internal.h"
 
@@ -105,9 +111,10 @@ struct AttnParams {
   const __nv_bfloat16 *kv;   // [T][D]
   const int32_t *topk_idx;   // [tpr][topk]
   const float *sink;         // [H] or nullptr
-  __nv_bfloat16 *out;        // [tpr][H][Dv]
+  __nv_bfloat16 *out;        // [tpr][H][Dv], or [cp][T][hc][Dv] when hc > 0
   float scale_log2;          // softmax_scale * log2(e)
   int32_t topk, H, D, Dv, num_tokens;
+  int32_t hc;                // heads per rank of the head-sharded output, 0 = view layout
   int *err;
 };
 
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *stg_free = staged + 2;             // [2] the bulk copy has read our tile (sender)
   uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (8 softmax warps)
   uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (8 warps)
-  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p
+  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p, [3] g
   float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,6 +178,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     misc[1] = base;
     misc[2] = p;
+    misc[3] = g;
     mbar_init(q_full, 1);
     mbar_init(q_ready, 8);
     for (int s = 0; s < C::kStages; ++s) {
@@ -208,8 +216,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   __nv_bfloat16 *out_row = P.out + (static_cast<int64_t>(slot) * P.H) * P.Dv + main_dim0;
 
   if (nb == 0) {
-    // pad slot: zero output rows
-    if (warp < 4 && tid < P.H) {
+    // pad slot: zero output rows (the head-sharded layout has none)
+    if (P.hc == 0 && warp < 4 && tid < P.H) {
       __nv_bfloat16 *o = out_row + static_cast<int64_t>(tid) * P.Dv;
       for (int c = 0; c < C::DVC; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
     }
@@ -549,6 +557,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (P.sink && h < P.H) l += ex2(P.sink[h] * 1.4426950408889634f - m_used);
       const float inv = 1.f / l;
       __nv_bfloat16 *o = out_row + static_cast<int64_t>(h) * P.Dv;
+      if (P.hc > 0) {  // head-sharded: rank h / hc, token g, head h % hc
+        const int rd = h / P.hc;
+        o = P.out + ((static_cast<int64_t>(rd) * P.num_tokens + misc[3]) * P.hc + (h - rd * P.hc)) * P.Dv +
+            main_dim0;
+      }
 #pragma unroll 1
       for (int c = w * (C::kOCols / 2); c < (w + 1) * (C::kOCols / 2); c += 32) {
         uint32_t r[32];
@@ -621,17 +634,18 @@ dsa_status launch_attn(const void *q, int32_t tpr, const AttnParams &P, cudaStre
 
 using namespace dsa;
 
-extern "C" dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
-                                              const void *q, const void *kv, int32_t num_tokens,
-                                              const int32_t *topk_idx, int32_t topk, const float *attn_sink,
-                                              float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
-                                              dsa_stream_t stream) {
+static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr, const void *q,
+                                   const void *kv, int32_t num_tokens, const int32_t *topk_idx, int32_t topk,
+                                   const float *attn_sink, float softmax_scale, int32_t H, int32_t D, int32_t Dv,
+                                   int32_t cp_size, void *out, dsa_stream_t stream) {
   if (!md || !q || !kv || !topk_idx || !out) return DSA_ERR_INVALID_ARG;
   if (!md->scalars || !md->local_query_start_loc || !md->local_req_kv_base || !md->local_token_pos)
     return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(topk_idx)) return DSA_ERR_INVALID_ARG;
   if (batch < 0 || tpr < 0 || num_tokens < 1 || topk < 1) return DSA_ERR_SHAPE;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return DSA_ERR_INVALID_ARG;
+  if (cp_size < 0) return DSA_ERR_INVALID_ARG;
+  if (cp_size > 0 && (H < 1 || H % cp_size != 0)) return DSA_ERR_SHAPE;
   if (tpr == 0) return DSA_OK;
   if (static_cast<int64_t>(tpr) * 2 > INT32_MAX) return DSA_ERR_SHAPE;
   const bool big = H == 128 && D == 576 && Dv == 512 && topk == 2048;
@@ -650,7 +664,28 @@ extern "C" dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, i
                D,
                Dv,
                num_tokens,
+               cp_size > 0 ? H / cp_size : 0,
                err};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return big ? launch_attn<BigAttn>(q, tpr, P, s) : launch_attn<TinyAttn>(q, tpr, P, s);
+}
+
+extern "C" dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                              const void *q, const void *kv, int32_t num_tokens,
+                                              const int32_t *topk_idx, int32_t topk, const float *attn_sink,
+                                              float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
+                                              dsa_stream_t stream) {
+  return sparse_attn_impl(md, batch, tpr, q, kv, num_tokens, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv, 0,
+                          out, stream);
+}
+
+extern "C" dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_metadata *md, int32_t batch,
+                                                          int32_t tpr, const void *q, const void *kv,
+                                                          int32_t num_tokens, const int32_t *topk_idx, int32_t topk,
+                                                          const float *attn_sink, float softmax_scale, int32_t H,
+                                                          int32_t D, int32_t Dv, int32_t cp_size, void *out,
+                                                          dsa_stream_t stream) {
+  if (cp_size < 1) return DSA_ERR_INVALID_ARG;
+  return sparse_attn_impl(md, batch, tpr, q, kv, num_tokens, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv,
+                          cp_size, out, stream);
 }

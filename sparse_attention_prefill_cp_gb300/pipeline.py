@@ -8,15 +8,21 @@ q local, KV full; "[DeepSeek v3.2] 上下文并行详解", 第三部分):
   a4  causal top-k       }
   a5  dsa_sparse_attn_prefill, per view
   a6  dsa_cp_rerange of the per-view outputs back to flat token order
-Buffers are allocated once at construction; ``run`` only launches kernels on
-the current stream.  The views emulate CP ranks: no collective is involved.
+``run_headsharded`` instead writes the attention outputs straight into the
+head-sharded layout [cp][T][H / cp][Dv] that the head/token all-to-all after
+the attention produces (单层前向数据流 (6)), with no a6;
+``all_to_all_heads`` is the same permutation as a separate pass over the
+per-view outputs.  Buffers are allocated once (the head-sharded one on first
+use); the methods only launch kernels on the current stream.  The views
+emulate CP ranks: no collective is involved.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (CPLocalMetadata, dsa_cp_build_local_metadata, dsa_cp_geometry, dsa_cp_rerange, dsa_cp_split,
-               dsa_indexer_topk, dsa_indexer_topk_workspace_size, dsa_sparse_attn_prefill)
+from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_metadata, dsa_cp_geometry,
+               dsa_cp_rerange, dsa_cp_split, dsa_indexer_topk, dsa_indexer_topk_workspace_size,
+               dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_headsharded)
 
 
 class DSAPrefill:
@@ -47,6 +53,7 @@ class DSAPrefill:
         self.out = torch.empty((self.T, H, Dv), dtype=torch.bfloat16, device=dev)
         ws = workspace_bytes or dsa_indexer_topk_workspace_size(tpr, self.max_kv_len, topk)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.out_hs = None  # [cp][T][H / cp][Dv], allocated on first use
 
     def launches_per_step(self) -> int:
         """Kernel launches of one ``run``: metadata per view, 3 splits, per view
@@ -95,4 +102,30 @@ class DSAPrefill:
         out = self.rerange(stream)
         if "end" in ev:
             ev["end"].record(s)
+        return out
+
+    def _head_sharded_buffer(self):
+        if self.out_hs is None:
+            if self.H % self.cp_size:
+                raise ValueError("the head count must divide by cp_size")
+            self.out_hs = torch.empty((self.cp_size, self.T, self.H // self.cp_size, self.Dv), dtype=torch.bfloat16,
+                                      device=self.device)
+        return self.out_hs
+
+    def all_to_all_heads(self, stream=None):
+        """The per-view outputs of the last ``run`` -> head-sharded [cp, T, H / cp, Dv]."""
+        return dsa_cp_all_to_all_heads(self.out_split, self.T, self.cp_size, self.mode, self._head_sharded_buffer(),
+                                       stream)
+
+    def run_headsharded(self, q, kv, q_idx, k_idx, w, sink=None, stream=None):
+        """a1, a2, then per view a3 + a4 + a5 with the attention writing the
+        head-sharded layout directly; returns out_hs [cp, T, H / cp, Dv]."""
+        out = self._head_sharded_buffer()
+        self.metadata(stream)
+        self.split(q, q_idx, w, stream)
+        for r in range(self.cp_size):
+            dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
+                             self.topk_idx[r], self.workspace, stream)
+            dsa_sparse_attn_prefill_headsharded(self.md[r], self.q_split[r], kv, self.topk_idx[r], self.scale,
+                                                self.Dv, self.cp_size, out, sink, stream)
         return out

@@ -91,3 +91,16 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.dsa_sparse_attn_prefill(C.byref(md), 1, 8, p, p, 16, p, 2048, None, C.c_float(-1.0), 128, 576,
                                        512, p, None) == 1
     assert lib.dsa_indexer_topk(None, 1, 8, 16, p, p, p, 16, 64, 128, 2048, p, p, 1 << 20, None) == 1
+    # head/token all-to-all: null, bad mode / cp, heads not divisible by cp
+    assert lib.dsa_cp_all_to_all_heads(None, 128, 1024, 10, 8, 0, p, None) == 1
+    assert lib.dsa_cp_all_to_all_heads(p, 128, 1024, 10, 8, 5, p, None) == 1
+    assert lib.dsa_cp_all_to_all_heads(p, 128, 1024, 10, 0, 0, p, None) == 1
+    assert lib.dsa_cp_all_to_all_heads(p, 128, 1024, 10, 3, 0, p, None) == 2
+    assert lib.dsa_cp_all_to_all_heads(p, 128, 0, 10, 8, 0, p, None) == 2
+    # fused head-sharded attention: cp_size < 1, heads not divisible by cp, uncompiled dims
+    assert lib.dsa_sparse_attn_prefill_headsharded(C.byref(md), 1, 8, p, p, 16, p, 2048, None, C.c_float(0.07), 128,
+                                                   576, 512, 0, p, None) == 1
+    assert lib.dsa_sparse_attn_prefill_headsharded(C.byref(md), 1, 8, p, p, 16, p, 2048, None, C.c_float(0.07), 128,
+                                                   576, 512, 3, p, None) == 2
+    assert lib.dsa_sparse_attn_prefill_headsharded(C.byref(md), 1, 8, p, p, 16, p, 2048, None, C.c_float(0.07), 64,
+                                                   576, 512, 2, p, None) == 3

@@ -106,6 +106,58 @@ def test_split_rerange_bit_exact(T, cp, row_shape, dtype, mode):
     assert torch.equal(z.cpu(), x)
 
 
+# ------------------------------------------------------------------ head/token all-to-all
+
+def _a2a_reference(y, T, cp, mode):
+    """[cp, tpr, H, Dv] -> [cp, T, H / cp, Dv] with torch's index_select on the
+    oracle's slot of every token (used where the full oracle is too large)."""
+    _, tpr = O.padded_geometry(T, cp)
+    perm = np.empty(T, dtype=np.int64)
+    for r in range(cp):
+        for i, g in enumerate(O.local_rows(T, cp, r, mode)):
+            if g >= 0:
+                perm[g] = r * tpr + i
+    H, Dv = y.shape[2], y.shape[3]
+    flat = y.reshape(cp * tpr, H, Dv).index_select(0, torch.from_numpy(perm).to(y.device))
+    return flat.view(T, cp, H // cp, Dv).permute(1, 0, 2, 3).contiguous()
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T,cp,H,Dv", [(256, 2, 8, 48), (13, 4, 8, 48), (5, 8, 8, 48), (37, 16, 128, 512),
+                                       (300, 8, 128, 512), (11805, 4, 128, 512), (8192, 8, 128, 512)])
+def test_all_to_all_heads_bit_exact(T, cp, H, Dv, mode):
+    _, tpr = O.padded_geometry(T, cp)
+    g = torch.Generator(device="cuda").manual_seed(T * 31 + cp)
+    y = torch.randn((cp, tpr, H, Dv), generator=g, device="cuda").to(torch.bfloat16)
+    got = dsa.dsa_cp_all_to_all_heads(y, T, cp, mode)
+    dsa.dsa_poll_device_error()
+    assert got.shape == (cp, T, H // cp, Dv)
+    if y.numel() <= 4_000_000:  # the whole output against the oracle, bit for bit
+        ref = O.all_to_all_heads(y.cpu().view(torch.int16).numpy(), T, cp, mode)
+        assert np.array_equal(got.cpu().view(torch.int16).numpy(), ref)
+    assert torch.equal(got.view(torch.int16), _a2a_reference(y, T, cp, mode).view(torch.int16))
+
+
+@pytest.mark.parametrize("wl,mode", [(TINY, IN_SEQ_SPLIT), (TINY, ROUND_ROBIN),
+                                     (TINY.with_(name="tiny-sink", sink=True), ROUND_ROBIN),
+                                     (VARLEN_4, ROUND_ROBIN), (LONG_8K, IN_SEQ_SPLIT)], ids=lambda v: str(v)[:12])
+def test_fused_headsharded_attention_is_bit_identical(wl, mode):
+    """The attention writing the head-sharded layout directly equals the view
+    layout followed by the all-to-all, bit for bit, and writes every element."""
+    x = draw_inputs(wl, device="cuda")
+    pipe, _ = run_pipeline(wl, mode, x)
+    ref = pipe.all_to_all_heads().clone()
+    pipe.out_hs.view(torch.int16).fill_(0x7FC1)  # a NaN pattern no output has
+    got = pipe.run_headsharded(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
+    dsa.dsa_poll_device_error()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    if wl is TINY:  # and the all-to-all of the reranged output is the oracle's transpose of it
+        T, cp = wl.num_tokens, wl.cp_size
+        full = pipe.out.cpu().view(torch.int16).numpy()
+        exp = np.moveaxis(full.reshape(T, cp, wl.H // cp, wl.Dv), 1, 0)
+        assert np.array_equal(ref.cpu().view(torch.int16).numpy(), exp)
+
+
 # ------------------------------------------------------------------ indexer scores
 
 INT_FULL = LONG_8K.with_(name="int-full-2x", lengths=(2500, 700), cp_size=2, modes=MODES, integer=True, seed=9)
