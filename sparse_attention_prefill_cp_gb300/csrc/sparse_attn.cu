@@ -87,7 +87,7 @@ struct AttnCfg {
   static constexpr int kOffP = kOffStg + kRecvBytes;
   static constexpr int kOffRed = kOffP + kPBytes;             // [3][2 warpgroups][128] floats
   static constexpr int kOffBar = kOffRed + 3 * 2 * 128 * 4;
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 * 10 + 1;
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 * 10 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 32 + 1024;
   // the tiny variant asks for enough smem that at most two CTAs share an SM's TMEM
@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *stg_free = staged + 2;             // [2] the bulk copy has read our tile (sender)
   uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (8 softmax warps)
   uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (8 warps)
+  uint64_t *o_staged = fin_full + 1;           // normalised O rows staged in smem (8 warps)
   int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p, [3] g
   float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&consumed[b], 8);
     }
     mbar_init(fin_full, 8);
+    mbar_init(o_staged, 8);
     fence_mbar_init();
   }
   if (warp == 8) {
@@ -555,13 +557,54 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (ok) {
       tc_fence_after();
       if (P.sink && h < P.H) l += ex2(P.sink[h] * 1.4426950408889634f - m_used);
-      const float inv = 1.f / l;
-      __nv_bfloat16 *o = out_row + static_cast<int64_t>(h) * P.Dv;
-      if (P.hc > 0) {  // head-sharded: rank h / hc, token g, head h % hc
-        const int rd = h / P.hc;
-        o = P.out + ((static_cast<int64_t>(rd) * P.num_tokens + misc[3]) * P.hc + (h - rd * P.hc)) * P.Dv +
-            main_dim0;
+    }
+    const float inv = 1.f / l;
+    // destination of output row hh (this CTA's value columns)
+    auto out_of = [&](int hh) -> __nv_bfloat16 * {
+      if (P.hc > 0) {  // head-sharded: rank hh / hc, token g, head hh % hc
+        const int rd = hh / P.hc;
+        return P.out + ((static_cast<int64_t>(rd) * P.num_tokens + misc[3]) * P.hc + (hh - rd * P.hc)) * P.Dv +
+               main_dim0;
       }
+      return out_row + static_cast<int64_t>(hh) * P.Dv;
+    };
+    if constexpr (C::SPLIT) {
+      // Normalised rows go through shared memory (stages 0-1, free once every
+      // PV is done): thread h writes its row's 16-byte units, unit u of row h
+      // at u ^ (h & 31) so that neither the row-wise writes nor the column-wise
+      // reads below collide on banks; then each warp stores whole 512-byte rows
+      // with one coalesced instruction per row.
+      static_assert(C::DVC == 256, "one 512-byte row per CTA");
+      uint8_t *ost = smem + C::kOffStage;
+      if (ok) {
+#pragma unroll 1
+        for (int c = w * (C::kOCols / 2); c < (w + 1) * (C::kOCols / 2); c += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            const int u = (c + k) >> 3;
+            *reinterpret_cast<uint4 *>(ost + h * 512 + ((u ^ (h & 31)) << 4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(r[k + 0]) * inv, __uint_as_float(r[k + 1]) * inv),
+                           pack_bf16x2(__uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv),
+                           pack_bf16x2(__uint_as_float(r[k + 4]) * inv, __uint_as_float(r[k + 5]) * inv),
+                           pack_bf16x2(__uint_as_float(r[k + 6]) * inv, __uint_as_float(r[k + 7]) * inv));
+          }
+        }
+      }
+      warp_arrive(o_staged, lane);
+      ok = __all_sync(0xffffffffu, mbar_wait(o_staged, 0, P.err, 39) && ok);
+      if (ok) {
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const int hh = warp + 8 * k;
+          const uint4 v = *reinterpret_cast<const uint4 *>(ost + hh * 512 + ((lane ^ (hh & 31)) << 4));
+          *reinterpret_cast<uint4 *>(out_of(hh) + lane * 8) = v;
+        }
+      }
+    } else if (ok) {  // tiny shapes: rows stored directly
+      __nv_bfloat16 *o = out_of(h);
 #pragma unroll 1
       for (int c = w * (C::kOCols / 2); c < (w + 1) * (C::kOCols / 2); c += 32) {
         uint32_t r[32];
