@@ -44,6 +44,13 @@ design notes):
       the softmax denominator only; absent means no term.
   R8  KV rows stay in full flat order; request b's key s is flat row qs_b + s.
   R9  a prefix (seq_len != query length, i.e. chunked prefill) is rejected.
+  R11 head-tail in-seq-split (only named by [xLLM] 7, as a worker-side split):
+      the zigzag split.  tokens_per_rank is as for the other modes; the first
+      cp*ceil(tpr/2) padded rows are cut into head chunks of ceil(tpr/2) rows
+      (rank r: chunk r), the rest into tail chunks of floor(tpr/2) rows given
+      out in reverse rank order (rank r: chunk cp-1-r), so a rank pairs an early
+      (short-context) chunk with a late one; a rank's slots are its head rows
+      then its tail rows, i.e. ascending flat order.
   R10 the head/token all-to-all after the attention ([xLLM] 单层前向数据流 (6))
       leaves rank r' with heads r'*H/cp .. (r'+1)*H/cp - 1 of every real token,
       tokens in flat order for both split modes (for in-seq-split the
@@ -60,6 +67,7 @@ import numpy as np
 
 IN_SEQ_SPLIT = 0
 ROUND_ROBIN = 1
+HEAD_TAIL = 2
 
 
 # --------------------------------------------------------------------------
@@ -87,16 +95,23 @@ def local_rows(num_tokens: int, cp_size: int, cp_rank: int, mode: int) -> np.nda
       the flattened stream is cut evenly, padding at the end (R1, R2).
     round-robin: [blog] 2.B -- rank r holds arange(r, tokens, cp_size), i.e.
       token g goes to rank g % cp_size, slot g // cp_size (R3).
+    head-tail: the zigzag split of R11 ([xLLM] 7 names it only).
     """
     if not 0 <= cp_rank < cp_size:
         raise ValueError("cp_rank out of range")
     _, tpr = padded_geometry(num_tokens, cp_size)
+    head, tail = (tpr + 1) // 2, tpr // 2  # R11: head and tail chunk lengths
     rows = np.full(tpr, -1, dtype=np.int64)
     for i in range(tpr):
         if mode == IN_SEQ_SPLIT:
             g = cp_rank * tpr + i
         elif mode == ROUND_ROBIN:
             g = cp_rank + i * cp_size
+        elif mode == HEAD_TAIL:
+            if i < head:
+                g = cp_rank * head + i
+            else:
+                g = cp_size * head + (cp_size - 1 - cp_rank) * tail + (i - head)
         else:
             raise ValueError("unknown mode")
         if g < num_tokens:
@@ -140,6 +155,11 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
     if mode == IN_SEQ_SPLIT:
         local_start = min(cp_rank * tpr, T)
         local_end = min((cp_rank + 1) * tpr, T)
+    elif mode == HEAD_TAIL:
+        # the span from the head chunk's start to the tail chunk's end (R11)
+        head, tail = (tpr + 1) // 2, tpr // 2
+        local_start = min(cp_rank * head, T)
+        local_end = max(local_start, min(cp_size * head + (cp_size - cp_rank) * tail, T))
     else:
         # the strided range {local_start + i*cp_size < local_end}
         local_start = min(cp_rank, T)

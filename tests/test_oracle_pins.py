@@ -15,9 +15,9 @@ import torch
 
 from conftest import read_golden, read_golden_lines
 from oracle import dsa_oracle as O
-from workloads import IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, draw_inputs
+from workloads import HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, draw_inputs
 
-MODES = (IN_SEQ_SPLIT, ROUND_ROBIN)
+MODES = (IN_SEQ_SPLIT, ROUND_ROBIN, HEAD_TAIL)
 
 
 def _f64(t):
@@ -64,6 +64,36 @@ def test_split_rerange_identity_and_padding(T, cp, mode):
 def test_round_robin_counts_differ_by_at_most_one(T, cp):
     counts = [int(np.sum(O.local_rows(T, cp, r, ROUND_ROBIN) >= 0)) for r in range(cp)]
     assert sum(counts) == T and max(counts) - min(counts) <= 1
+
+
+def test_head_tail_hand_examples():
+    # zigzag: tokens_per_rank as for the other modes; head chunks of ceil(tpr/2)
+    # rows, tail chunks of floor(tpr/2) rows in reverse rank order
+    assert O.local_rows(10, 2, 0, HEAD_TAIL).tolist() == [0, 1, 2, 8, 9]
+    assert O.local_rows(10, 2, 1, HEAD_TAIL).tolist() == [3, 4, 5, 6, 7]
+    assert O.local_rows(9, 2, 0, HEAD_TAIL).tolist() == [0, 1, 2, 8, -1]
+    assert O.local_rows(8, 2, 0, HEAD_TAIL).tolist() == [0, 1, 6, 7]
+    assert O.local_rows(8, 2, 1, HEAD_TAIL).tolist() == [2, 3, 4, 5]
+
+
+@pytest.mark.parametrize("T,cp", [(16, 2), (64, 4), (96, 8), (48, 3)])
+def test_head_tail_is_the_textbook_zigzag_for_even_chunks(T, cp):
+    # with T a multiple of 2*cp, rank r holds equal chunks r and 2cp-1-r of the
+    # stream cut into 2cp pieces (numpy's array_split)
+    chunks = np.array_split(np.arange(T), 2 * cp)
+    for r in range(cp):
+        want = np.concatenate([chunks[r], chunks[2 * cp - 1 - r]])
+        assert np.array_equal(O.local_rows(T, cp, r, HEAD_TAIL), want)
+
+
+@pytest.mark.parametrize("T,cp", [(11805, 4), (65536, 8), (184265, 16)])
+def test_head_tail_balances_causal_work(T, cp):
+    # the sum of in-stream positions (a proxy for causal attention work) per rank
+    # is far more even than with the contiguous in-seq-split
+    def spread(mode):
+        work = [int(np.sum(r[r >= 0])) for r in (O.local_rows(T, cp, k, mode) for k in range(cp))]
+        return max(work) / max(1, min(work))
+    assert spread(HEAD_TAIL) < 1.2 < spread(IN_SEQ_SPLIT)
 
 
 # ---------------------------------------------------------------- head/token all-to-all
@@ -134,7 +164,7 @@ def test_metadata_hand_cases():
         head, lqs, kvl, lkv, rid, base, pos = line.split("|")
         case, mode_s, rank = head.split()
         lengths = _CASES[case]
-        mode = IN_SEQ_SPLIT if mode_s == "inseq" else ROUND_ROBIN
+        mode = {"inseq": IN_SEQ_SPLIT, "rr": ROUND_ROBIN, "ht": HEAD_TAIL}[mode_s]
         md = O.build_local_metadata(_qsl(lengths), lengths, _CP[case], int(rank), mode)
         assert md["local_query_start_loc"] == _ints(lqs), line
         assert md["local_seq_lens"] == _ints(kvl), line

@@ -33,7 +33,8 @@ import torch
 
 IN_SEQ_SPLIT = 0
 ROUND_ROBIN = 1
-MODE_NAMES = {IN_SEQ_SPLIT: "in-seq-split", ROUND_ROBIN: "round-robin-split"}
+HEAD_TAIL = 2
+MODE_NAMES = {IN_SEQ_SPLIT: "in-seq-split", ROUND_ROBIN: "round-robin-split", HEAD_TAIL: "head-tail-split"}
 
 
 def mixed_lengths(seed: int = 4, n: int = 16, lo: int = 512, hi: int = 32768) -> tuple:
