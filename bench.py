@@ -9,7 +9,7 @@ in HBM before the timed region (``value``); ``e2e`` repeats the step through
 pinned host buffers with the copies inside the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME] [--mode in-seq|round-robin]
+                       [--workload NAME] [--mode in-seq|round-robin|head-tail]
 Under torchrun each rank runs its own batch (weak scaling); rank 0 prints
 one JSON line.
 """
@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
-    ap.add_argument("--mode", choices=["in-seq", "round-robin"], default=None)
+    ap.add_argument("--mode", choices=["in-seq", "round-robin", "head-tail"], default=None)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -429,7 +429,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     wl = W.ALL[args.workload]
-    mode = wl.modes[0] if args.mode is None else (W.IN_SEQ_SPLIT if args.mode == "in-seq" else W.ROUND_ROBIN)
+    mode = wl.modes[0] if args.mode is None else {"in-seq": W.IN_SEQ_SPLIT, "round-robin": W.ROUND_ROBIN,
+                                                   "head-tail": W.HEAD_TAIL}[args.mode]
     if world > 1:
         backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
         torch.distributed.init_process_group(backend=backend)

@@ -56,7 +56,7 @@ typedef enum {
   DSA_ERR_DEVICE_PREFIX = 8   /* metadata: seq_lens != query lengths        */
 } dsa_status;
 
-typedef enum { DSA_CP_IN_SEQ_SPLIT = 0, DSA_CP_ROUND_ROBIN = 1 } dsa_cp_mode;
+typedef enum { DSA_CP_IN_SEQ_SPLIT = 0, DSA_CP_ROUND_ROBIN = 1, DSA_CP_HEAD_TAIL = 2 } dsa_cp_mode;
 
 /* Indices into dsa_cp_local_metadata.scalars. */
 enum {
@@ -130,6 +130,12 @@ dsa_status dsa_cp_metadata_bind(int32_t *buffer, int32_t batch, int32_t num_toke
  * cp_size):
  *   DSA_CP_IN_SEQ_SPLIT: rank r holds rows [r*tpr, (r+1)*tpr)
  *   DSA_CP_ROUND_ROBIN:  rank r holds rows g with g % cp_size == r, slot g / cp_size.
+ *   DSA_CP_HEAD_TAIL:    the zigzag split ([xLLM] "7. Worker 侧 gate" names
+ *                        "head-tail" only): with h = ceil(tpr/2), t = floor(tpr/2),
+ *                        rank r holds rows [r*h, (r+1)*h) then
+ *                        [cp*h + (cp-1-r)*t, cp*h + (cp-r)*t), both clipped to
+ *                        [0, num_tokens) -- an early chunk paired with a late one,
+ *                        which evens out the causal work.
  * cp_size == 1 gives the identity view.
  */
 dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc, const int32_t *seq_lens,

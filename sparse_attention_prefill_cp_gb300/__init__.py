@@ -17,9 +17,10 @@ from ._lib import DSAError, LocalMetadata, check, load  # noqa: F401
 
 IN_SEQ_SPLIT = 0
 ROUND_ROBIN = 1
+HEAD_TAIL = 2
 
 __all__ = [
-    "IN_SEQ_SPLIT", "ROUND_ROBIN", "DSAError", "CPLocalMetadata", "load",
+    "IN_SEQ_SPLIT", "ROUND_ROBIN", "HEAD_TAIL", "DSAError", "CPLocalMetadata", "load",
     "dsa_cp_geometry", "dsa_cp_metadata_sizes", "dsa_cp_build_local_metadata", "dsa_cp_split",
     "dsa_cp_rerange", "dsa_cp_all_to_all_heads", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk",
     "dsa_indexer_scores", "dsa_sparse_attn_prefill", "dsa_sparse_attn_prefill_headsharded", "dsa_poll_device_error",

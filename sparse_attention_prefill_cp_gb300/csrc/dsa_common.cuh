@@ -418,6 +418,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// CP split geometry: the flat row of local slot i of rank r, and its inverse.
+// tpr = tokens_per_rank.  In-seq-split: contiguous chunks of tpr rows;
+// round-robin: row g on rank g % cp, slot g / cp; head-tail (zigzag): head
+// chunks of h = ceil(tpr/2) rows for ranks 0..cp-1, then tail chunks of
+// t = floor(tpr/2) rows for ranks cp-1..0, a rank's slots being its head rows
+// then its tail rows.  Rows >= the token count are pad slots.
+__host__ __device__ __forceinline__ int64_t cp_row_of_slot(int64_t r, int64_t i, int64_t tpr, int64_t cp,
+                                                           int mode) {
+  if (mode == DSA_CP_IN_SEQ_SPLIT) return r * tpr + i;
+  if (mode == DSA_CP_ROUND_ROBIN) return r + i * cp;
+  const int64_t h = (tpr + 1) / 2, t = tpr / 2;
+  return i < h ? r * h + i : cp * h + (cp - 1 - r) * t + (i - h);
+}
+__host__ __device__ __forceinline__ void cp_slot_of_row(int64_t g, int64_t tpr, int64_t cp, int mode, int64_t &r,
+                                                        int64_t &i) {
+  if (mode == DSA_CP_IN_SEQ_SPLIT) {
+    r = g / tpr;
+    i = g - r * tpr;
+  } else if (mode == DSA_CP_ROUND_ROBIN) {
+    r = g % cp;
+    i = g / cp;
+  } else {
+    const int64_t h = (tpr + 1) / 2, t = tpr / 2, half = cp * h;
+    if (g < half) {
+      r = g / h;
+      i = g - r * h;
+    } else {  // t > 0 here: with t == 0 every row lies in the head chunks
+      const int64_t u = g - half, q = u / t;
+      r = cp - 1 - q;
+      i = h + (u - q * t);
+    }
+  }
+}
+
 // Local request j holding local slot `slot`: local_query_start_loc[j] <= slot < [j+1].
 __device__ __forceinline__ int find_local_request(const int32_t *lqs, int nreq, int slot) {
   int lo = 0, hi = nreq;  // answer in [lo, hi)

@@ -4,8 +4,10 @@
 //
 // One CTA per call.  Per request b the number of local rows and the last
 // local position come from closed forms (an interval intersection for
-// in-seq-split, an arithmetic progression for round-robin); a block-wide
-// exclusive scan compacts the requests that have local rows.
+// in-seq-split, two for the head-tail zigzag, an arithmetic progression for
+// round-robin); a block-wide exclusive scan compacts the requests that have
+// local rows.  In every mode a rank's slots are in ascending flat order, so
+// the local rows of a request are consecutive slots.
 #include "dsa_common.cuh"
 #include "internal.h"
 
@@ -83,8 +85,12 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
   // local slot -> flat token row
   const int64_t lo_inseq = static_cast<int64_t>(rank) * tpr;
   const int64_t hi_inseq = lo_inseq + tpr < T ? lo_inseq + tpr : T;
+  // head-tail: the head chunk [lo_h, hi_h) and the tail chunk [lo_t, hi_t), clipped to T
+  const int64_t ch = (tpr + 1) / 2, ct = tpr / 2;
+  const int64_t lo_h = static_cast<int64_t>(rank) * ch, lo_t = cp * ch + (cp - 1 - rank) * ct;
+  const int64_t hi_h = lo_h + ch < T ? lo_h + ch : T, hi_t = lo_t + ct < T ? lo_t + ct : T;
   for (int64_t i = tid; i < tpr; i += kThreads) {
-    const int64_t g = (mode == DSA_CP_IN_SEQ_SPLIT) ? lo_inseq + i : rank + i * cp;
+    const int64_t g = cp_row_of_slot(rank, i, tpr, cp, mode);
     md.local_token_pos[i] = (!bad && g < T) ? static_cast<int32_t>(g) : -1;
   }
   if (tid == 0) {
@@ -107,6 +113,17 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
           if (hi > lo) {
             q_len = hi - lo;
             last = hi - 1;
+          }
+        } else if (mode == DSA_CP_HEAD_TAIL) {
+          const int64_t lo1 = qs > lo_h ? qs : lo_h, hi1 = qe < hi_h ? qe : hi_h;
+          const int64_t lo2 = qs > lo_t ? qs : lo_t, hi2 = qe < hi_t ? qe : hi_t;
+          if (hi1 > lo1) {
+            q_len += hi1 - lo1;
+            last = hi1 - 1;
+          }
+          if (hi2 > lo2) {  // the tail chunk lies after the head chunk
+            q_len += hi2 - lo2;
+            last = hi2 - 1;
           }
         } else {
           // first g >= qs with g % cp == rank
@@ -147,6 +164,11 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
     if (mode == DSA_CP_IN_SEQ_SPLIT) {
       s[DSA_MD_LOCAL_START] = static_cast<int32_t>(lo_inseq < T ? lo_inseq : T);
       s[DSA_MD_LOCAL_END] = static_cast<int32_t>(hi_inseq > lo_inseq ? hi_inseq : (lo_inseq < T ? lo_inseq : T));
+    } else if (mode == DSA_CP_HEAD_TAIL) {  // from the head chunk's start to the tail chunk's end
+      const int64_t st = lo_h < T ? lo_h : T;
+      const int64_t en = lo_t + ct < T ? lo_t + ct : T;
+      s[DSA_MD_LOCAL_START] = static_cast<int32_t>(st);
+      s[DSA_MD_LOCAL_END] = static_cast<int32_t>(en > st ? en : st);
     } else {
       s[DSA_MD_LOCAL_START] = rank < T ? rank : T;
       s[DSA_MD_LOCAL_END] = T;
@@ -169,7 +191,8 @@ extern "C" dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc
                                                   const dsa_cp_local_metadata *out, dsa_stream_t stream) {
   if (!query_start_loc || !seq_lens || !out) return DSA_ERR_INVALID_ARG;
   if (cp_size < 1 || cp_rank < 0 || cp_rank >= cp_size) return DSA_ERR_INVALID_ARG;
-  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN && mode != DSA_CP_HEAD_TAIL)
+    return DSA_ERR_INVALID_ARG;
   if (!out->scalars || !out->local_query_start_loc || !out->local_seq_lens || !out->local_kv_start_loc ||
       !out->local_req_id || !out->local_req_kv_base || !out->local_token_pos)
     return DSA_ERR_INVALID_ARG;

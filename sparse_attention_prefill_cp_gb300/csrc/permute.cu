@@ -23,7 +23,7 @@ struct SplitMap {  // dst [n_ranks][tpr] <- src [T]
   __device__ __forceinline__ int64_t operator()(int64_t d, int64_t e) const {
     const int64_t r = rank < 0 ? d / tpr : rank;
     const int64_t i = rank < 0 ? d - r * tpr : d;
-    const int64_t g = (mode == DSA_CP_IN_SEQ_SPLIT) ? r * tpr + i : r + i * cp;
+    const int64_t g = cp_row_of_slot(r, i, tpr, cp, mode);
     return g < T ? g * e : -1;
   }
 };
@@ -32,8 +32,8 @@ struct RerangeMap {  // dst [T] <- src [cp][tpr]
   int64_t tpr;
   int32_t cp, mode;
   __device__ __forceinline__ int64_t operator()(int64_t g, int64_t e) const {
-    const int64_t r = (mode == DSA_CP_IN_SEQ_SPLIT) ? g / tpr : g % cp;
-    const int64_t i = (mode == DSA_CP_IN_SEQ_SPLIT) ? g - r * tpr : g / cp;
+    int64_t r, i;
+    cp_slot_of_row(g, tpr, cp, mode, r, i);
     return (r * tpr + i) * e;
   }
 };
@@ -46,8 +46,8 @@ struct HeadA2AMap {
   int32_t cp, mode;
   __device__ __forceinline__ int64_t operator()(int64_t d, int64_t e) const {
     const int64_t rd = d / T, g = d - rd * T;
-    const int64_t r = (mode == DSA_CP_IN_SEQ_SPLIT) ? g / tpr : g % cp;
-    const int64_t i = (mode == DSA_CP_IN_SEQ_SPLIT) ? g - r * tpr : g / cp;
+    int64_t r, i;
+    cp_slot_of_row(g, tpr, cp, mode, r, i);
     return ((r * tpr + i) * cp + rd) * e;  // a token row is cp slices of e units
   }
 };
@@ -125,7 +125,8 @@ using namespace dsa;
 extern "C" dsa_status dsa_cp_split(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
                                    dsa_cp_mode mode, int32_t cp_rank, void *dst, dsa_stream_t stream) {
   if (!src || !dst) return DSA_ERR_INVALID_ARG;
-  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN && mode != DSA_CP_HEAD_TAIL)
+    return DSA_ERR_INVALID_ARG;
   if (cp_size < 1 || cp_rank < -1 || cp_rank >= cp_size) return DSA_ERR_INVALID_ARG;
   if (row_bytes <= 0 || num_tokens < 0) return DSA_ERR_SHAPE;
   int32_t pad = 0, tpr = 0;
@@ -139,7 +140,8 @@ extern "C" dsa_status dsa_cp_split(const void *src, int64_t row_bytes, int32_t n
 extern "C" dsa_status dsa_cp_rerange(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
                                      dsa_cp_mode mode, void *dst, dsa_stream_t stream) {
   if (!src || !dst) return DSA_ERR_INVALID_ARG;
-  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN && mode != DSA_CP_HEAD_TAIL)
+    return DSA_ERR_INVALID_ARG;
   if (cp_size < 1) return DSA_ERR_INVALID_ARG;
   if (row_bytes <= 0 || num_tokens < 0) return DSA_ERR_SHAPE;
   int32_t pad = 0, tpr = 0;
@@ -153,7 +155,8 @@ extern "C" dsa_status dsa_cp_all_to_all_heads(const void *src, int32_t num_heads
                                               int32_t num_tokens, int32_t cp_size, dsa_cp_mode mode, void *dst,
                                               dsa_stream_t stream) {
   if (!src || !dst) return DSA_ERR_INVALID_ARG;
-  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN && mode != DSA_CP_HEAD_TAIL)
+    return DSA_ERR_INVALID_ARG;
   if (cp_size < 1) return DSA_ERR_INVALID_ARG;
   if (num_heads < 1 || num_heads % cp_size != 0 || head_bytes <= 0 || num_tokens < 0) return DSA_ERR_SHAPE;
   int32_t pad = 0, tpr = 0;

@@ -16,11 +16,11 @@ import torch
 import sparse_attention_prefill_cp_gb300 as dsa
 from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill
 from oracle import dsa_oracle as O
-from workloads import (IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, LONG_8K, VARLEN_4, LONG_64K, MIXED_16,
+from workloads import (HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, LONG_8K, VARLEN_4, LONG_64K, MIXED_16,
                        Workload, draw_inputs, sample_rows)
 
 pytestmark = pytest.mark.gpu
-MODES = (IN_SEQ_SPLIT, ROUND_ROBIN)
+MODES = (IN_SEQ_SPLIT, ROUND_ROBIN, HEAD_TAIL)
 SCORE_TOL = 1e-3
 ATT_MAX_ABS, ATT_REL_L2 = 2e-2, 1e-2
 
@@ -138,7 +138,7 @@ def test_all_to_all_heads_bit_exact(T, cp, H, Dv, mode):
     assert torch.equal(got.view(torch.int16), _a2a_reference(y, T, cp, mode).view(torch.int16))
 
 
-@pytest.mark.parametrize("wl,mode", [(TINY, IN_SEQ_SPLIT), (TINY, ROUND_ROBIN),
+@pytest.mark.parametrize("wl,mode", [(TINY, IN_SEQ_SPLIT), (TINY, ROUND_ROBIN), (TINY, HEAD_TAIL),
                                      (TINY.with_(name="tiny-sink", sink=True), ROUND_ROBIN),
                                      (VARLEN_4, ROUND_ROBIN), (LONG_8K, IN_SEQ_SPLIT)], ids=lambda v: str(v)[:12])
 def test_fused_headsharded_attention_is_bit_identical(wl, mode):
@@ -350,7 +350,8 @@ def _device_inputs(wl):
 
 
 @pytest.mark.parametrize("wl,mode", [(LONG_8K, IN_SEQ_SPLIT), (VARLEN_4, ROUND_ROBIN), (MIXED_16, ROUND_ROBIN),
-                                     (MIXED_16, IN_SEQ_SPLIT), (LONG_64K, ROUND_ROBIN)],
+                                     (MIXED_16, IN_SEQ_SPLIT), (LONG_64K, ROUND_ROBIN), (LONG_8K, HEAD_TAIL),
+                                     (MIXED_16, HEAD_TAIL)],
                          ids=lambda v: v.name if isinstance(v, Workload) else str(v))
 def test_full_size_sampled_rows(wl, mode):
     xd = _device_inputs(wl)
