@@ -324,6 +324,8 @@ def run_ours(args, wl, mode, rank, world):
     # dominant kernel: the attention launches
     per_view_flops = view_attention_flops(wl, wl.cp_size, mode)
     attn_ms = [e0.elapsed_time(e1) for (_, e0, e1) in attn_events]
+    per_view = [statistics.mean([e0.elapsed_time(e1) for (rr, e0, e1) in attn_events if rr == r])
+                for r in range(wl.cp_size)]
     attn_flops = [per_view_flops[r] for (r, _, _) in attn_events]
     pk = peaks()
     achieved = (sum(attn_flops) / (sum(attn_ms) / 1e3)) / 1e12
@@ -416,6 +418,8 @@ def run_ours(args, wl, mode, rank, world):
         "clocks": clocks,
         "gpu_launches": launches,
         "aux": aux,
+        "views": {"attn_ms": per_view, "max_over_mean": max(per_view) / statistics.mean(per_view),
+                  "note": "attention time of each CP view; on one GPU per rank the slowest sets the pace"},
     }
     if not args.no_cpu_baseline:
         rows, secs, desc = oracle_rows(wl, mode, n_seconds=args.cpu_seconds)
