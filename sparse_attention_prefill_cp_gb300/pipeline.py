@@ -27,7 +27,7 @@ from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_meta
 
 class DSAPrefill:
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
-                 softmax_scale: float, device=None, workspace_bytes: int | None = None):
+                 softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1):
         self.device = torch.device(device or "cuda")
         self.lengths = [int(x) for x in lengths]
         self.cp_size, self.mode = int(cp_size), int(mode)
@@ -52,7 +52,12 @@ class DSAPrefill:
         self.out_split = torch.empty((cp, tpr, H, Dv), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((self.T, H, Dv), dtype=torch.bfloat16, device=dev)
         ws = workspace_bytes or dsa_indexer_topk_workspace_size(tpr, self.max_kv_len, topk)
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # views on several streams: one score workspace per stream, so that the
+        # tail of one view's kernels overlaps the start of the next view's
+        self.view_streams = max(1, int(view_streams))
+        self.workspaces = [torch.empty(ws, dtype=torch.uint8, device=dev) for _ in range(self.view_streams)]
+        self.workspace = self.workspaces[0]
+        self._side = None
         self.out_hs = None  # [cp][T][H / cp][Dv], allocated on first use
 
     def launches_per_step(self) -> int:
@@ -74,11 +79,37 @@ class DSAPrefill:
         dsa_cp_split(q_idx, self.cp_size, self.mode, -1, self.qi_split, stream)
         dsa_cp_split(w, self.cp_size, self.mode, -1, self.w_split, stream)
 
-    def view(self, r: int, kv, k_idx, sink=None, stream=None):          # a3 + a4 + a5
+    def view(self, r: int, kv, k_idx, sink=None, stream=None, workspace=None):  # a3 + a4 + a5
         dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
-                         self.topk_idx[r], self.workspace, stream)
+                         self.topk_idx[r], self.workspace if workspace is None else workspace, stream)
         dsa_sparse_attn_prefill(self.md[r], self.q_split[r], kv, self.topk_idx[r], self.scale, self.Dv, sink,
                                 self.out_split[r], stream)
+
+    def side_streams(self):
+        if self._side is None:
+            self._side = [torch.cuda.Stream(self.device) for _ in range(self.view_streams)]
+        return self._side
+
+    def views(self, kv, k_idx, sink, stream):
+        """Every view's a3-a5.  With one view stream they run in order on
+        ``stream``; with n > 1, view r runs on side stream r % n (forked from
+        and joined back into ``stream``), each with its own workspace."""
+        if self.view_streams == 1:
+            for r in range(self.cp_size):
+                self.view(r, kv, k_idx, sink, stream)
+            return
+        side = self.side_streams()
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for st in side:
+            st.wait_event(fork)
+        for r in range(self.cp_size):
+            k = r % self.view_streams
+            self.view(r, kv, k_idx, sink, side[k], self.workspaces[k])
+        for st in side:
+            join = torch.cuda.Event()
+            join.record(st)
+            stream.wait_event(join)
 
     def rerange(self, stream=None):                                     # a6
         return dsa_cp_rerange(self.out_split, self.T, self.cp_size, self.mode, self.out, stream)
@@ -95,8 +126,7 @@ class DSAPrefill:
         self.split(q, q_idx, w, stream)
         if "core_start" in ev:
             ev["core_start"].record(s)
-        for r in range(self.cp_size):
-            self.view(r, kv, k_idx, sink, stream)
+        self.views(kv, k_idx, sink, s)
         if "core_end" in ev:
             ev["core_end"].record(s)
         out = self.rerange(stream)
@@ -129,3 +159,85 @@ class DSAPrefill:
             dsa_sparse_attn_prefill_headsharded(self.md[r], self.q_split[r], kv, self.topk_idx[r], self.scale,
                                                 self.Dv, self.cp_size, out, sink, stream)
         return out
+
+
+class HostStreamedPrefill:
+    """Prefill batches that live in pinned host memory, with the copies
+    overlapped: while batch s computes, the inputs of batch s + 1 go up on one
+    copy stream and the output of batch s - 1 comes down on another.
+
+    ``depth`` sets of device buffers (one ``DSAPrefill`` each, inputs and
+    outputs) rotate, so a set is reused only after its last batch's output has
+    been read back.  ``submit`` only enqueues work; the caller synchronises (or
+    waits on ``done_event(s)``) before reading the host output of batch s.
+    Every compute step is the same sequence of library calls as
+    ``DSAPrefill.run``.
+    """
+
+    INPUTS = ("q", "kv", "q_idx", "k_idx", "w", "sink")
+
+    def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
+                 softmax_scale: float, device=None, depth: int = 2, view_streams: int = 1):
+        if depth < 1:
+            raise ValueError("depth must be at least 1")
+        self.pipes = [DSAPrefill(lengths, cp_size, mode, H, D, Dv, HI, DI, topk, softmax_scale, device,
+                                 view_streams=view_streams) for _ in range(depth)]
+        self.device = self.pipes[0].device
+        self.depth = depth
+        self.dev_in = [None] * depth
+        self.h2d = torch.cuda.Stream(self.device)
+        self.d2h = torch.cuda.Stream(self.device)
+        self.computed = [torch.cuda.Event() for _ in range(depth)]
+        self.read_back = [torch.cuda.Event() for _ in range(depth)]
+        self.in_ready = [torch.cuda.Event() for _ in range(depth)]
+        self._done = {}
+        self._submitted = 0
+
+    def _inputs(self, k, host):
+        if self.dev_in[k] is None:
+            self.dev_in[k] = {n: (torch.empty(host[n].shape, dtype=host[n].dtype, device=self.device)
+                                  if host.get(n) is not None else None) for n in self.INPUTS}
+        return self.dev_in[k]
+
+    def submit(self, host: dict, out_host: torch.Tensor, stream=None) -> int:
+        """Enqueue one batch: ``host`` maps q, kv, q_idx, k_idx, w (and sink or
+        None) to pinned CPU tensors; ``out_host`` is a pinned CPU tensor
+        [T, H, Dv] bf16 that receives the output.  Returns the batch number."""
+        s = self._submitted
+        k = s % self.depth
+        pipe = self.pipes[k]
+        for n in self.INPUTS:
+            t = host.get(n)
+            if t is not None and (t.device.type != "cpu" or not t.is_pinned()):
+                raise ValueError(f"{n}: pinned host memory expected")
+        if out_host.device.type != "cpu" or not out_host.is_pinned():
+            raise ValueError("out_host: pinned host memory expected")
+        compute = stream or torch.cuda.current_stream(self.device)
+        dev = self._inputs(k, host)
+        first_use = s < self.depth
+        # inputs of set k: free once the batch that used them has computed
+        if not first_use:
+            self.h2d.wait_event(self.computed[k])
+        with torch.cuda.stream(self.h2d):
+            for n in self.INPUTS:
+                if dev[n] is not None:
+                    dev[n].copy_(host[n], non_blocking=True)
+        self.in_ready[k].record(self.h2d)
+        compute.wait_event(self.in_ready[k])
+        if not first_use:
+            compute.wait_event(self.read_back[k])  # the output buffer of set k has been read back
+        out = pipe.run(dev["q"], dev["kv"], dev["q_idx"], dev["k_idx"], dev["w"], dev["sink"], stream=compute)
+        self.computed[k].record(compute)
+        self.d2h.wait_event(self.computed[k])
+        with torch.cuda.stream(self.d2h):
+            out_host.copy_(out, non_blocking=True)
+        self.read_back[k].record(self.d2h)
+        done = torch.cuda.Event(enable_timing=True)
+        done.record(self.d2h)
+        self._done[s] = done
+        self._submitted += 1
+        return s
+
+    def done_event(self, s: int) -> torch.cuda.Event:
+        """Recorded on the copy-out stream once batch s's output is on the host."""
+        return self._done[s]

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import sparse_attention_prefill_cp_gb300 as dsa
-from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill
+from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill, HostStreamedPrefill
 from oracle import dsa_oracle as O
 from workloads import (HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, LONG_8K, VARLEN_4, LONG_64K, MIXED_16,
                        Workload, draw_inputs, sample_rows)
@@ -298,6 +298,35 @@ def test_views_reproduce_single_view_bitwise(wl, mode):
     out_views = out_views.clone()
     _, out_single = run_pipeline(wl, mode, x, cp_size=1)
     assert torch.equal(out_views, out_single)
+
+
+@pytest.mark.parametrize("mode", (IN_SEQ_SPLIT, ROUND_ROBIN))
+def test_view_streams_and_host_streaming_are_bit_identical(mode):
+    # the same library calls on other streams: views spread over two streams,
+    # and batches streamed from pinned host memory with overlapped copies,
+    # give the single-stream output bit for bit (each batch its own inputs)
+    wl = FLOAT_FULL
+    xs = [draw_inputs(wl, device="cuda", seed_offset=b) for b in range(3)]
+    refs = []
+    for x in xs:
+        _, out = run_pipeline(wl, mode, x)
+        refs.append(out.clone())
+    pipe2 = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                       view_streams=2)
+    for x, ref in zip(xs, refs):
+        assert torch.equal(pipe2.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"]), ref)
+    hs = HostStreamedPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                             depth=2, view_streams=2)
+    hosts = [{k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()} for x in xs]
+    outs = [torch.empty((wl.num_tokens, wl.H, wl.Dv), dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    ids = [hs.submit(hosts[b % 3], outs[b]) for b in range(5)]
+    torch.cuda.synchronize()
+    dsa.dsa_poll_device_error()
+    for b, s in enumerate(ids):
+        assert hs.done_event(s).query()
+        assert torch.equal(outs[b], refs[b % 3].cpu()), b
+    with pytest.raises(ValueError):
+        hs.submit({k: (v.cpu() if v is not None else None) for k, v in xs[0].items()}, outs[0])
 
 
 def test_whole_path_integer_variant_matches_oracle():
