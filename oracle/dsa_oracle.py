@@ -43,7 +43,14 @@ design notes):
   R7  the sink is a logit already in scaled units that adds exp(sink - m) to
       the softmax denominator only; absent means no term.
   R8  KV rows stay in full flat order; request b's key s is flat row qs_b + s.
-  R9  a prefix (seq_len != query length, i.e. chunked prefill) is rejected.
+  R9  chunked prefill ([xLLM] 测试与验证 lists it; 单层前向数据流 (4) gives the
+      attention separate KV geometry: cu_seqlens_ori_kv, seqused_kv): request
+      b's queries are the last q_len_b positions of its sequence of
+      seq_lens[b] >= q_len_b tokens, after a prefix of seq_lens[b] - q_len_b
+      positions whose KV is already there.  KV and index keys hold every
+      request's whole sequence, requests in order: position s of request b is
+      KV row kv_start_b + s, kv_start_b = sum of seq_lens before b.  With no
+      prefix kv_start_b = qs_b and this is R8.
   R11 head-tail in-seq-split (only named by [xLLM] 7, as a worker-side split):
       the zigzag split.  tokens_per_rank is as for the other modes; the first
       cp*ceil(tpr/2) padded rows are cut into head chunks of ceil(tpr/2) rows
@@ -136,18 +143,25 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
     ends at their last position (right-aligned) (R4).
     [xLLM] 5: batch_size / max_seqlen_q are replaced by the local geometry.
 
-    Extras (R8): local_req_id (global request index), local_req_kv_base (flat
-    row of the request's first token) and local_token_pos (flat row of every
-    local slot, -1 for pad).
+    Extras (R8, R9): local_req_id (global request index), local_req_kv_base
+    (KV row of the request's position 0), local_req_pos_base (a local slot of
+    flat query row g is at in-request position g - local_req_pos_base, i.e.
+    qs_b minus the request's prefix) and local_token_pos (flat query row of
+    every local slot, -1 for pad); num_tokens = T and num_kv_rows = the KV rows
+    of the batch (the sum of seq_lens).
     """
     qsl = [int(x) for x in query_start_loc]
     sl = [int(x) for x in seq_lens]
     B = len(sl)
     if len(qsl) != B + 1 or qsl[0] != 0:
         raise ValueError("query_start_loc must have B+1 entries starting at 0")
+    prefix, kv_start = [], [0]
     for b in range(B):
-        if qsl[b + 1] - qsl[b] != sl[b]:
-            raise ValueError("seq_lens != query lengths (prefix KV) is not supported (R9)")
+        q_len = qsl[b + 1] - qsl[b]
+        if q_len < 0 or sl[b] < q_len:
+            raise ValueError("seq_lens[b] must be at least the query length of request b (R9)")
+        prefix.append(sl[b] - q_len)
+        kv_start.append(kv_start[-1] + sl[b])
     T = qsl[B]
     pad, tpr = padded_geometry(T, cp_size)
     rows = local_rows(T, cp_size, cp_rank, mode)
@@ -165,15 +179,16 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
         local_start = min(cp_rank, T)
         local_end = T
 
-    q_lens, kv_lens, req_id, kv_base = [], [], [], []
+    q_lens, kv_lens, req_id, kv_base, pos_base = [], [], [], [], []
     for b in range(B):
         mine = [int(g) for g in rows if g >= 0 and qsl[b] <= g < qsl[b + 1]]
         if not mine:
             continue  # R5
         q_lens.append(len(mine))
-        kv_lens.append(max(mine) - qsl[b] + 1)  # R4: last local position + 1
+        kv_lens.append(prefix[b] + max(mine) - qsl[b] + 1)  # R4: last local position + 1
         req_id.append(b)
-        kv_base.append(qsl[b])
+        kv_base.append(kv_start[b])         # R9: KV row of position 0
+        pos_base.append(qsl[b] - prefix[b])  # position of flat row g = g - pos_base
 
     lqs = [0]
     for n in q_lens:
@@ -197,6 +212,9 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
         "local_req_id": req_id,
         "local_req_kv_base": kv_base,
         "local_token_pos": [int(g) for g in rows],
+        "local_req_pos_base": pos_base,
+        "num_tokens": T,
+        "num_kv_rows": kv_start[-1],
     }
 
 
@@ -340,8 +358,10 @@ def view_row(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int,
 
     Returns (selected global KV rows ascending [<=topk] int64, scores fp64
     [p+1], output fp64 [H, Dv]); (None, None, zeros) for a pad slot.
-    The local query of flat row g, request b at position p = g - qs_b, sees
-    keys qs_b .. qs_b + p (causal, same request; R8).
+    The local query of flat row g in request b, at in-request position
+    p = g - local_req_pos_base (= g - qs_b without a prefix), sees the keys at
+    positions 0 .. p of its own request, KV rows kv_base .. kv_base + p
+    (causal, same request; R8, R9).
     """
     g = md["local_token_pos"][slot]
     H = np.asarray(q_loc[slot]).shape[0]
@@ -349,7 +369,7 @@ def view_row(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int,
         return None, None, np.zeros((H, Dv))
     j = request_of_slot(md, slot)
     base = md["local_req_kv_base"][j]
-    p = g - base
+    p = g - md["local_req_pos_base"][j]
     keys = np.arange(base, base + p + 1)
     scores = indexer_scores(q_idx_loc[slot], w_loc[slot], np.asarray(k_idx)[keys])
     sel = base + topk_positions(scores, topk)
@@ -378,7 +398,10 @@ def prefill(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mod
             scale: float, Dv: int, sink=None):
     """The whole prefill through cp_size views: split the local tensors, run
     every view with full KV and index keys, rerange the outputs to flat order
-    ([xLLM] 单层前向数据流: q local, KV full).  Returns out [T, H, Dv] fp64."""
+    ([xLLM] 单层前向数据流: q local, KV full).  q, q_idx, w hold the T query
+    tokens; kv and k_idx the KV rows of every request's whole sequence (R9;
+    the same T rows when seq_lens equal the query lengths).  Returns
+    out [T, H, Dv] fp64."""
     q = np.asarray(q, dtype=np.float64)
     q_idx = np.asarray(q_idx, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)

@@ -15,7 +15,7 @@ import torch
 
 from conftest import read_golden, read_golden_lines
 from oracle import dsa_oracle as O
-from workloads import HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, draw_inputs
+from workloads import HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, chunk_inputs, draw_inputs
 
 MODES = (IN_SEQ_SPLIT, ROUND_ROBIN, HEAD_TAIL)
 
@@ -194,7 +194,7 @@ def test_metadata_partitions_all_query_tokens(lengths, cp, mode):
         # every local query's position is inside its request's visible extent
         for j in range(md["local_batch"]):
             for slot in range(md["local_query_start_loc"][j], md["local_query_start_loc"][j + 1]):
-                p = md["local_token_pos"][slot] - md["local_req_kv_base"][j]
+                p = md["local_token_pos"][slot] - md["local_req_pos_base"][j]
                 assert 0 <= p < md["local_seq_lens"][j]
     assert total == T and np.all(owner == 1)
 
@@ -222,9 +222,77 @@ def test_metadata_in_seq_right_aligned_extent():
             assert md["local_start"] == 8192 // cp * r and md["local_end"] == 8192 // cp * (r + 1)
 
 
-def test_metadata_rejects_prefix():
+def test_metadata_rejects_seq_lens_shorter_than_queries():
     with pytest.raises(ValueError):
-        O.build_local_metadata([0, 4], [6], 2, 0, IN_SEQ_SPLIT)
+        O.build_local_metadata([0, 4], [3], 2, 0, IN_SEQ_SPLIT)
+
+
+_PREFIX_CASES = {"P": ([3, 2], [5, 2], 2), "Q": ([4], [10], 3)}  # q_lens, seq_lens, cp
+
+
+def test_metadata_prefix_hand_cases():
+    seen = set()
+    for line in read_golden_lines("metadata_prefix_hand_cases.txt"):
+        head, lqs, kvl, lkv, rid, base, pbase, pos = line.split("|")
+        case, mode_s, rank = head.split()
+        q_lens, seq_lens, cp = _PREFIX_CASES[case]
+        mode = {"inseq": IN_SEQ_SPLIT, "rr": ROUND_ROBIN, "ht": HEAD_TAIL}[mode_s]
+        md = O.build_local_metadata(_qsl(q_lens), seq_lens, cp, int(rank), mode)
+        assert md["local_query_start_loc"] == _ints(lqs), line
+        assert md["local_seq_lens"] == _ints(kvl), line
+        assert md["local_kv_start_loc"] == _ints(lkv), line
+        assert md["local_req_id"] == _ints(rid), line
+        assert md["local_req_kv_base"] == _ints(base), line
+        assert md["local_req_pos_base"] == _ints(pbase), line
+        assert md["local_token_pos"] == _ints(pos), line
+        assert md["num_tokens"] == sum(q_lens) and md["num_kv_rows"] == sum(seq_lens)
+        seen.add((case, mode_s, int(rank)))
+    assert len(seen) == 12
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("q_lens,prefixes,cp", [([37, 20, 9], [25, 0, 4], 3), ([5, 1, 12], [0, 30, 3], 4),
+                                                ([64], [192], 8)])
+def test_metadata_prefix_extents(q_lens, prefixes, cp, mode):
+    # with a prefix the extents stay right-aligned: every local query sits inside
+    # its request's visible extent, the extents of a request over all ranks end at
+    # its seq_len, and the KV base of request b is the sum of the seq_lens before it
+    seq_lens = [n + p for n, p in zip(q_lens, prefixes)]
+    qsl = _qsl(q_lens)
+    widest = [0] * len(q_lens)
+    for r in range(cp):
+        md = O.build_local_metadata(qsl, seq_lens, cp, r, mode)
+        for j in range(md["local_batch"]):
+            b = md["local_req_id"][j]
+            assert md["local_req_kv_base"][j] == sum(seq_lens[:b])
+            assert md["local_req_pos_base"][j] == qsl[b] - prefixes[b]
+            widest[b] = max(widest[b], md["local_seq_lens"][j])
+            for slot in range(md["local_query_start_loc"][j], md["local_query_start_loc"][j + 1]):
+                p = md["local_token_pos"][slot] - md["local_req_pos_base"][j]
+                assert prefixes[b] <= p < md["local_seq_lens"][j] <= seq_lens[b]
+    assert widest == seq_lens
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("cp", [1, 2, 3])
+def test_chunked_prefill_rows_equal_whole_prefill(cp, mode):
+    # a request processed as prefix (KV only) + chunk (queries) gives exactly the
+    # chunk's rows of the whole-sequence prefill: the same keys, scores, top-k and
+    # attention per row, only the geometry differs
+    lengths, prefixes = [37, 20, 9], [25, 0, 4]
+    wl = TINY.with_(name="tiny-chunk", lengths=tuple(lengths), topk=8, sink=True)
+    x = draw_inputs(wl)
+    xf = {k: (_f64(v) if v is not None else None) for k, v in x.items()}
+    whole = O.prefill(xf["q"], xf["kv"], xf["q_idx"], xf["k_idx"], xf["w"], _qsl(lengths), lengths, cp, mode,
+                      wl.topk, wl.scale, wl.Dv, xf["sink"])
+    xc, q_lens, seq_lens = chunk_inputs(x, lengths, prefixes)
+    xcf = {k: (_f64(v) if v is not None else None) for k, v in xc.items()}
+    chunk = O.prefill(xcf["q"], xcf["kv"], xcf["q_idx"], xcf["k_idx"], xcf["w"], _qsl(q_lens), seq_lens, cp, mode,
+                      wl.topk, wl.scale, wl.Dv, xcf["sink"])
+    rows = [g for b, (n, p) in enumerate(zip(lengths, prefixes)) for g in range(sum(lengths[:b]) + p,
+                                                                                 sum(lengths[:b]) + n)]
+    assert chunk.shape[0] == sum(q_lens)
+    np.testing.assert_allclose(chunk, whole[rows], rtol=1e-13, atol=1e-13)
 
 
 # ---------------------------------------------------------------- indexer

@@ -159,3 +159,24 @@ def sample_rows(n_rows_total: int, count: int, seed: int, must=()) -> np.ndarray
             break
         seen.add(int(x))
     return np.array(sorted(seen), dtype=np.int64)
+
+
+def chunk_inputs(x: dict, lengths, prefixes) -> tuple:
+    """Inputs of a chunked prefill cut from a whole-sequence batch ``x`` (drawn
+    for ``lengths``): request b keeps its first ``prefixes[b]`` positions as
+    KV only, and its remaining positions are the queries.  q, q_idx and w keep
+    the query rows; kv, k_idx and sink stay whole (every request's sequence, in
+    order).  Returns (inputs, query lengths, seq_lens)."""
+    lengths = [int(n) for n in lengths]
+    prefixes = [int(p) for p in prefixes]
+    if len(prefixes) != len(lengths) or any(p < 0 or p > n for p, n in zip(prefixes, lengths)):
+        raise ValueError("0 <= prefix <= length for every request")
+    rows, start = [], 0
+    for n, p in zip(lengths, prefixes):
+        rows.extend(range(start + p, start + n))
+        start += n
+    idx = torch.tensor(rows, dtype=torch.long, device=x["q"].device)
+    out = dict(x)
+    for k in ("q", "q_idx", "w"):
+        out[k] = x[k].index_select(0, idx).contiguous()
+    return out, [n - p for n, p in zip(lengths, prefixes)], lengths
