@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define DSA_CP_ABI_VERSION 1
+#define DSA_CP_ABI_VERSION 2
 
 typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 
@@ -53,7 +53,7 @@ typedef enum {
   DSA_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed          */
   DSA_ERR_DEVICE_TIMEOUT = 6, /* a device wait ran past its limit           */
   DSA_ERR_DEVICE_BOUNDS = 7,  /* a device-side index was out of range       */
-  DSA_ERR_DEVICE_PREFIX = 8   /* metadata: seq_lens != query lengths        */
+  DSA_ERR_DEVICE_SEQ_LENS = 8 /* metadata: a seq_lens below its query length */
 } dsa_status;
 
 typedef enum { DSA_CP_IN_SEQ_SPLIT = 0, DSA_CP_ROUND_ROBIN = 1, DSA_CP_HEAD_TAIL = 2 } dsa_cp_mode;
@@ -68,7 +68,9 @@ enum {
   DSA_MD_LOCAL_NUM_TOKENS = 5,
   DSA_MD_LOCAL_MAX_SEQLEN_Q = 6,
   DSA_MD_LOCAL_MAX_SEQLEN_KV = 7,
-  DSA_MD_NUM_SCALARS = 8
+  DSA_MD_NUM_TOKENS = 8,   /* query tokens T of the batch        */
+  DSA_MD_NUM_KV_ROWS = 9,  /* KV rows of the batch = sum seq_lens */
+  DSA_MD_NUM_SCALARS = 10
 };
 
 /*
@@ -77,7 +79,7 @@ enum {
  * arrays owned by the caller; dsa_cp_metadata_bind carves them out of one
  * buffer of dsa_cp_metadata_sizes() ints.  B = global batch size,
  * tpr = tokens_per_rank.
- *   scalars[8]                  see DSA_MD_*; in round-robin mode the local
+ *   scalars[10]                 see DSA_MD_*; in round-robin mode the local
  *                               rows are {local_start + i*cp_size < local_end}
  *   local_query_start_loc[B+1]  cu-seqlens of the local queries (first
  *                               local_batch+1 entries valid)
@@ -86,9 +88,15 @@ enum {
  *                               (right-aligned, [xLLM] 单层前向数据流 (4))
  *   local_kv_start_loc[B+1]     exclusive cumsum of local_seq_lens
  *   local_req_id[B]             global request index of each local request
- *   local_req_kv_base[B]        flat row of that request's first token (KV
- *                               and index keys stay in full flat order)
- *   local_token_pos[tpr]        flat token row of every local slot, -1 = pad
+ *   local_req_kv_base[B]        KV row of that request's position 0 (KV and
+ *                               index keys hold every request's whole
+ *                               sequence, requests in order: the sum of the
+ *                               seq_lens before it; = its first query row
+ *                               when there is no prefix)
+ *   local_token_pos[tpr]        flat query row of every local slot, -1 = pad
+ *   local_req_pos_base[B]       a local slot of flat query row g in that
+ *                               request is at position g - local_req_pos_base
+ *                               (= first query row - prefix length)
  * Requests with no local row are not in the local batch.
  */
 typedef struct {
@@ -99,6 +107,7 @@ typedef struct {
   int32_t *local_req_id;
   int32_t *local_req_kv_base;
   int32_t *local_token_pos;
+  int32_t *local_req_pos_base;
 } dsa_cp_local_metadata;
 
 /* Host only.  num_tokens_pad = ceil(num_tokens / cp_size) * cp_size and
@@ -109,7 +118,7 @@ dsa_status dsa_cp_geometry(int32_t num_tokens, int32_t cp_size, int32_t *num_tok
                            int32_t *tokens_per_rank);
 
 /* Host only.  Number of int32 elements one view's metadata needs:
- * 8 + 2*(batch+1) + 3*batch + tokens_per_rank.  `ints_needed` is a host
+ * 10 + 2*(batch+1) + 4*batch + tokens_per_rank.  `ints_needed` is a host
  * pointer. */
 dsa_status dsa_cp_metadata_sizes(int32_t batch, int32_t num_tokens, int32_t cp_size,
                                  size_t *ints_needed);
@@ -123,9 +132,18 @@ dsa_status dsa_cp_metadata_bind(int32_t *buffer, int32_t batch, int32_t num_toke
  * build_cp_local_metadata ([xLLM] "代码实现 / 2", [blog] "2.B"): the local
  * view of rank cp_rank.  query_start_loc [batch+1] and seq_lens [batch] are
  * device arrays with query_start_loc[0] = 0, query_start_loc[batch] =
- * num_tokens and seq_lens[b] = query length of request b (a prefix, i.e.
- * chunked prefill, is reported as DSA_ERR_DEVICE_PREFIX through
- * dsa_poll_device_error).  `out` is a host struct of device pointers.
+ * num_tokens and seq_lens[b] = the KV length of request b, at least its
+ * query length q_len_b.  Chunked prefill ([xLLM] 测试与验证; the separate KV
+ * geometry of 单层前向数据流 (4)): the queries of request b are the last
+ * q_len_b positions of its seq_lens[b]-token sequence, after a prefix of
+ * seq_lens[b] - q_len_b positions whose KV is already present; KV and index
+ * keys hold every request's whole sequence, requests in order.  With
+ * seq_lens = query lengths there is no prefix.  A seq_lens below its query
+ * length, or sum(seq_lens) beyond int32, is reported as
+ * DSA_ERR_DEVICE_SEQ_LENS through dsa_poll_device_error, and inconsistent
+ * query_start_loc as DSA_ERR_DEVICE_BOUNDS.  `out` is a host struct of
+ * device pointers.  The local KV extent of a request (local_seq_lens) is its
+ * prefix plus the positions up to its last local query (right-aligned).
  * Split of the flat token stream (padded at the end to a multiple of
  * cp_size):
  *   DSA_CP_IN_SEQ_SPLIT: rank r holds rows [r*tpr, (r+1)*tpr)
@@ -190,10 +208,11 @@ dsa_status dsa_indexer_topk_workspace_size(int32_t tokens_per_rank, int32_t max_
 /*
  * Lightning indexer + causal top-k for one CP view ([xLLM] 单层前向数据流
  * (3) and "4. Indexer full/local 分离": local queries and weights, full
- * index keys).  For every local slot i with flat row g in request b,
- * position p = g - qs_b:
- *   I[i, s] = sum_j w[i, j] * ReLU(q_idx[i, j, :] . k_idx[qs_b + s, :]),  s = 0..p
- * and topk_idx[i, :] = the flat KV rows qs_b + s of the topk largest
+ * index keys).  For every local slot i with flat query row g in request b,
+ * in-request position p = g - local_req_pos_base[b] and KV base
+ * kb = local_req_kv_base[b] (p = g - qs_b and kb = qs_b without a prefix):
+ *   I[i, s] = sum_j w[i, j] * ReLU(q_idx[i, j, :] . k_idx[kb + s, :]),  s = 0..p
+ * and topk_idx[i, :] = the KV rows kb + s of the topk largest
  * I[i, s], ties to the lower s, in ascending order; rows with p + 1 <= topk
  * select every s; unused entries and pad slots are -1.
  *   md           host struct of device pointers (dsa_cp_build_local_metadata)
@@ -203,7 +222,7 @@ dsa_status dsa_indexer_topk_workspace_size(int32_t tokens_per_rank, int32_t max_
  *                longest request); a larger extent on the device is a
  *                DSA_ERR_DEVICE_BOUNDS
  *   q_idx        bf16 [tpr][HI][DI]   (local, split)
- *   k_idx        bf16 [num_tokens][DI] (full)
+ *   k_idx        bf16 [num_kv_rows][DI] (full: every request's whole sequence)
  *   w            fp32 [tpr][HI]        (local, split)
  *   topk_idx     int32 [tpr][topk]     output
  *   workspace    device scratch of ws_bytes bytes (16-byte aligned)
@@ -211,7 +230,7 @@ dsa_status dsa_indexer_topk_workspace_size(int32_t tokens_per_rank, int32_t max_
  */
 dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
                             int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
-                            int32_t num_tokens, int32_t HI, int32_t DI, int32_t topk, int32_t *topk_idx,
+                            int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t topk, int32_t *topk_idx,
                             void *workspace, size_t ws_bytes, dsa_stream_t stream);
 
 /*
@@ -240,7 +259,7 @@ dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int3
  */
 dsa_status dsa_indexer_topk_noalloc(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
                                     int32_t max_kv_len, const void *q_idx, const void *k_idx,
-                                    const float *w, int32_t num_tokens, int32_t HI, int32_t DI,
+                                    const float *w, int32_t num_kv_rows, int32_t HI, int32_t DI,
                                     int32_t topk, int32_t *topk_idx, dsa_stream_t stream);
 
 /*
@@ -251,7 +270,7 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_cp_local_metadata *md, int32_t bat
  */
 dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
                               int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
-                              int32_t num_tokens, int32_t HI, int32_t DI, int32_t row_begin,
+                              int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t row_begin,
                               int32_t row_count, float *scores, dsa_stream_t stream);
 
 /*
@@ -264,9 +283,11 @@ dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, in
  * with m any common shift and the sink term present only when attn_sink
  * is non-NULL (a logit in scaled units that adds to the denominator only).
  *   q          bf16 [tpr][H][D] (local, split)
- *   kv         bf16 [num_tokens][D] (full); value = the first Dv columns
- *   topk_idx   int32 [tpr][topk] flat KV rows, -1 = unused (as produced by
- *              dsa_indexer_topk: the valid entries first)
+ *   kv         bf16 [num_kv_rows][D] (full: every request's whole sequence);
+ *              value = the first Dv columns
+ *   topk_idx   int32 [tpr][topk] KV rows, -1 = unused (as produced by
+ *              dsa_indexer_topk: the valid entries first); a row outside
+ *              [0, num_kv_rows) is a DSA_ERR_DEVICE_BOUNDS and is not read
  *   attn_sink  fp32 [H] or NULL
  *   out        bf16 [tpr][H][Dv]; pad slots are written as zeros
  * QK and PV run on the tensor cores (bf16 operands, fp32 accumulate); the
@@ -274,7 +295,7 @@ dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, in
  * view, so reranged views reproduce the single-view result.
  */
 dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
-                                   const void *q, const void *kv, int32_t num_tokens,
+                                   const void *q, const void *kv, int32_t num_kv_rows,
                                    const int32_t *topk_idx, int32_t topk, const float *attn_sink,
                                    float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
                                    dsa_stream_t stream);
@@ -284,21 +305,22 @@ dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batc
  * output stores ([xLLM] 单层前向数据流 (4) then (6)): same inputs and
  * arithmetic (the results are bit-identical to dsa_sparse_attn_prefill
  * followed by dsa_cp_all_to_all_heads), but each head row is written
- * straight to its place in out bf16 [cp_size][num_tokens][H / cp_size][Dv]:
- * rank h / (H / cp_size), token local_token_pos[i], head h % (H / cp_size).
+ * straight to its place in out bf16 [cp_size][T][H / cp_size][Dv], with
+ * T = the batch's query tokens (scalars[DSA_MD_NUM_TOKENS]): rank
+ * h / (H / cp_size), token local_token_pos[i], head h % (H / cp_size).
  * Pad slots write nothing.  Every view of a batch writes into the same out;
  * their rows do not overlap.  cp_size >= 1 (else DSA_ERR_INVALID_ARG) and H
  * must divide by cp_size (else DSA_ERR_SHAPE).
  */
 dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
-                                               const void *q, const void *kv, int32_t num_tokens,
+                                               const void *q, const void *kv, int32_t num_kv_rows,
                                                const int32_t *topk_idx, int32_t topk, const float *attn_sink,
                                                float softmax_scale, int32_t H, int32_t D, int32_t Dv,
                                                int32_t cp_size, void *out, dsa_stream_t stream);
 
 /* Synchronise `stream`, then return (and clear) the first error a kernel
  * recorded on the current device since the last poll: DSA_OK, or
- * DSA_ERR_DEVICE_TIMEOUT / _BOUNDS / _PREFIX; DSA_ERR_CUDA if the sync
+ * DSA_ERR_DEVICE_TIMEOUT / _BOUNDS / _SEQ_LENS; DSA_ERR_CUDA if the sync
  * itself failed (the message is in dsa_last_cuda_error()). */
 dsa_status dsa_poll_device_error(dsa_stream_t stream);
 

@@ -64,9 +64,9 @@ class CPLocalMetadata:
     of pointers into it (dsa_cp_local_metadata)."""
 
     FIELDS = ("local_query_start_loc", "local_seq_lens", "local_kv_start_loc", "local_req_id",
-              "local_req_kv_base", "local_token_pos")
+              "local_req_kv_base", "local_token_pos", "local_req_pos_base")
     SCALARS = ("num_tokens_pad", "tokens_per_rank", "local_start", "local_end", "local_batch",
-               "local_num_tokens", "local_max_seqlen_q", "local_max_seqlen_kv")
+               "local_num_tokens", "local_max_seqlen_q", "local_max_seqlen_kv", "num_tokens", "num_kv_rows")
 
     def __init__(self, batch: int, num_tokens: int, cp_size: int, device=None):
         self.batch, self.num_tokens, self.cp_size = int(batch), int(num_tokens), int(cp_size)
@@ -81,12 +81,15 @@ class CPLocalMetadata:
         """Read the view back (synchronises); lists trimmed to their valid length."""
         b = self.buffer.cpu().tolist()
         B, tpr = self.batch, self.tokens_per_rank
-        out = dict(zip(self.SCALARS, b[:8]))
-        o = 8
+        ns = len(self.SCALARS)
+        out = dict(zip(self.SCALARS, b[:ns]))
+        o = ns
         nb = out["local_batch"]
+        # the order of dsa_cp_metadata_bind's carve-up
         for name, size, valid in (("local_query_start_loc", B + 1, nb + 1), ("local_seq_lens", B, nb),
                                   ("local_kv_start_loc", B + 1, nb + 1), ("local_req_id", B, nb),
-                                  ("local_req_kv_base", B, nb), ("local_token_pos", tpr, tpr)):
+                                  ("local_req_kv_base", B, nb), ("local_req_pos_base", B, nb),
+                                  ("local_token_pos", tpr, tpr)):
             out[name] = b[o:o + valid]
             o += size
         return out
@@ -282,7 +285,7 @@ def dsa_sparse_attn_prefill_headsharded(md: CPLocalMetadata, q: torch.Tensor, kv
     tpr, H, D = q.shape
     if tpr != md.tokens_per_rank or kv.shape[1] != D or topk_idx.shape[0] != tpr:
         raise ValueError("q / kv / topk_idx shapes do not match the view")
-    if cp_size < 1 or H % cp_size or tuple(out.shape) != (cp_size, kv.shape[0], H // cp_size, Dv):
+    if cp_size < 1 or H % cp_size or tuple(out.shape) != (cp_size, md.num_tokens, H // cp_size, Dv):
         raise ValueError("out must be [cp_size, T, H / cp_size, Dv] with H divisible by cp_size")
     check(load().dsa_sparse_attn_prefill_headsharded(C.byref(md.struct), md.batch, tpr, _ptr(q), _ptr(kv),
                                                      kv.shape[0], _ptr(topk_idx), topk_idx.shape[1],

@@ -21,6 +21,7 @@ class LocalMetadata(C.Structure):
         ("local_req_id", C.c_void_p),
         ("local_req_kv_base", C.c_void_p),
         ("local_token_pos", C.c_void_p),
+        ("local_req_pos_base", C.c_void_p),
     ]
 
 
@@ -63,7 +64,7 @@ SIGNATURES = {
 STATUS = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_SHAPE", 3: "DSA_ERR_UNSUPPORTED",
     4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT", 7: "DSA_ERR_DEVICE_BOUNDS",
-    8: "DSA_ERR_DEVICE_PREFIX",
+    8: "DSA_ERR_DEVICE_SEQ_LENS",
 }
 
 _LIB = None

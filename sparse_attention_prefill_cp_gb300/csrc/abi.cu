@@ -100,7 +100,8 @@ const char *dsa_status_string(dsa_status s) {
     case DSA_ERR_CUDA: return "DSA_ERR_CUDA: a CUDA call failed (see dsa_last_cuda_error)";
     case DSA_ERR_DEVICE_TIMEOUT: return "DSA_ERR_DEVICE_TIMEOUT: a device-side wait ran past its limit";
     case DSA_ERR_DEVICE_BOUNDS: return "DSA_ERR_DEVICE_BOUNDS: a device-side index was out of range";
-    case DSA_ERR_DEVICE_PREFIX: return "DSA_ERR_DEVICE_PREFIX: seq_lens differ from query lengths (prefix KV)";
+    case DSA_ERR_DEVICE_SEQ_LENS:
+      return "DSA_ERR_DEVICE_SEQ_LENS: a seq_lens entry is below its query length (or the KV rows overflow int32)";
   }
   return "unknown dsa_status";
 }
@@ -123,7 +124,7 @@ dsa_status dsa_cp_metadata_sizes(int32_t batch, int32_t num_tokens, int32_t cp_s
   dsa_status st = dsa_cp_geometry(num_tokens, cp_size, &pad, &tpr);
   if (st != DSA_OK) return st;
   *ints_needed = static_cast<size_t>(DSA_MD_NUM_SCALARS) + 2 * (static_cast<size_t>(batch) + 1) +
-                 3 * static_cast<size_t>(batch) + static_cast<size_t>(tpr);
+                 4 * static_cast<size_t>(batch) + static_cast<size_t>(tpr);
   return DSA_OK;
 }
 
@@ -141,6 +142,7 @@ dsa_status dsa_cp_metadata_bind(int32_t *buffer, int32_t batch, int32_t num_toke
   out->local_kv_start_loc = p;     p += B + 1;
   out->local_req_id = p;           p += B;
   out->local_req_kv_base = p;      p += B;
+  out->local_req_pos_base = p;     p += B;
   out->local_token_pos = p;
   return DSA_OK;
 }

@@ -70,7 +70,7 @@ struct IdxParams {
   const float *w;      // [tpr][HI]
   float *scores;       // [rows][ld]
   int64_t ld;          // score row stride (floats)
-  int32_t tpr, row_begin, row_end, max_kv_len, num_tokens;
+  int32_t tpr, row_begin, row_end, max_kv_len, num_kv_rows;
   int *err;
 };
 
@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     misc[3] = 0;  // any valid slot
   }
   __syncthreads();
-  // per-slot causal extent: flat key rows [base, base + p]
+  // per-slot causal extent: key rows [base, base + p] (base = KV row of the
+  // request's position 0, p = the query's in-request position)
   for (int t = tid; t < C::kTileTok; t += C::kThreads) {
     const int slot = slot0 + t;
     int base = 0, p = -1;
@@ -111,8 +112,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (g >= 0 && local_batch > 0) {
         const int j = find_local_request(P.md.local_query_start_loc, local_batch, slot);
         base = P.md.local_req_kv_base[j];
-        p = g - base;
-        if (p < 0 || p >= P.max_kv_len || g >= P.num_tokens) {
+        p = g - P.md.local_req_pos_base[j];
+        if (p < 0 || p >= P.max_kv_len || base < 0 || base + p >= P.num_kv_rows) {
           record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 41, slot);
           p = -1;
         }
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     if (g >= 0 && nb > 0) {
       const int j = find_local_request(md.local_query_start_loc, nb, slot);
       base = md.local_req_kv_base[j];
-      p = g - base;
+      p = g - md.local_req_pos_base[j];
       if (p < 0 || p >= max_kv_len) {
         record_error(err, DSA_ERR_DEVICE_BOUNDS, 42, slot);
         p = -1;
@@ -421,7 +422,7 @@ __global__ void fill_kernel(float *p, int64_t n, float v) {
 
 // ------------------------------------------------------------------ host side
 template <class C>
-dsa_status make_maps(const void *q_idx, const void *k_idx, int32_t tpr, int32_t num_tokens, CUtensorMap *qmap,
+dsa_status make_maps(const void *q_idx, const void *k_idx, int32_t tpr, int32_t num_kv_rows, CUtensorMap *qmap,
                      CUtensorMap *kmap) {
   const CUtensorMapSwizzle sw = C::kCWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   uint64_t qdims[2] = {static_cast<uint64_t>(C::DI), static_cast<uint64_t>(tpr) * C::HI};
@@ -429,7 +430,7 @@ dsa_status make_maps(const void *q_idx, const void *k_idx, int32_t tpr, int32_t 
   uint32_t qbox[2] = {static_cast<uint32_t>(C::kCW), 256};
   dsa_status st = encode_tensor_map(qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_idx, qdims, qstr, qbox, sw);
   if (st != DSA_OK) return st;
-  uint64_t kdims[2] = {static_cast<uint64_t>(C::DI), static_cast<uint64_t>(num_tokens)};
+  uint64_t kdims[2] = {static_cast<uint64_t>(C::DI), static_cast<uint64_t>(num_kv_rows)};
   uint32_t kbox[2] = {static_cast<uint32_t>(C::kCW), 128};
   return encode_tensor_map(kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k_idx, kdims, qstr, kbox, sw);
 }
@@ -448,17 +449,18 @@ dsa_status launch_indexer(const CUtensorMap &qmap, const CUtensorMap &kmap, cons
 
 struct Args {
   const dsa_cp_local_metadata *md;
-  int32_t batch, tpr, max_kv_len, num_tokens, HI, DI;
+  int32_t batch, tpr, max_kv_len, num_kv_rows, HI, DI;
   const void *q_idx, *k_idx;
   const float *w;
 };
 
 dsa_status validate(const Args &a) {
   if (!a.md || !a.q_idx || !a.k_idx || !a.w) return DSA_ERR_INVALID_ARG;
-  if (!a.md->scalars || !a.md->local_query_start_loc || !a.md->local_req_kv_base || !a.md->local_token_pos)
+  if (!a.md->scalars || !a.md->local_query_start_loc || !a.md->local_req_kv_base || !a.md->local_token_pos ||
+      !a.md->local_req_pos_base)
     return DSA_ERR_INVALID_ARG;
   if (!aligned16(a.q_idx) || !aligned16(a.k_idx)) return DSA_ERR_INVALID_ARG;
-  if (a.batch < 0 || a.tpr < 0 || a.max_kv_len < 1 || a.num_tokens < 1) return DSA_ERR_SHAPE;
+  if (a.batch < 0 || a.tpr < 0 || a.max_kv_len < 1 || a.num_kv_rows < 1) return DSA_ERR_SHAPE;
   if (static_cast<int64_t>(a.tpr) * a.HI > INT32_MAX) return DSA_ERR_SHAPE;
   return DSA_OK;
 }
@@ -470,11 +472,11 @@ template <class C>
 dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *out, int64_t ld,
                       cudaStream_t stream) {
   CUtensorMap qmap, kmap;
-  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_tokens, &qmap, &kmap);
+  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_kv_rows, &qmap, &kmap);
   if (st != DSA_OK) return st;
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
-  IdxParams P{*a.md, a.w, out, ld, a.tpr, row_begin, row_end, a.max_kv_len, a.num_tokens, err};
+  IdxParams P{*a.md, a.w, out, ld, a.tpr, row_begin, row_end, a.max_kv_len, a.num_kv_rows, err};
   return launch_indexer<C>(qmap, kmap, P, stream);
 }
 
@@ -485,14 +487,14 @@ dsa_status run_topk(const Args &a, int32_t *topk_idx, void *ws, size_t ws_bytes,
   rows_fit = rows_fit / C::kTileTok * C::kTileTok;
   if (rows_fit < C::kTileTok) return DSA_ERR_WORKSPACE;
   CUtensorMap qmap, kmap;
-  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_tokens, &qmap, &kmap);
+  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_kv_rows, &qmap, &kmap);
   if (st != DSA_OK) return st;
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
   float *scores = static_cast<float *>(ws);
   for (int64_t r0 = 0; r0 < a.tpr; r0 += rows_fit) {
     const int32_t r1 = static_cast<int32_t>(r0 + rows_fit < a.tpr ? r0 + rows_fit : a.tpr);
-    IdxParams P{*a.md, a.w, scores, ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_tokens, err};
+    IdxParams P{*a.md, a.w, scores, ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows, err};
     st = launch_indexer<C>(qmap, kmap, P, stream);
     if (st != DSA_OK) return st;
     topk_kernel<TOPK><<<static_cast<unsigned>(r1 - r0), kTopkThreads, 0, stream>>>(
@@ -524,10 +526,10 @@ extern "C" dsa_status dsa_indexer_topk_workspace_size(int32_t tokens_per_rank, i
 
 extern "C" dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
                                        int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
-                                       int32_t num_tokens, int32_t HI, int32_t DI, int32_t topk,
+                                       int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t topk,
                                        int32_t *topk_idx, void *workspace, size_t ws_bytes,
                                        dsa_stream_t stream) {
-  Args a{md, batch, tpr, max_kv_len, num_tokens, HI, DI, q_idx, k_idx, w};
+  Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx, k_idx, w};
   dsa_status st = validate(a);
   if (st != DSA_OK) return st;
   if (!topk_idx || !workspace || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
@@ -540,9 +542,9 @@ extern "C" dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t 
 
 extern "C" dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
                                          int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
-                                         int32_t num_tokens, int32_t HI, int32_t DI, int32_t row_begin,
+                                         int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t row_begin,
                                          int32_t row_count, float *scores, dsa_stream_t stream) {
-  Args a{md, batch, tpr, max_kv_len, num_tokens, HI, DI, q_idx, k_idx, w};
+  Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx, k_idx, w};
   dsa_status st = validate(a);
   if (st != DSA_OK) return st;
   if (!scores) return DSA_ERR_INVALID_ARG;
@@ -602,9 +604,9 @@ dsa_status static_scratch(void **out) {
 
 extern "C" dsa_status dsa_indexer_topk_noalloc(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
                                                int32_t max_kv_len, const void *q_idx, const void *k_idx,
-                                               const float *w, int32_t num_tokens, int32_t HI, int32_t DI,
+                                               const float *w, int32_t num_kv_rows, int32_t HI, int32_t DI,
                                                int32_t topk, int32_t *topk_idx, dsa_stream_t stream) {
-  Args a{md, batch, tpr, max_kv_len, num_tokens, HI, DI, q_idx, k_idx, w};
+  Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx, k_idx, w};
   dsa_status st = validate(a);
   if (st != DSA_OK) return st;
   if (!topk_idx) return DSA_ERR_INVALID_ARG;

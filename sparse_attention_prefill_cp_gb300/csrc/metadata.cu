@@ -6,8 +6,14 @@
 // local position come from closed forms (an interval intersection for
 // in-seq-split, two for the head-tail zigzag, an arithmetic progression for
 // round-robin); a block-wide exclusive scan compacts the requests that have
-// local rows.  In every mode a rank's slots are in ascending flat order, so
-// the local rows of a request are consecutive slots.
+// local rows and accumulates the KV start of every request (the sum of the
+// seq_lens before it).  In every mode a rank's slots are in ascending flat
+// order, so the local rows of a request are consecutive slots.
+//
+// Chunked prefill (section 测试与验证 lists it; section 单层前向数据流 (4)
+// gives the attention its own KV geometry): seq_lens[b] may exceed the query
+// length; the queries are then the last positions of the request's sequence
+// and its KV extent includes the prefix.
 #include "dsa_common.cuh"
 #include "internal.h"
 
@@ -17,41 +23,38 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-struct Triple {
-  int a, b, c;
+// Per request: a = has local rows, b = local rows, c = local KV extent,
+// d = seq_lens (every request, for the KV starts).
+struct Quad {
+  int a, b, c, d;
+  __device__ void add(const Quad &o) {
+    a += o.a;
+    b += o.b;
+    c += o.c;
+    d += o.d;
+  }
 };
 
-// Exclusive scan of (a, b, c) over the block; returns the block totals in `tot`.
-__device__ Triple block_exclusive_scan(Triple v, Triple &tot) {
-  __shared__ Triple warp_tot[kWarps];
+// Exclusive scan of Quad over the block; returns the block totals in `tot`.
+__device__ Quad block_exclusive_scan(Quad v, Quad &tot) {
+  __shared__ Quad warp_tot[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  Triple inc = v;
+  Quad inc = v;
   for (int off = 1; off < 32; off <<= 1) {
-    int a = __shfl_up_sync(0xffffffffu, inc.a, off);
-    int b = __shfl_up_sync(0xffffffffu, inc.b, off);
-    int c = __shfl_up_sync(0xffffffffu, inc.c, off);
-    if (lane >= off) {
-      inc.a += a;
-      inc.b += b;
-      inc.c += c;
-    }
+    const Quad o = {__shfl_up_sync(0xffffffffu, inc.a, off), __shfl_up_sync(0xffffffffu, inc.b, off),
+                    __shfl_up_sync(0xffffffffu, inc.c, off), __shfl_up_sync(0xffffffffu, inc.d, off)};
+    if (lane >= off) inc.add(o);
   }
   if (lane == 31) warp_tot[warp] = inc;
   __syncthreads();
-  Triple before = {0, 0, 0};
-  tot = {0, 0, 0};
+  Quad before = {0, 0, 0, 0};
+  tot = {0, 0, 0, 0};
   for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) {
-      before.a += warp_tot[w].a;
-      before.b += warp_tot[w].b;
-      before.c += warp_tot[w].c;
-    }
-    tot.a += warp_tot[w].a;
-    tot.b += warp_tot[w].b;
-    tot.c += warp_tot[w].c;
+    if (w < warp) before.add(warp_tot[w]);
+    tot.add(warp_tot[w]);
   }
   __syncthreads();
-  return {before.a + inc.a - v.a, before.b + inc.b - v.b, before.c + inc.c - v.c};
+  return {before.a + inc.a - v.a, before.b + inc.b - v.b, before.c + inc.c - v.c, before.d + inc.d - v.d};
 }
 
 __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__restrict__ qsl,
@@ -59,28 +62,35 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
                                                                int T, int cp, int rank, int mode,
                                                                dsa_cp_local_metadata md, int *err) {
   __shared__ int s_bad;
-  __shared__ int s_run[3];  // running local_batch, query total, kv total
+  __shared__ int s_run[4];  // running local_batch, query total, kv extent total, kv rows
   __shared__ int s_maxq, s_maxkv;
+  __shared__ unsigned long long s_kv_rows;
   const int tid = threadIdx.x;
   const int64_t tpr = (static_cast<int64_t>(T) + cp - 1) / cp;
 
   if (tid == 0) {
     s_bad = 0;
-    s_run[0] = s_run[1] = s_run[2] = 0;
+    s_run[0] = s_run[1] = s_run[2] = s_run[3] = 0;
     s_maxq = s_maxkv = 0;
+    s_kv_rows = 0;
   }
   __syncthreads();
-  // Inputs must describe a plain prefill: cu-seqlens from 0 to T, and
-  // seq_lens equal to the query lengths (no prefix KV).
+  // Inputs: cu-seqlens from 0 to T; seq_lens at least the query lengths, in
+  // total within int32 (the KV rows are indexed with int32).
+  unsigned long long kv_rows = 0;
   for (int b = tid; b < B; b += kThreads) {
-    const int qs = __ldg(qsl + b), qe = __ldg(qsl + b + 1);
+    const int qs = __ldg(qsl + b), qe = __ldg(qsl + b + 1), sl = __ldg(seq_lens + b);
     if (qe < qs || qs < 0 || qe > T) atomicOr(&s_bad, 1);
-    else if (__ldg(seq_lens + b) != qe - qs) atomicOr(&s_bad, 2);
+    else if (sl < qe - qs) atomicOr(&s_bad, 2);
+    kv_rows += sl > 0 ? static_cast<unsigned long long>(sl) : 0ull;
   }
+  atomicAdd(&s_kv_rows, kv_rows);
   if (tid == 0 && (__ldg(qsl) != 0 || __ldg(qsl + B) != T)) atomicOr(&s_bad, 1);
   __syncthreads();
+  if (tid == 0 && s_kv_rows > static_cast<unsigned long long>(INT32_MAX)) s_bad |= 2;
+  __syncthreads();
   const int bad = s_bad;
-  if (bad && tid == 0) record_error(err, (bad & 1) ? DSA_ERR_DEVICE_BOUNDS : DSA_ERR_DEVICE_PREFIX, 46, bad);
+  if (bad && tid == 0) record_error(err, (bad & 1) ? DSA_ERR_DEVICE_BOUNDS : DSA_ERR_DEVICE_SEQ_LENS, 46, bad);
 
   // local slot -> flat token row
   const int64_t lo_inseq = static_cast<int64_t>(rank) * tpr;
@@ -101,11 +111,13 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
   if (!bad) {
     for (int base = 0; base < B; base += kThreads) {
       const int b = base + tid;
-      Triple v = {0, 0, 0};
-      int qs = 0;
+      Quad v = {0, 0, 0, 0};
+      int qs = 0, prefix = 0;
       if (b < B) {
         qs = __ldg(qsl + b);
         const int qe = __ldg(qsl + b + 1);
+        v.d = __ldg(seq_lens + b);
+        prefix = v.d - (qe - qs);
         int64_t q_len = 0, last = -1;
         if (mode == DSA_CP_IN_SEQ_SPLIT) {
           const int64_t lo = qs > lo_inseq ? qs : lo_inseq;
@@ -133,17 +145,19 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
             last = g0 + (q_len - 1) * cp;
           }
         }
-        if (q_len > 0) v = {1, static_cast<int>(q_len), static_cast<int>(last - qs + 1)};
+        // KV extent: the prefix plus the positions up to the last local query
+        if (q_len > 0) v = {1, static_cast<int>(q_len), static_cast<int>(prefix + last - qs + 1), v.d};
       }
-      Triple tot;
-      Triple ex = block_exclusive_scan(v, tot);
+      Quad tot;
+      Quad ex = block_exclusive_scan(v, tot);
       if (v.a) {
         const int j = s_run[0] + ex.a;
         md.local_query_start_loc[j + 1] = s_run[1] + ex.b + v.b;
         md.local_kv_start_loc[j + 1] = s_run[2] + ex.c + v.c;
         md.local_seq_lens[j] = v.c;
         md.local_req_id[j] = b;
-        md.local_req_kv_base[j] = qs;
+        md.local_req_kv_base[j] = s_run[3] + ex.d;  // KV row of position 0
+        md.local_req_pos_base[j] = qs - prefix;     // position of flat row g = g - pos_base
         atomicMax(&s_maxq, v.b);
         atomicMax(&s_maxkv, v.c);
       }
@@ -152,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
         s_run[0] += tot.a;
         s_run[1] += tot.b;
         s_run[2] += tot.c;
+        s_run[3] += tot.d;
       }
       __syncthreads();
     }
@@ -177,6 +192,8 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
     s[DSA_MD_LOCAL_NUM_TOKENS] = s_run[1];
     s[DSA_MD_LOCAL_MAX_SEQLEN_Q] = s_maxq;
     s[DSA_MD_LOCAL_MAX_SEQLEN_KV] = s_maxkv;
+    s[DSA_MD_NUM_TOKENS] = T;
+    s[DSA_MD_NUM_KV_ROWS] = bad ? 0 : static_cast<int32_t>(s_kv_rows);
   }
 }
 
@@ -194,7 +211,7 @@ extern "C" dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc
   if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN && mode != DSA_CP_HEAD_TAIL)
     return DSA_ERR_INVALID_ARG;
   if (!out->scalars || !out->local_query_start_loc || !out->local_seq_lens || !out->local_kv_start_loc ||
-      !out->local_req_id || !out->local_req_kv_base || !out->local_token_pos)
+      !out->local_req_id || !out->local_req_kv_base || !out->local_token_pos || !out->local_req_pos_base)
     return DSA_ERR_INVALID_ARG;
   if (batch < 0 || num_tokens < 0) return DSA_ERR_SHAPE;
   int32_t pad = 0, tpr = 0;

@@ -26,16 +26,19 @@
 // the exchange agent, 10-15 gather of the selected rows with 16-byte cp.async
 // straight into the 128B / 64B swizzled tiles (two warps per stage, eight
 // threads per 128-byte chunk so that loads coalesce into whole lines).  Key blocks of
-// 64 rows, 4 smem stages.  The partial S tiles are exchanged rounded to bf16:
-// the softmax threads stage their rows locally and warp 9 ships each tile to
-// the peer's double-buffered receive tiles with one bulk copy that completes
-// the peer's mbarrier transaction count, one block ahead of the softmax that
-// needs it.  Each CTA softmaxes its own
-// fp32 partial plus the peer's bf16 one and normalises its own O half.  P (bf16) goes to a shared-memory
-// tile, so an S buffer is free as soon as it has been read and QK runs two
-// blocks ahead of PV.  The running max is rescaled lazily: O and l change
-// only when some row of a warp sees its block max exceed the max in use by
-// more than 2^8.
+// 64 rows, 4 smem stages.  S is scaled to log2 units (softmax_scale *
+// log2 e) as it leaves TMEM, and the partial S tiles are exchanged in fp16
+// (11 significant bits; the scaled logits are far inside its range, and the
+// conversion saturates rather than overflow): the softmax threads stage their
+// rows locally and warp 9 ships each tile to the peer's double-buffered
+// receive tiles with one bulk copy that completes the peer's mbarrier
+// transaction count, one block ahead of the softmax that needs it.  Each CTA
+// softmaxes its own fp32 partial plus the peer's fp16 one and normalises its
+// own O half.  P (bf16) goes to a shared-memory tile, so an S buffer is free
+// as soon as it has been read and QK runs two blocks ahead of PV; the
+// denominator sums the same bf16-rounded P that the PV product uses.  The
+// running max is rescaled lazily: O and l change only when some row of a warp
+// sees its block max exceed the max in use by more than 2^8.
 //
 // The tiny shapes (H = 8, D = 64, Dv = 48) run the same kernel on one CTA
 // with Q rows 8..127 zero-filled by the TMA.
@@ -45,6 +48,10 @@
 // after the attention produces (单层前向数据流 (6)): [cp][T][H / cp][Dv], rank
 // rd holding heads rd * H / cp .. of every real token (pad slots write
 // nothing).
+//
+// A query's selected rows are KV rows of its own request, whose position 0
+// is KV row local_req_kv_base; with chunked prefill the KV holds the prefix
+// too and the query's position is g - local_req_pos_base.
 #include "dsa_common.cuh"
 #include "internal.h"
 
@@ -77,7 +84,7 @@ struct AttnCfg {
   static constexpr int kQCol = kSCol + 2 * kBN;     // Q main dims, bf16 pairs
   static constexpr int kTmemCols = (kQCol + NMAIN * 32) <= 256 ? 256 : 512;
   // shared memory
-  static constexpr int kRecvBytes = SPLIT ? 128 * kBN * 2 : 0;  // one partial-S tile (bf16), rows swizzled
+  static constexpr int kRecvBytes = SPLIT ? 128 * kBN * 2 : 0;  // one partial-S tile (fp16), rows swizzled
   static constexpr int kPBytes = 128 * 128;                     // P tile [128 heads][64 keys] bf16, SW128
   static constexpr int kOffStage = 0;
   static constexpr int kOffQStage = kOffStage + kStageBytes;  // Q main staged in stages 1..2 at start
@@ -113,7 +120,7 @@ struct AttnParams {
   const float *sink;         // [H] or nullptr
   __nv_bfloat16 *out;        // [tpr][H][Dv], or [cp][T][hc][Dv] when hc > 0
   float scale_log2;          // softmax_scale * log2(e)
-  int32_t topk, H, D, Dv, num_tokens;
+  int32_t topk, H, D, Dv, num_kv_rows;
   int32_t hc;                // heads per rank of the head-sharded output, 0 = view layout
   int *err;
 };
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (8 softmax warps)
   uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (8 warps)
   uint64_t *o_staged = fin_full + 1;           // normalised O rows staged in smem (8 warps)
-  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p, [3] g
+  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p, [3] g, [4] T
   float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,8 +178,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (g >= 0 && nbatch > 0) {
       const int j = find_local_request(P.md.local_query_start_loc, nbatch, slot);
       base = P.md.local_req_kv_base[j];
-      p = g - base;
-      if (p < 0 || g >= P.num_tokens) {
+      p = g - P.md.local_req_pos_base[j];
+      if (p < 0 || base < 0 || base + p >= P.num_kv_rows) {
         record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 44, slot);
         p = -1;
       }
@@ -180,6 +187,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     misc[1] = base;
     misc[2] = p;
     misc[3] = g;
+    misc[4] = P.md.scalars[DSA_MD_NUM_TOKENS];
     mbar_init(q_full, 1);
     mbar_init(q_ready, 8);
     for (int s = 0; s < C::kStages; ++s) {
@@ -352,7 +360,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int rr = 0; rr < kRowsPerThread; ++rr) {
         const int r = r0 + 8 * rr;
         int row = rows[rr];
-        if (j * C::kBN + r < n_valid && (row < 0 || row >= P.num_tokens)) {
+        if (j * C::kBN + r < n_valid && (row < 0 || row >= P.num_kv_rows)) {
           record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, j * C::kBN + r);
           row = -1;
         }
@@ -401,12 +409,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     tc_fence_before();
     warp_arrive(q_ready, lane);
 
-    // partial-S tile rows: 64 bf16 (128 bytes), 16-byte unit u stored at u ^ (h & 7)
+    // partial-S tile rows: 64 fp16 (128 bytes), 16-byte unit u stored at u ^ (h & 7)
     uint8_t *recv0 = smem + C::kOffRecv;
-    // stage our 32 columns of a partial S row (fp32 registers), rounded to bf16,
-    // for the exchange agent (SPLIT only).  Each CTA softmaxes its own fp32
-    // partial plus the peer's bf16 partial and normalises its own O half with
-    // its own sum, so the two CTAs need not agree bitwise.
+    // stage our 32 columns of a partial S row (fp32 registers, log2 units),
+    // rounded to fp16, for the exchange agent (SPLIT only).  Each CTA
+    // softmaxes its own fp32 partial plus the peer's fp16 partial and
+    // normalises its own O half with its own sum, so the two CTAs need not
+    // agree bitwise.
     auto stage = [&](int j, const float (&v)[32]) {
       const int b = j & 1;
       uint8_t *row = smem + C::kOffStg + h * 128;
@@ -414,19 +423,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int k = 0; k < 32; k += 8) {
         const int u = (w * C::kHalf + k) >> 3;
         *reinterpret_cast<uint4 *>(row + ((u ^ (h & 7)) << 4)) =
-            make_uint4(pack_bf16x2(v[k], v[k + 1]), pack_bf16x2(v[k + 2], v[k + 3]),
-                       pack_bf16x2(v[k + 4], v[k + 5]), pack_bf16x2(v[k + 6], v[k + 7]));
+            make_uint4(pack_f16x2_sat(v[k], v[k + 1]), pack_f16x2_sat(v[k + 2], v[k + 3]),
+                       pack_f16x2_sat(v[k + 4], v[k + 5]), pack_f16x2_sat(v[k + 6], v[k + 7]));
       }
       fence_proxy_async_smem();  // the bulk copy reads the tile through the async proxy
       warp_arrive(&staged[b], lane);
     };
-    // load our 32 columns of S(j) from TMEM once; the buffer is then free for QK(j+2)
+    // load our 32 columns of S(j) from TMEM once, scaled to log2 units; the
+    // buffer is then free for QK(j+2)
+    const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
     auto load_s = [&](int j, float (&v)[32]) {
       uint32_t r[32];
       tmem_ld32(lane_base + C::kSCol + (j & 1) * C::kBN + w * C::kHalf, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+      for (int k = 0; k < 32; k += 2)
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2), v[k], v[k + 1]);
       tc_fence_before();
       warp_arrive(&s_free[j & 1], lane);
     };
@@ -468,10 +480,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           const uint4 v = *reinterpret_cast<const uint4 *>(my_recv + ((u ^ (h & 7)) << 4));
           const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            f2_unpack(f2_add(f2_pack(x[k + 2 * e], x[k + 2 * e + 1]),
-                             f2_pack(__uint_as_float(pv[e] << 16), __uint_as_float(pv[e] & 0xffff0000u))),
-                      x[k + 2 * e], x[k + 2 * e + 1]);
+          for (int e = 0; e < 4; ++e) {
+            float lo, hi;
+            unpack_f16x2(pv[e], lo, hi);
+            f2_unpack(f2_add(f2_pack(x[k + 2 * e], x[k + 2 * e + 1]), f2_pack(lo, hi)), x[k + 2 * e], x[k + 2 * e + 1]);
+          }
         }
         warp_arrive(&consumed[b], lane);  // the agent tells the peer that recv[b] may be refilled
       }
@@ -491,8 +504,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       warp_arrive(&red_full[b], lane);
       ok = __all_sync(0xffffffffu, mbar_wait(&red_full[b], (i >> 1) & 1, P.err, 33, i));
       if (!ok) break;
-      const float mraw = fmaxf(red[(b * 2) * 128 + h], red[(b * 2 + 1) * 128 + h]);
-      const float mblk = mraw * P.scale_log2;  // scale > 0: the max commutes with it
+      const float mblk = fmaxf(red[(b * 2) * 128 + h], red[(b * 2 + 1) * 128 + h]);  // log2 units
       // lazy rescale: only when some row of the warp saw its max grow by more
       // than 2^8; rows whose max did not grow get alpha = 1 (exact).  Both
       // warpgroups see the same row maxima, so they decide alike.
@@ -524,15 +536,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!ok) break;
       }
       uint32_t packed[16];
-      const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2), nm2 = f2_pack(-m_used, -m_used);
+      const uint64_t nm2 = f2_pack(-m_used, -m_used);
       uint64_t acc[2] = {0, 0};  // +0.0f pairs
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
         float t0, t1;
-        f2_unpack(f2_fma(f2_pack(x[k], x[k + 1]), sc2, nm2), t0, t1);
-        const float a = ex2(t0), c = ex2(t1);
-        acc[(k >> 1) & 1] = f2_add(acc[(k >> 1) & 1], f2_pack(a, c));
-        packed[k >> 1] = pack_bf16x2(a, c);
+        f2_unpack(f2_add(f2_pack(x[k], x[k + 1]), nm2), t0, t1);
+        const uint32_t pk = pack_bf16x2(ex2(t0), ex2(t1));
+        packed[k >> 1] = pk;
+        // the denominator sums the bf16 values that PV multiplies
+        acc[(k >> 1) & 1] = f2_add(acc[(k >> 1) & 1], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
       }
       float s0, s1, s2, s3;
       f2_unpack(acc[0], s0, s1);
@@ -563,7 +576,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     auto out_of = [&](int hh) -> __nv_bfloat16 * {
       if (P.hc > 0) {  // head-sharded: rank hh / hc, token g, head hh % hc
         const int rd = hh / P.hc;
-        return P.out + ((static_cast<int64_t>(rd) * P.num_tokens + misc[3]) * P.hc + (hh - rd * P.hc)) * P.Dv +
+        return P.out + ((static_cast<int64_t>(rd) * misc[4] + misc[3]) * P.hc + (hh - rd * P.hc)) * P.Dv +
                main_dim0;
       }
       return out_row + static_cast<int64_t>(hh) * P.Dv;
@@ -678,14 +691,15 @@ dsa_status launch_attn(const void *q, int32_t tpr, const AttnParams &P, cudaStre
 using namespace dsa;
 
 static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr, const void *q,
-                                   const void *kv, int32_t num_tokens, const int32_t *topk_idx, int32_t topk,
+                                   const void *kv, int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
                                    const float *attn_sink, float softmax_scale, int32_t H, int32_t D, int32_t Dv,
                                    int32_t cp_size, void *out, dsa_stream_t stream) {
   if (!md || !q || !kv || !topk_idx || !out) return DSA_ERR_INVALID_ARG;
-  if (!md->scalars || !md->local_query_start_loc || !md->local_req_kv_base || !md->local_token_pos)
+  if (!md->scalars || !md->local_query_start_loc || !md->local_req_kv_base || !md->local_token_pos ||
+      !md->local_req_pos_base)
     return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(topk_idx)) return DSA_ERR_INVALID_ARG;
-  if (batch < 0 || tpr < 0 || num_tokens < 1 || topk < 1) return DSA_ERR_SHAPE;
+  if (batch < 0 || tpr < 0 || num_kv_rows < 1 || topk < 1) return DSA_ERR_SHAPE;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return DSA_ERR_INVALID_ARG;
   if (cp_size < 0) return DSA_ERR_INVALID_ARG;
   if (cp_size > 0 && (H < 1 || H % cp_size != 0)) return DSA_ERR_SHAPE;
@@ -706,7 +720,7 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
                H,
                D,
                Dv,
-               num_tokens,
+               num_kv_rows,
                cp_size > 0 ? H / cp_size : 0,
                err};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -714,21 +728,21 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
 }
 
 extern "C" dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
-                                              const void *q, const void *kv, int32_t num_tokens,
+                                              const void *q, const void *kv, int32_t num_kv_rows,
                                               const int32_t *topk_idx, int32_t topk, const float *attn_sink,
                                               float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
                                               dsa_stream_t stream) {
-  return sparse_attn_impl(md, batch, tpr, q, kv, num_tokens, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv, 0,
+  return sparse_attn_impl(md, batch, tpr, q, kv, num_kv_rows, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv, 0,
                           out, stream);
 }
 
 extern "C" dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_metadata *md, int32_t batch,
                                                           int32_t tpr, const void *q, const void *kv,
-                                                          int32_t num_tokens, const int32_t *topk_idx, int32_t topk,
+                                                          int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
                                                           const float *attn_sink, float softmax_scale, int32_t H,
                                                           int32_t D, int32_t Dv, int32_t cp_size, void *out,
                                                           dsa_stream_t stream) {
   if (cp_size < 1) return DSA_ERR_INVALID_ARG;
-  return sparse_attn_impl(md, batch, tpr, q, kv, num_tokens, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv,
+  return sparse_attn_impl(md, batch, tpr, q, kv, num_kv_rows, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv,
                           cp_size, out, stream);
 }

@@ -27,22 +27,32 @@ from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_meta
 
 class DSAPrefill:
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
-                 softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1):
+                 softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1,
+                 prefix_lens=None):
+        """``lengths``: query tokens per request.  ``prefix_lens`` (chunked
+        prefill): KV positions per request that precede its queries; the KV
+        and index-key tensors passed to ``run`` then hold every request's
+        whole sequence (prefix + queries), requests in order."""
         self.device = torch.device(device or "cuda")
         self.lengths = [int(x) for x in lengths]
+        self.prefix_lens = [0] * len(self.lengths) if prefix_lens is None else [int(x) for x in prefix_lens]
+        if len(self.prefix_lens) != len(self.lengths) or min(self.prefix_lens, default=0) < 0:
+            raise ValueError("one non-negative prefix length per request")
         self.cp_size, self.mode = int(cp_size), int(mode)
         self.H, self.D, self.Dv, self.HI, self.DI, self.topk = H, D, Dv, HI, DI, topk
         self.scale = float(softmax_scale)
         self.T = sum(self.lengths)
         self.B = len(self.lengths)
-        self.max_kv_len = max(self.lengths)
+        self.kv_lens = [n + p for n, p in zip(self.lengths, self.prefix_lens)]
+        self.num_kv_rows = sum(self.kv_lens)
+        self.max_kv_len = max(self.kv_lens)
         self.pad, self.tpr = dsa_cp_geometry(self.T, cp_size)
         qsl = [0]
         for n in self.lengths:
             qsl.append(qsl[-1] + n)
         dev = self.device
         self.query_start_loc = torch.tensor(qsl, dtype=torch.int32, device=dev)
-        self.seq_lens = torch.tensor(self.lengths, dtype=torch.int32, device=dev)
+        self.seq_lens = torch.tensor(self.kv_lens, dtype=torch.int32, device=dev)
         self.md = [CPLocalMetadata(self.B, self.T, cp_size, dev) for _ in range(cp_size)]
         cp, tpr = cp_size, self.tpr
         self.q_split = torch.empty((cp, tpr, H, D), dtype=torch.bfloat16, device=dev)
@@ -177,11 +187,11 @@ class HostStreamedPrefill:
     INPUTS = ("q", "kv", "q_idx", "k_idx", "w", "sink")
 
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
-                 softmax_scale: float, device=None, depth: int = 2, view_streams: int = 1):
+                 softmax_scale: float, device=None, depth: int = 2, view_streams: int = 1, prefix_lens=None):
         if depth < 1:
             raise ValueError("depth must be at least 1")
         self.pipes = [DSAPrefill(lengths, cp_size, mode, H, D, Dv, HI, DI, topk, softmax_scale, device,
-                                 view_streams=view_streams) for _ in range(depth)]
+                                 view_streams=view_streams, prefix_lens=prefix_lens) for _ in range(depth)]
         self.device = self.pipes[0].device
         self.depth = depth
         self.dev_in = [None] * depth

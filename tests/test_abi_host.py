@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     for code, name in _lib.STATUS.items():
         assert lib.dsa_status_string(code).decode().startswith(name)
 
@@ -49,14 +49,15 @@ def test_metadata_sizes_and_bind(lib):
     B, T, cp = 4, 11805, 4
     n = dsa.dsa_cp_metadata_sizes(B, T, cp)
     tpr = O.padded_geometry(T, cp)[1]
-    assert n == 8 + 2 * (B + 1) + 3 * B + tpr
+    assert n == 10 + 2 * (B + 1) + 4 * B + tpr
     md = _lib.LocalMetadata()
     base = 0x10000
     assert lib.dsa_cp_metadata_bind(C.c_void_p(base), B, T, cp, C.byref(md)) == 0
     offs = [md.scalars, md.local_query_start_loc, md.local_seq_lens, md.local_kv_start_loc, md.local_req_id,
-            md.local_req_kv_base, md.local_token_pos]
-    assert [(o - base) // 4 for o in offs] == [0, 8, 8 + B + 1, 8 + 2 * B + 1, 8 + 3 * B + 2, 8 + 4 * B + 2,
-                                                8 + 5 * B + 2]
+            md.local_req_kv_base, md.local_req_pos_base, md.local_token_pos]
+    assert [(o - base) // 4 for o in offs] == [0, 10, 10 + B + 1, 10 + 2 * B + 1, 10 + 3 * B + 2, 10 + 4 * B + 2,
+                                                10 + 5 * B + 2, 10 + 6 * B + 2]
+    assert (md.local_token_pos - base) // 4 + tpr == n
 
 
 def test_workspace_size_holds_a_tile():

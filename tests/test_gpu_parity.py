@@ -17,7 +17,7 @@ import sparse_attention_prefill_cp_gb300 as dsa
 from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill, HostStreamedPrefill
 from oracle import dsa_oracle as O
 from workloads import (HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, LONG_8K, VARLEN_4, LONG_64K, MIXED_16,
-                       Workload, draw_inputs, sample_rows)
+                       Workload, chunk_inputs, draw_inputs, sample_rows)
 
 pytestmark = pytest.mark.gpu
 MODES = (IN_SEQ_SPLIT, ROUND_ROBIN, HEAD_TAIL)
@@ -70,9 +70,29 @@ def test_metadata_bit_exact(lengths, cp, mode):
     dsa.dsa_poll_device_error()
 
 
-def test_metadata_prefix_is_reported():
+PREFIX_META_CASES = [([3, 2], [2, 0], 2), ([4], [6], 3), ([8000, 800, 5, 3000], [100, 0, 7, 2000], 4),
+                     ([17, 1, 30, 2, 9], [0, 5, 0, 1, 100], 5), ([64], [65472], 8)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("q_lens,prefixes,cp", PREFIX_META_CASES, ids=lambda v: str(v)[:24])
+def test_metadata_with_prefix_bit_exact(q_lens, prefixes, cp, mode):
+    # chunked prefill: seq_lens = prefix + query length
+    T = sum(q_lens)
+    seq_lens = [n + p for n, p in zip(q_lens, prefixes)]
+    qsl = torch.tensor(qsl_of(q_lens), dtype=torch.int32, device="cuda")
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    for r in range(cp):
+        got = dsa.dsa_cp_build_local_metadata(qsl, sl, T, cp, r, mode).to_host()
+        ref = O.build_local_metadata(qsl_of(q_lens), seq_lens, cp, r, mode)
+        for k, v in ref.items():
+            assert got[k] == v, (k, r)
+    dsa.dsa_poll_device_error()
+
+
+def test_metadata_short_seq_lens_is_reported():
     qsl = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
-    sl = torch.tensor([6], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([3], dtype=torch.int32, device="cuda")
     dsa.dsa_cp_build_local_metadata(qsl, sl, 4, 2, 0, IN_SEQ_SPLIT)
     with pytest.raises(dsa.DSAError) as e:
         dsa.dsa_poll_device_error()
@@ -196,7 +216,7 @@ def test_indexer_scores(wl, mode):
                 continue
             j = O.request_of_slot(md, i)
             base = md["local_req_kv_base"][j]
-            p = g - base
+            p = g - md["local_req_pos_base"][j]
             ref = O.indexer_scores(qi_loc[i], w_loc[i], k_idx[base:base + p + 1])
             got = sc[i, :p + 1]
             if wl.integer:
@@ -247,7 +267,8 @@ def test_topk(wl, mode):
                 continue
             j = O.request_of_slot(md, i)
             base = md["local_req_kv_base"][j]
-            ref = O.indexer_scores(qi_loc[i], w_loc[i], k_idx[base:g + 1])
+            p = g - md["local_req_pos_base"][j]
+            ref = O.indexer_scores(qi_loc[i], w_loc[i], k_idx[base:base + p + 1])
             check_topk_row(idx[r, i], ref, base, wl.topk, exact=wl.integer)
 
 
@@ -372,6 +393,68 @@ def test_out_of_range_index_is_reported_not_read():
     assert e.value.status == 7
 
 
+# ------------------------------------------------------------------ chunked prefill (prefix KV)
+
+CHUNK_CASES = [(TINY.with_(name="tiny-chunk", lengths=(200, 56), sink=True), (150, 20)),
+               (TINY_INT.with_(name="tiny-int-chunk"), (100,)),
+               (FLOAT_FULL.with_(name="float-full-chunk"), (1800, 300)),
+               (INT_FULL.with_(name="int-full-chunk"), (2100, 0))]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("wl,prefixes", CHUNK_CASES, ids=lambda v: v.name if isinstance(v, Workload) else str(v))
+def test_chunked_prefill(wl, prefixes, mode):
+    # whole sequences drawn for wl.lengths; the chunked batch keeps the first
+    # prefixes[b] positions of request b as KV only and queries the rest
+    x = draw_inputs(wl)
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    _, whole = run_pipeline(wl, mode, xd)
+    whole = whole.clone()
+    xc, q_lens, seq_lens = chunk_inputs(xd, wl.lengths, prefixes)
+    pipe = DSAPrefill(q_lens, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      prefix_lens=prefixes)
+    out = pipe.run(xc["q"], xc["kv"], xc["q_idx"], xc["k_idx"], xc["w"], xc["sink"])
+    dsa.dsa_poll_device_error()
+    # 1. the chunk's rows of the whole-sequence prefill, bit for bit
+    rows = [g for b, (n, p) in enumerate(zip(wl.lengths, prefixes))
+            for g in range(sum(wl.lengths[:b]) + p, sum(wl.lengths[:b]) + n)]
+    assert torch.equal(out, whole[torch.tensor(rows, device="cuda")])
+    # 2. metadata, top-k and attention against the oracle on the chunked geometry
+    qc = {k: f64(v) for k, v in xc.items() if v is not None}
+    sink = qc.get("sink")
+    rng = np.random.default_rng(3)
+    idx = pipe.topk_idx.cpu().numpy()
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(qsl_of(q_lens), seq_lens, wl.cp_size, r, mode)
+        got = pipe.md[r].to_host()
+        for k, v in md.items():
+            assert got[k] == v, (k, r)
+        q_loc = O.split(qc["q"], wl.cp_size, mode)[r]
+        qi_loc = O.split(qc["q_idx"], wl.cp_size, mode)[r]
+        w_loc = O.split(qc["w"], wl.cp_size, mode)[r]
+        slots = range(pipe.tpr) if pipe.tpr <= 300 else sorted(set(rng.choice(pipe.tpr, 40, replace=False)) |
+                                                                 {0, pipe.tpr - 1})
+        for i in slots:
+            g = md["local_token_pos"][i]
+            if g < 0:
+                assert np.all(idx[r, i] == -1)
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            p = g - md["local_req_pos_base"][j]
+            ref_scores = O.indexer_scores(qi_loc[i], w_loc[i], qc["k_idx"][base:base + p + 1])
+            check_topk_row(idx[r, i], ref_scores, base, wl.topk, exact=wl.integer)
+            sel = idx[r, i][idx[r, i] >= 0]
+            ref = O.sparse_attention(q_loc[i], qc["kv"][sel], wl.scale, wl.Dv, sink)
+            check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref)
+    # 3. the head-sharded output of the chunked batch is the all-to-all of its views
+    if wl.H % wl.cp_size == 0:
+        fused = pipe.run_headsharded(xc["q"], xc["kv"], xc["q_idx"], xc["k_idx"], xc["w"], xc["sink"]).clone()
+        pipe.run(xc["q"], xc["kv"], xc["q_idx"], xc["k_idx"], xc["w"], xc["sink"])
+        assert torch.equal(fused, pipe.all_to_all_heads())
+    dsa.dsa_poll_device_error()
+
+
 # ------------------------------------------------------------------ full-size configurations, sampled rows
 
 def _device_inputs(wl):
@@ -407,9 +490,10 @@ def test_full_size_sampled_rows(wl, mode):
         i = md_all[r]["local_token_pos"].index(g)
         j = O.request_of_slot(md_all[r], i)
         base = md_all[r]["local_req_kv_base"][j]
+        p = g - md_all[r]["local_req_pos_base"][j]
         qi = f64(xd["q_idx"][g])
         w = f64(xd["w"][g])
-        ref_scores = O.indexer_scores(qi, w, k_idx[base:g + 1])
+        ref_scores = O.indexer_scores(qi, w, k_idx[base:base + p + 1])
         row = pipe.topk_idx[r, i].cpu().numpy()
         check_topk_row(row, ref_scores, base, wl.topk, exact=False)
         sel = row[row >= 0]
