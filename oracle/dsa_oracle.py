@@ -64,6 +64,9 @@ design notes):
       rank-major order already is the flat order; for round-robin the rows are
       put back in flat order as by rerange); H must divide by cp.
 
+  R12 the FP8 latent-KV cache ([blog] 1, named only): the OCP E4M3 row layout
+      of the FP8 section at the end of this file.
+
 parity pins: every function here is pinned by tests/test_oracle_pins.py
 against worked examples from the pages (tests/golden/), closed forms,
 invariants, brute force on tiny inputs and independent library routines.
@@ -413,3 +416,108 @@ def prefill(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mod
         md = build_local_metadata(query_start_loc, seq_lens, cp_size, r, mode)
         _, outs[r] = prefill_view(md, qs[r], qis[r], ws[r], kv, k_idx, topk, scale, Dv, sink)
     return rerange(outs, T, cp_size, mode)
+
+
+# --------------------------------------------------------------------------
+# FP8 latent-KV cache (R12)
+# --------------------------------------------------------------------------
+#
+# R12 "FP8 KV Cache" ([blog] 1 核心改动总结: round-robin-split lifts the old
+#     restriction that NSA prefill CP could not use an FP8 KV cache) is named
+#     without a format.  Reading taken: the published DeepSeek-V3.2 layout of
+#     one latent row -- the Dv value ("nope") columns as OCP FP8 E4M3 codes with
+#     one fp32 scale per tile of 128 columns (scale = tile max|x| / 448, 1 for
+#     an all-zero tile), then the D - Dv rope columns kept as bf16, the row
+#     padded with zero bytes to a multiple of 16.  Codes round to nearest even
+#     and saturate at +-448; decisions are taken in fp32 (x / scale).  The
+#     attention over the cache is the attention over its dequantized rows,
+#     bf16(fp32(decode(code)) * scale).
+
+E4M3_MAX = 448.0
+FP8_TILE = 128
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of OCP E4M3 codes (1 sign, 4 exponent bits with bias 7, 3
+    mantissa bits; exponent field 0 is subnormal, S.1111.111 is NaN, no
+    infinities) as float64."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = (c >> 7) & 1
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Nearest E4M3 code of each finite value, ties to the even mantissa,
+    magnitudes above 448 clamped to 448; the sign is kept (also of zero)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                       # a = f * 2^ex, f in [0.5, 1)
+    binade = np.maximum(ex - 1, -6)           # subnormals share the 2^-6 binade's step
+    step = np.exp2(binade - 3.0)              # 3 mantissa bits
+    r = np.rint(a / step) * step              # round half to even (exact scaling)
+    r = np.minimum(r, E4M3_MAX)
+    _, ex2 = np.frexp(r)
+    e_unb = ex2 - 1
+    normal = r >= 2.0 ** -6
+    e_field = np.where(normal, e_unb + 7, 0)
+    m_field = np.where(normal, r / np.exp2(e_unb.astype(np.float64)) * 8.0 - 8.0, r / 2.0 ** -9)
+    code = (e_field.astype(np.int64) << 3) | np.rint(m_field).astype(np.int64)
+    code = code | (np.signbit(v).astype(np.int64) << 7)
+    return code.astype(np.uint8)
+
+
+def bf16_round(x) -> np.ndarray:
+    """fp32 values rounded to the nearest bf16 (ties to even), as float32."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def kv_fp8_row_bytes(D: int, Dv: int) -> int:
+    """Bytes of one cache row: Dv codes, 4 bytes per 128-column tile, 2 bytes
+    per rope column, padded to a multiple of 16."""
+    tiles = -(-Dv // FP8_TILE)
+    raw = Dv + 4 * tiles + 2 * (D - Dv)
+    return -(-raw // 16) * 16
+
+
+def kv_fp8_quantize(kv, Dv: int) -> np.ndarray:
+    """bf16-valued latent rows kv [R, D] -> cache bytes [R, kv_fp8_row_bytes]."""
+    x = np.asarray(kv, dtype=np.float32)
+    R, D = x.shape
+    tiles = -(-Dv // FP8_TILE)
+    out = np.zeros((R, kv_fp8_row_bytes(D, Dv)), dtype=np.uint8)
+    for t in range(tiles):
+        cols = slice(t * FP8_TILE, min((t + 1) * FP8_TILE, Dv))
+        amax = np.abs(x[:, cols]).max(axis=1)
+        scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        v = (x[:, cols] / scale[:, None]).astype(np.float32)   # fp32 division, rounded to nearest
+        out[:, cols] = e4m3_encode(v)
+        out[:, Dv + 4 * t: Dv + 4 * t + 4] = scale.view(np.uint8).reshape(R, 4)
+    rope = x[:, Dv:].astype(np.float32).view(np.uint32) >> 16     # bf16-valued: the upper half
+    off = Dv + 4 * tiles
+    out[:, off: off + 2 * (D - Dv)] = rope.astype(np.uint16).view(np.uint8).reshape(R, 2 * (D - Dv))
+    return out
+
+
+def kv_fp8_dequantize(cache, D: int, Dv: int) -> np.ndarray:
+    """Cache bytes [R, row_bytes] -> the latent rows [R, D] it stands for
+    (bf16 values as float64): value column c of tile t is
+    bf16(fp32(decode(code)) * scale_t), rope columns are the stored bf16."""
+    b = np.asarray(cache, dtype=np.uint8)
+    R = b.shape[0]
+    tiles = -(-Dv // FP8_TILE)
+    out = np.zeros((R, D), dtype=np.float64)
+    for t in range(tiles):
+        cols = slice(t * FP8_TILE, min((t + 1) * FP8_TILE, Dv))
+        scale = np.ascontiguousarray(b[:, Dv + 4 * t: Dv + 4 * t + 4]).view(np.float32).reshape(R)
+        val = e4m3_decode(b[:, cols]).astype(np.float32) * scale[:, None]    # fp32 product, rounded
+        out[:, cols] = bf16_round(val)
+    off = Dv + 4 * tiles
+    rope16 = np.ascontiguousarray(b[:, off: off + 2 * (D - Dv)]).view(np.uint16).astype(np.uint32) << 16
+    out[:, Dv:] = rope16.view(np.float32)
+    return out

@@ -443,3 +443,78 @@ def test_short_rows_select_everything():
     assert list(idx[63]) == list(range(64))
     assert np.all(idx[64] >= 0) and len(set(idx[64])) == 64 and idx[64].max() <= 64
     assert np.all(idx[200] >= 0) and np.all(np.diff(idx[200]) > 0) and idx[200].max() <= 200
+
+
+# ---------------------------------------------------------------- FP8 latent-KV cache (R12)
+# The pages name an FP8 KV cache without a format; the reading is the OCP E4M3
+# code with per-128-column fp32 scales and bf16 rope columns.  Pins: values the
+# E4M3 format fixes, torch's own float8_e4m3fn conversion (a library routine),
+# round trips and the quantisation error bound.
+
+def test_e4m3_format_values():
+    # sign | exponent (bias 7) | 3 mantissa bits; exponent 0 is subnormal
+    pairs = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5, 0x38: 1.0,
+             0x3C: 1.5, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in pairs.items():
+        assert O.e4m3_decode([c])[0] == v, hex(c)
+    assert np.isnan(O.e4m3_decode([0x7F, 0xFF])).all()
+    assert np.signbit(O.e4m3_decode([0x80])[0]) and O.e4m3_decode([0x80])[0] == 0.0
+    vals = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(vals) > 0)  # positive codes are ordered by value
+
+
+def test_e4m3_encode_matches_torch_and_rounds_ties_to_even():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = O.e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    assert np.array_equal(O.e4m3_encode(vals[finite]), codes[finite])
+    pos = np.sort(vals[(vals > 0) & finite])
+    mids = (pos[:-1] + pos[1:]) / 2          # exact ties between neighbours
+    got = O.e4m3_decode(O.e4m3_encode(mids))
+    lo_even = (O.e4m3_encode(pos[:-1]) & 1) == 0
+    assert np.array_equal(got, np.where(lo_even, pos[:-1], pos[1:]))
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal(100000) * np.exp2(rng.uniform(-14, 8, 100000))).astype(np.float32)
+    v = np.clip(v, -447.0, 447.0).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(v), ref)
+    assert O.e4m3_encode([500.0, -1e6, 449.0])[0] == 0x7E and O.e4m3_encode([-1e6])[0] == 0xFE
+
+
+def test_bf16_round_matches_torch():
+    x = np.concatenate([np.random.default_rng(8).standard_normal(20000).astype(np.float32),
+                        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8)], dtype=np.float32)])
+    assert np.array_equal(O.bf16_round(x), torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+
+
+@pytest.mark.parametrize("D,Dv", [(576, 512), (64, 48)])
+def test_kv_fp8_cache_layout_and_error_bound(D, Dv):
+    gen = torch.Generator().manual_seed(11)
+    kv = (torch.randn(300, D, generator=gen) * torch.exp2(torch.randn(300, 1, generator=gen) * 3)).to(torch.bfloat16)
+    kv[7, :] = 0.0  # an all-zero row: scale 1, codes 0
+    x = kv.float().numpy()
+    c = O.kv_fp8_quantize(x, Dv)
+    tiles = -(-Dv // 128)
+    assert c.shape == (300, O.kv_fp8_row_bytes(D, Dv)) and c.shape[1] % 16 == 0
+    assert O.kv_fp8_row_bytes(576, 512) == 656
+    rope = np.ascontiguousarray(c[:, Dv + 4 * tiles: Dv + 4 * tiles + 2 * (D - Dv)]).view(np.uint16)
+    assert np.array_equal(rope, kv[:, Dv:].view(torch.int16).numpy().view(np.uint16))
+    assert np.all(c[:, Dv + 4 * tiles + 2 * (D - Dv):] == 0)
+    d = O.kv_fp8_dequantize(c, D, Dv)
+    assert np.array_equal(d[:, Dv:], x[:, Dv:])
+    for t in range(tiles):
+        cols = slice(t * 128, min((t + 1) * 128, Dv))
+        scale = np.ascontiguousarray(c[:, Dv + 4 * t: Dv + 4 * t + 4]).view(np.float32).reshape(-1)
+        amax = np.abs(x[:, cols]).max(axis=1)
+        assert np.array_equal(scale, np.where(amax > 0, (amax / np.float32(448)).astype(np.float32), 1.0))
+        # the largest magnitude of a tile encodes to +-448
+        j = np.abs(x[:, cols]).argmax(axis=1)
+        top = c[np.arange(300), t * 128 + j]
+        nz = amax > 0
+        assert np.all((top[nz] & 0x7F) == 0x7E)
+        # error: half an E4M3 step at the value's binade (scaled) plus half a bf16 ulp
+        v = np.abs(x[:, cols]) / scale[:, None]
+        half_step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(v, 2.0 ** -20))), -6) - 4) * scale[:, None]
+        bound = half_step + np.abs(d[:, cols]) * 2.0 ** -8 + 1e-30
+        assert np.all(np.abs(d[:, cols] - x[:, cols]) <= bound)
+    assert np.all(c[7, :Dv] == 0) and np.all(d[7] == 0)
