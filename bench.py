@@ -424,8 +424,26 @@ def run_ours(args, wl, mode, rank, world):
         aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
                      "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
     aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
+    # FP8 latent-KV cache: quantise / dequantise as HBM passes (bytes read +
+    # written), and the a3-a5 core over the cache (dequantisation + views)
+    cache = dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv)
+    kv_rows = torch.empty_like(x["kv"])
+    fp8_bytes = x["kv"].shape[0] * (wl.D * 2 + cache.shape[1])
+    for name, fn in (("kv_fp8_quantize", lambda: dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv, cache)),
+                     ("kv_fp8_dequantize", lambda: dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows))):
+        ms = timed(fn)
+        aux[name] = {"ms": ms, "bytes": fp8_bytes, "gbs": fp8_bytes / (ms / 1e3) / 1e9,
+                     "frac_hbm": fp8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+
+    def fp8_core():
+        rows = dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows)
+        pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
+
+    aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
     aux["note"] = ("a2a_heads: all views' [tpr][H][Dv] outputs -> [cp][T][H/cp][Dv] head-sharded; "
-                   "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores")
+                   "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
+                   "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
+                   "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views)")
     dsa.dsa_poll_device_error()
 
     launches = pipe.launches_per_step() * args.steps

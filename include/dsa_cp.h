@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define DSA_CP_ABI_VERSION 2
+#define DSA_CP_ABI_VERSION 3
 
 typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 
@@ -317,6 +317,35 @@ dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_metadata *md, 
                                                const int32_t *topk_idx, int32_t topk, const float *attn_sink,
                                                float softmax_scale, int32_t H, int32_t D, int32_t Dv,
                                                int32_t cp_size, void *out, dsa_stream_t stream);
+
+/*
+ * FP8 latent-KV cache ([blog] "1 核心改动总结": round-robin-split lifts the
+ * restriction that NSA prefill CP could not use an FP8 KV cache; the page
+ * gives no format).  Row layout taken (the published DeepSeek-V3.2 one):
+ *   bytes [0, Dv)                  the Dv value columns as OCP FP8 E4M3 codes
+ *   bytes [Dv, Dv + 4*tiles)       one fp32 scale per tile of 128 value columns
+ *                                  (tiles = ceil(Dv / 128)); scale = tile
+ *                                  max|x| / 448, 1 for an all-zero tile
+ *   next 2*(D - Dv) bytes          the rope columns, bf16 as given
+ *   zero bytes up to row_bytes     (a multiple of 16; 656 for D 576, Dv 512)
+ * Codes are round-to-nearest-even of x / scale (fp32, IEEE division),
+ * saturated at +-448.  Supported: 1 <= Dv <= D <= 65536, Dv and D - Dv
+ * multiples of 8 (else DSA_ERR_SHAPE).  Byte-exact results.
+ */
+/* Host only: bytes of one cache row. */
+dsa_status dsa_kv_fp8_row_bytes(int32_t D, int32_t Dv, size_t *bytes);
+
+/* Quantise kv bf16 [num_rows][D] into cache [num_rows][row_bytes] (device
+ * buffers, 16-byte aligned, caller-owned; asynchronous on `stream`). */
+dsa_status dsa_kv_fp8_quantize(const void *kv, int32_t num_rows, int32_t D, int32_t Dv, void *cache,
+                               dsa_stream_t stream);
+
+/* The rows a cache stands for: kv bf16 [num_rows][D] with value column c of
+ * tile t = bf16(fp32(decode(code)) * scale_t) (one fp32 rounding, then round
+ * to nearest bf16) and the rope columns as stored.  The sparse attention over
+ * an FP8 cache reads these rows. */
+dsa_status dsa_kv_fp8_dequantize(const void *cache, int32_t num_rows, int32_t D, int32_t Dv, void *kv,
+                                 dsa_stream_t stream);
 
 /* Synchronise `stream`, then return (and clear) the first error a kernel
  * recorded on the current device since the last poll: DSA_OK, or

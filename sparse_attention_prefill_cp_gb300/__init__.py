@@ -295,6 +295,43 @@ def dsa_sparse_attn_prefill_headsharded(md: CPLocalMetadata, q: torch.Tensor, kv
     return out
 
 
+def dsa_kv_fp8_row_bytes(D: int, Dv: int) -> int:
+    """Bytes of one FP8 latent-KV cache row (include/dsa_cp.h)."""
+    n = C.c_size_t()
+    check(load().dsa_kv_fp8_row_bytes(D, Dv, C.byref(n)), "dsa_kv_fp8_row_bytes")
+    return n.value
+
+
+def dsa_kv_fp8_quantize(kv: torch.Tensor, Dv: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kv bf16 [R, D] -> FP8 cache uint8 [R, row_bytes]."""
+    _need(kv, torch.bfloat16, "kv")
+    R, D = kv.shape
+    rb = dsa_kv_fp8_row_bytes(D, Dv)
+    if out is None:
+        out = torch.empty((R, rb), dtype=torch.uint8, device=kv.device)
+    _need(out, torch.uint8, "out")
+    if tuple(out.shape) != (R, rb):
+        raise ValueError(f"out must be [{R}, {rb}]")
+    check(load().dsa_kv_fp8_quantize(_ptr(kv), R, D, Dv, _ptr(out), _stream(stream)), "dsa_kv_fp8_quantize")
+    return out
+
+
+def dsa_kv_fp8_dequantize(cache: torch.Tensor, D: int, Dv: int, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """FP8 cache uint8 [R, row_bytes] -> the bf16 rows [R, D] it stands for."""
+    _need(cache, torch.uint8, "cache")
+    R = cache.shape[0]
+    if cache.dim() != 2 or cache.shape[1] != dsa_kv_fp8_row_bytes(D, Dv):
+        raise ValueError("cache rows do not have the FP8 row size of (D, Dv)")
+    if out is None:
+        out = torch.empty((R, D), dtype=torch.bfloat16, device=cache.device)
+    _need(out, torch.bfloat16, "out")
+    if tuple(out.shape) != (R, D):
+        raise ValueError(f"out must be [{R}, {D}]")
+    check(load().dsa_kv_fp8_dequantize(_ptr(cache), R, D, Dv, _ptr(out), _stream(stream)), "dsa_kv_fp8_dequantize")
+    return out
+
+
 def dsa_poll_device_error(stream=None) -> None:
     """Synchronise and raise DSAError if a kernel recorded a device-side error
     (with the site that recorded it)."""

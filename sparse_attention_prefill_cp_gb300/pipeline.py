@@ -22,17 +22,19 @@ import torch
 
 from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_metadata, dsa_cp_geometry,
                dsa_cp_rerange, dsa_cp_split, dsa_indexer_topk, dsa_indexer_topk_workspace_size,
-               dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_headsharded)
+               dsa_kv_fp8_dequantize, dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_headsharded)
 
 
 class DSAPrefill:
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
                  softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1,
-                 prefix_lens=None):
+                 prefix_lens=None, kv_fp8: bool = False):
         """``lengths``: query tokens per request.  ``prefix_lens`` (chunked
         prefill): KV positions per request that precede its queries; the KV
         and index-key tensors passed to ``run`` then hold every request's
-        whole sequence (prefix + queries), requests in order."""
+        whole sequence (prefix + queries), requests in order.  ``kv_fp8``:
+        the latent KV passed to ``run`` is the FP8 cache (uint8 rows of
+        dsa_kv_fp8_row_bytes), dequantised once per batch before the views."""
         self.device = torch.device(device or "cuda")
         self.lengths = [int(x) for x in lengths]
         self.prefix_lens = [0] * len(self.lengths) if prefix_lens is None else [int(x) for x in prefix_lens]
@@ -69,15 +71,19 @@ class DSAPrefill:
         self.workspace = self.workspaces[0]
         self._side = None
         self.out_hs = None  # [cp][T][H / cp][Dv], allocated on first use
+        self.kv_fp8 = bool(kv_fp8)
+        self.kv_rows = (torch.empty((self.num_kv_rows, D), dtype=torch.bfloat16, device=dev) if self.kv_fp8
+                        else None)
 
     def launches_per_step(self) -> int:
-        """Kernel launches of one ``run``: metadata per view, 3 splits, per view
-        (indexer + top-k) per workspace chunk and one attention, 1 rerange."""
+        """Kernel launches of one ``run``: metadata per view, 3 splits, the FP8
+        dequantisation (if any), per view (indexer + top-k) per workspace chunk
+        and one attention, 1 rerange."""
         ld = (self.max_kv_len + 3) // 4 * 4
         tile = 8 if self.HI == 64 else 128
         rows_fit = (self.workspace.numel() // (ld * 4)) // tile * tile
         chunks = -(-self.tpr // rows_fit)
-        return self.cp_size + 3 + self.cp_size * (2 * chunks + 1) + 1
+        return self.cp_size + 3 + int(self.kv_fp8) + self.cp_size * (2 * chunks + 1) + 1
 
     def metadata(self, stream=None):                                     # a1
         for r in range(self.cp_size):
@@ -94,6 +100,14 @@ class DSAPrefill:
                          self.topk_idx[r], self.workspace if workspace is None else workspace, stream)
         dsa_sparse_attn_prefill(self.md[r], self.q_split[r], kv, self.topk_idx[r], self.scale, self.Dv, sink,
                                 self.out_split[r], stream)
+
+    def latent_kv(self, kv, stream=None):
+        """The bf16 latent rows the attention reads: ``kv`` itself, or the
+        rows an FP8 cache stands for (dequantised into a buffer of this
+        object)."""
+        if not self.kv_fp8:
+            return kv
+        return dsa_kv_fp8_dequantize(kv, self.D, self.Dv, self.kv_rows, stream)
 
     def side_streams(self):
         if self._side is None:
@@ -136,6 +150,7 @@ class DSAPrefill:
         self.split(q, q_idx, w, stream)
         if "core_start" in ev:
             ev["core_start"].record(s)
+        kv = self.latent_kv(kv, s)
         self.views(kv, k_idx, sink, s)
         if "core_end" in ev:
             ev["core_end"].record(s)
@@ -163,6 +178,7 @@ class DSAPrefill:
         out = self._head_sharded_buffer()
         self.metadata(stream)
         self.split(q, q_idx, w, stream)
+        kv = self.latent_kv(kv, stream)
         for r in range(self.cp_size):
             dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
                              self.topk_idx[r], self.workspace, stream)

@@ -455,6 +455,61 @@ def test_chunked_prefill(wl, prefixes, mode):
     dsa.dsa_poll_device_error()
 
 
+# ------------------------------------------------------------------ FP8 latent-KV cache
+
+@pytest.mark.parametrize("D,Dv,R", [(64, 48, 257), (576, 512, 8192)])
+def test_kv_fp8_quantize_and_dequantize_bit_exact(D, Dv, R):
+    gen = torch.Generator().manual_seed(21)
+    kv = torch.randn(R, D, generator=gen) * torch.exp2(torch.randn(R, 1, generator=gen) * 4)
+    kv[3] = 0.0                       # all-zero row: scale 1
+    kv[5, :Dv] *= 1e-6                # tiny values next to large ones in row 6
+    kv[6, 0] = 1e4
+    kv[6, 1:Dv] = torch.randn(Dv - 1, generator=gen) * 1e-4   # many codes round to +-0
+    kv = kv.to(torch.bfloat16)
+    cache = dsa.dsa_kv_fp8_quantize(kv.cuda(), Dv)
+    deq = dsa.dsa_kv_fp8_dequantize(cache, D, Dv)
+    dsa.dsa_poll_device_error()
+    ref = O.kv_fp8_quantize(kv.float().numpy(), Dv)
+    got = cache.cpu().numpy()
+    assert got.shape == ref.shape
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])], ref[tuple(bad[0])])
+    ref_deq = O.kv_fp8_dequantize(ref, D, Dv)
+    assert np.array_equal(deq.cpu().double().numpy(), ref_deq)
+
+
+@pytest.mark.parametrize("mode", (IN_SEQ_SPLIT, ROUND_ROBIN))
+@pytest.mark.parametrize("wl", [TINY.with_(name="tiny-sink", sink=True), FLOAT_FULL], ids=lambda w: w.name)
+def test_prefill_over_fp8_kv_cache(wl, mode):
+    # the path over an FP8 cache is the bf16 path over the rows the cache
+    # stands for: bit-identical to it, and within the attention bar of the
+    # oracle run on the oracle's own dequantised rows
+    x = draw_inputs(wl)
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    cache = dsa.dsa_kv_fp8_quantize(xd["kv"], wl.Dv)
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      kv_fp8=True)
+    out = pipe.run(xd["q"], cache, xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"]).clone()
+    dsa.dsa_poll_device_error()
+    kv_ref = O.kv_fp8_dequantize(O.kv_fp8_quantize(x["kv"].float().numpy(), wl.Dv), wl.D, wl.Dv)
+    assert np.array_equal(pipe.kv_rows.cpu().double().numpy(), kv_ref)
+    _, out_bf16 = run_pipeline(wl, mode, dict(xd, kv=pipe.kv_rows.clone()))
+    assert torch.equal(out, out_bf16)
+    sink = None if x["sink"] is None else f64(x["sink"])
+    idx = pipe.topk_idx.cpu().numpy()
+    rng = np.random.default_rng(4)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
+        q_loc, _, _ = _view_inputs(wl, mode, x, r)
+        slots = range(pipe.tpr) if pipe.tpr <= 300 else sorted(set(rng.choice(pipe.tpr, 40, replace=False)))
+        for i in slots:
+            if md["local_token_pos"][i] < 0:
+                continue
+            sel = idx[r, i][idx[r, i] >= 0]
+            ref = O.sparse_attention(q_loc[i], kv_ref[sel], wl.scale, wl.Dv, sink)
+            check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref)
+
+
 # ------------------------------------------------------------------ full-size configurations, sampled rows
 
 def _device_inputs(wl):
