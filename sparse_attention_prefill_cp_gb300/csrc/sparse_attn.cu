@@ -85,16 +85,19 @@ struct AttnCfg {
   static constexpr int kTmemCols = (kQCol + NMAIN * 32) <= 256 ? 256 : 512;
   // shared memory
   static constexpr int kRecvBytes = SPLIT ? 128 * kBN * 2 : 0;  // one partial-S tile (fp16), rows swizzled
-  static constexpr int kPBytes = 128 * 128;                     // P tile [128 heads][64 keys] bf16, SW128
+  // P [128 heads][64 keys] bf16, SW128: for the pair it overwrites the peer's
+  // partial-S tile of the same block (same row layout), so P is double
+  // buffered by the two receive tiles; the single CTA keeps its own tile
+  static constexpr int kPBytes = SPLIT ? 0 : 128 * 128;
   static constexpr int kOffStage = 0;
   static constexpr int kOffQStage = kOffStage + kStageBytes;  // Q main staged in stages 1..2 at start
   static constexpr int kOffQTail = kOffStage + kStages * kStageBytes;
   static constexpr int kOffRecv = kOffQTail + kQTail;
-  static constexpr int kOffStg = kOffRecv + 2 * kRecvBytes;   // our partial-S tile on its way out
-  static constexpr int kOffP = kOffStg + kRecvBytes;
+  static constexpr int kOffStg = kOffRecv + 2 * kRecvBytes;   // our partial-S tiles on their way out (two)
+  static constexpr int kOffP = kOffStg + 2 * kRecvBytes;
   static constexpr int kOffRed = kOffP + kPBytes;             // [3][2 warpgroups][128] floats
   static constexpr int kOffBar = kOffRed + 3 * 2 * 128 * 4;
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 * 10 + 2;
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 * 9 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 32 + 1024;
   // the tiny variant asks for enough smem that at most two CTAs share an SM's TMEM
@@ -152,14 +155,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *s_full = kv_empty + C::kStages;    // [2] QK done (MMA commit)
   uint64_t *s_free = s_full + 2;               // [2] S read out of TMEM (8 softmax warps)
   uint64_t *p_full = s_free + 2;               // [2] P tile written (8 softmax warps)
-  uint64_t *pv_done = p_full + 2;              // [2] PV done, P tile free (MMA commit)
+  uint64_t *pv_done = p_full + 2;              // [2] PV done, its P tile free (MMA commit)
   uint64_t *recv_full = pv_done + 2;           // [2] the peer's partial S landed (st.async tx)
-  uint64_t *recv_empty = recv_full + 2;        // [2] the peer consumed what we sent (peer's agent)
+  uint64_t *recv_empty = recv_full + 2;        // [2] the peer is done with what we sent (peer's agent)
   uint64_t *red_full = recv_empty + 2;         // [2] both warpgroups' block maxima written (8 warps)
   uint64_t *staged = red_full + 2;             // [2] our partial-S tile written (8 softmax warps)
   uint64_t *stg_free = staged + 2;             // [2] the bulk copy has read our tile (sender)
-  uint64_t *consumed = stg_free + 2;           // [2] we have read the peer's tile (8 softmax warps)
-  uint64_t *fin_full = consumed + 2;           // both warpgroups' denominators written (8 warps)
+  uint64_t *fin_full = stg_free + 2;           // both warpgroups' denominators written (8 warps)
   uint64_t *o_staged = fin_full + 1;           // normalised O rows staged in smem (8 warps)
   int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p, [3] g, [4] T
   float *red = reinterpret_cast<float *>(smem + C::kOffRed);
@@ -204,7 +206,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&red_full[b], 8);
       mbar_init(&staged[b], 8);
       mbar_init(&stg_free[b], 1);
-      mbar_init(&consumed[b], 8);
     }
     mbar_init(fin_full, 8);
     mbar_init(o_staged, 8);
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t st_addr = smem_u32(smem + C::kOffStage);
       const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
       const uint32_t p_addr = smem_u32(smem + C::kOffP);
+      const uint32_t recv_addr = smem_u32(smem + C::kOffRecv);
       bool ok = mbar_wait(q_full, 0, P.err, 23) && mbar_wait(q_ready, 0, P.err, 23);
       tc_fence_after();
       // event-driven issue: QK(j) as soon as its rows have landed and its S
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_after();
           const int bi = pv & 1, si = pv % C::kStages;
           const uint32_t vb = st_addr + si * C::kStageBytes;
-          const uint32_t pb = p_addr;
+          const uint32_t pb = C::SPLIT ? recv_addr + bi * C::kRecvBytes : p_addr;
 #pragma unroll
           for (int k = 0; k < C::kPVSteps; ++k) {
             const uint64_t a = smem_desc(pb + k * 32, 16, 1024, kLayoutSW128);
@@ -316,14 +318,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const int b = t & 1;
             if (!(ok = mbar_wait(&staged[b], (t >> 1) & 1, P.err, 35, t))) break;
             if (t >= 2 && !(ok = mbar_wait<true>(&recv_empty[b], ((t >> 1) & 1) ^ 1, P.err, 28, t))) break;
-            bulk_copy_to_peer(peer_recv + b * C::kRecvBytes, smem + C::kOffStg, C::kRecvBytes, peer_full + b * 8);
+            bulk_copy_to_peer(peer_recv + b * C::kRecvBytes, smem + C::kOffStg + b * C::kRecvBytes, C::kRecvBytes,
+                              peer_full + b * 8);
             bulk_commit();
             bulk_wait_read0();
             mbar_arrive(&stg_free[b]);
           }
           if (t >= 1) {
             const int b = (t - 1) & 1;
-            if (!(ok = mbar_wait(&consumed[b], ((t - 1) >> 1) & 1, P.err, 36, t - 1))) break;
+            // PV(t-1) has read P(t-1), which sits in the tile the peer filled
+            if (!(ok = mbar_wait(&pv_done[b], ((t - 1) >> 1) & 1, P.err, 36, t - 1))) break;
             mbar_arrive_remote_relaxed(&recv_empty[b], peer);
           }
         }
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // agree bitwise.
     auto stage = [&](int j, const float (&v)[32]) {
       const int b = j & 1;
-      uint8_t *row = smem + C::kOffStg + h * 128;
+      uint8_t *row = smem + C::kOffStg + (j & 1) * C::kRecvBytes + h * 128;
 #pragma unroll
       for (int k = 0; k < 32; k += 8) {
         const int u = (w * C::kHalf + k) >> 3;
@@ -463,7 +467,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // time it starts block i+1
         const int b1 = (i + 1) & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b1], ((i + 1) >> 1) & 1, P.err, 27, i + 1) &&
-                                         (!C::SPLIT || mbar_wait(&stg_free[b], (i >> 1) & 1, P.err, 28, i + 1)));
+                                         (!C::SPLIT || i < 1 ||
+                                          mbar_wait(&stg_free[(i + 1) & 1], ((i - 1) >> 1) & 1, P.err, 28, i + 1)));
         if (!ok) break;
         tc_fence_after();
         load_s(i + 1, nxt);
@@ -486,7 +491,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             f2_unpack(f2_add(f2_pack(x[k + 2 * e], x[k + 2 * e + 1]), f2_pack(lo, hi)), x[k + 2 * e], x[k + 2 * e + 1]);
           }
         }
-        warp_arrive(&consumed[b], lane);  // the agent tells the peer that recv[b] may be refilled
       }
       // row max over the whole block: this warpgroup's half, then the other's through smem
       const bool full = (i + 1) * C::kBN <= n_valid;
@@ -530,8 +534,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         l *= alpha;
         m_used = m_new;
       }
-      // P tile: wait until PV(i-1) has consumed it
-      if (i >= 1) {
+      // the single CTA's P tile: wait until PV(i-1) has consumed it (the pair
+      // writes P over the peer's tile of this block, which nothing else reads)
+      if (!C::SPLIT && i >= 1) {
         ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, P.err, 32, i));
         if (!ok) break;
       }
@@ -551,7 +556,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       f2_unpack(acc[0], s0, s1);
       f2_unpack(acc[1], s2, s3);
       l += (s0 + s1) + (s2 + s3);
-      uint8_t *prow = smem + C::kOffP + h * 128;
+      uint8_t *prow = smem + (C::SPLIT ? C::kOffRecv + b * C::kRecvBytes : C::kOffP) + h * 128;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int uu = w * 4 + u;
