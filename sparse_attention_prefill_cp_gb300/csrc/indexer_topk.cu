@@ -222,21 +222,32 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&t_full[g], j & 1, P.err, 18, j));
           if (!ok) break;
           tc_fence_after();
-          float acc[C::kTokPerHalf];
+          // per token, even and odd heads accumulate in the two halves of a
+          // packed fp32 pair (fma.rn.f32x2), summed at the end
+          uint64_t acc2[C::kTokPerHalf];
 #pragma unroll
-          for (int u = 0; u < C::kTokPerHalf; ++u) acc[u] = 0.f;
+          for (int u = 0; u < C::kTokPerHalf; ++u) acc2[u] = 0;  // +0.0f pairs
           const int tok0 = g * C::kTokPerGroup + half * C::kTokPerHalf;
-          const float *wrow = w_s + tok0 * C::HI;
+          const float2 *wrow2 = reinterpret_cast<const float2 *>(w_s + tok0 * C::HI);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t r[32];
             tmem_ld32(lane_base + g * 256 + half * 128 + c4 * 32, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 32; c += 2) {
               const int col = c4 * 32 + c;
-              acc[col / C::HI] = fmaf(wrow[col], fmaxf(__uint_as_float(r[c]), 0.f), acc[col / C::HI]);
+              const float2 wv = wrow2[col >> 1];
+              acc2[col / C::HI] = f2_fma(f2_pack(fmaxf(__uint_as_float(r[c]), 0.f), fmaxf(__uint_as_float(r[c + 1]), 0.f)),
+                                         f2_pack(wv.x, wv.y), acc2[col / C::HI]);
             }
+          }
+          float acc[C::kTokPerHalf];
+#pragma unroll
+          for (int u = 0; u < C::kTokPerHalf; ++u) {
+            float lo, hi;
+            f2_unpack(acc2[u], lo, hi);
+            acc[u] = lo + hi;
           }
           tc_fence_before();
           mbar_arrive(&t_empty[g]);
@@ -300,7 +311,9 @@ __device__ __forceinline__ void scan2(int a, int b, int &ea, int &eb, int &ta, i
   eb = pb + ib - b;
 }
 
-template <int TOPK>
+// CACHE: the row's order keys are kept in shared memory (dynamic, n words)
+// after the first pass, so the row is read from L2 once instead of five times.
+template <int TOPK, bool CACHE>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_metadata md, int32_t row_begin,
                                                             int32_t max_kv_len, const float *__restrict__ scores,
                                                             int64_t ld, int32_t *__restrict__ topk_idx, int *err) {
@@ -333,6 +346,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     return;
   }
   const float *row = scores + static_cast<int64_t>(blockIdx.x) * ld;
+  extern __shared__ uint32_t s_keys[];  // CACHE: [n] order keys
+  auto key_at = [&](int i) -> uint32_t { return CACHE ? s_keys[i] : order_key(row[i]); };
 
   uint32_t prefix = 0, mask = 0;
   int krem = TOPK;
@@ -340,9 +355,28 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) {
-      const uint32_t key = order_key(row[i]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    if (CACHE && pass == 0) {
+      // first pass: read the row (16-byte loads; rows start 16-byte aligned), keep its keys
+      for (int i = tid * 4; i < n; i += kTopkThreads * 4) {
+        if (i + 3 < n) {
+          const float4 v = *reinterpret_cast<const float4 *>(row + i);
+          const uint32_t k4[4] = {order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w)};
+          *reinterpret_cast<uint4 *>(s_keys + i) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) atomicAdd(&hist[k4[k] >> 24], 1u);
+        } else {
+          for (int k = i; k < n; ++k) {
+            const uint32_t key = order_key(row[k]);
+            s_keys[k] = key;
+            atomicAdd(&hist[key >> 24], 1u);
+          }
+        }
+      }
+    } else {
+      for (int i = tid; i < n; i += kTopkThreads) {
+        const uint32_t key = key_at(i);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
     }
     __syncthreads();
     if (tid < 32) {
@@ -384,7 +418,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     int c_eq = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      keys[k] = (i0 + k < n) ? order_key(row[i0 + k]) : 0u;
+      keys[k] = (i0 + k < n) ? key_at(i0 + k) : 0u;
       c_eq += (i0 + k < n && keys[k] == thr);
     }
     int e_eq, e_dummy, t_eq, t_dummy;
@@ -480,6 +514,26 @@ dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *
   return launch_indexer<C>(qmap, kmap, P, stream);
 }
 
+// Rows of up to kTopkCacheMax bytes of scores keep their keys in shared memory.
+constexpr int64_t kTopkCacheMax = 160 * 1024;
+
+template <int TOPK>
+dsa_status launch_topk(const dsa_cp_local_metadata &md, int32_t row_begin, int32_t rows, int32_t max_kv_len,
+                       const float *scores, int64_t ld, int32_t *topk_idx, int *err, cudaStream_t stream) {
+  const int64_t cache_bytes = ld * 4;
+  if (cache_bytes <= kTopkCacheMax) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<TOPK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(cache_bytes));
+    if (e != cudaSuccess) return cuda_fail(e);
+    topk_kernel<TOPK, true><<<static_cast<unsigned>(rows), kTopkThreads, static_cast<size_t>(cache_bytes), stream>>>(
+        md, row_begin, max_kv_len, scores, ld, topk_idx, err);
+  } else {
+    topk_kernel<TOPK, false><<<static_cast<unsigned>(rows), kTopkThreads, 0, stream>>>(md, row_begin, max_kv_len,
+                                                                                        scores, ld, topk_idx, err);
+  }
+  return check_launch();
+}
+
 template <class C, int TOPK>
 dsa_status run_topk(const Args &a, int32_t *topk_idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
   const int64_t ld = (static_cast<int64_t>(a.max_kv_len) + 3) / 4 * 4;
@@ -497,9 +551,8 @@ dsa_status run_topk(const Args &a, int32_t *topk_idx, void *ws, size_t ws_bytes,
     IdxParams P{*a.md, a.w, scores, ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows, err};
     st = launch_indexer<C>(qmap, kmap, P, stream);
     if (st != DSA_OK) return st;
-    topk_kernel<TOPK><<<static_cast<unsigned>(r1 - r0), kTopkThreads, 0, stream>>>(
-        *a.md, static_cast<int32_t>(r0), a.max_kv_len, scores, ld, topk_idx, err);
-    st = check_launch();
+    st = launch_topk<TOPK>(*a.md, static_cast<int32_t>(r0), r1 - static_cast<int32_t>(r0), a.max_kv_len, scores, ld,
+                           topk_idx, err, stream);
     if (st != DSA_OK) return st;
   }
   return DSA_OK;
