@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--mode", choices=["in-seq", "round-robin", "head-tail"], default=None)
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--unfused", action="store_true",
+                    help="split q and rerange the outputs as separate passes instead of in the attention")
     ap.add_argument("--view-streams", type=int, default=2,
                     help="streams the CP views are spread over (their kernels' tails overlap)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -268,29 +270,14 @@ def run_ours(args, wl, mode, rank, world):
     torch.cuda.set_device(dev)
     dsa.load()
     x = W.draw_inputs(wl, device=dev, seed_offset=rank)
+    fused = not args.unfused
     pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
-                      view_streams=args.view_streams)
+                      view_streams=args.view_streams, fused=fused)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     # attention launches timed live with events on the launching stream
     attn_events = []
-    orig_view = pipe.view
-
-    def timed_view(r, kv, k_idx, sink=None, stream=None, workspace=None):
-        st = stream or torch.cuda.current_stream()
-        dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], k_idx, pipe.w_split[r], pipe.topk, pipe.max_kv_len,
-                             pipe.topk_idx[r], pipe.workspace if workspace is None else workspace, st)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)  # on the stream the attention is launched on
-        dsa.dsa_sparse_attn_prefill(pipe.md[r], pipe.q_split[r], kv, pipe.topk_idx[r], pipe.scale, pipe.Dv, sink,
-                                    pipe.out_split[r], st)
-        e1.record(st)
-        if recording[0]:
-            attn_events.append((r, e0, e1))
-
-    recording = [False]
-    pipe.view = timed_view
 
     def step(events=None):
         return pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"], events=events)
@@ -300,7 +287,7 @@ def run_ours(args, wl, mode, rank, world):
     dsa.dsa_poll_device_error()
 
     def timed_steps(n, record_attention):
-        recording[0] = record_attention
+        pipe.attention_events = attn_events if record_attention else None
         evs = []
         for _ in range(n):
             flush.zero_()  # evict L2 between steps (outside the timed events)
@@ -308,7 +295,7 @@ def run_ours(args, wl, mode, rank, world):
             step(ev)
             evs.append(ev)
         torch.cuda.synchronize()
-        recording[0] = False
+        pipe.attention_events = None
         return ([ev["start"].elapsed_time(ev["end"]) for ev in evs],
                 [ev["core_start"].elapsed_time(ev["core_end"]) for ev in evs])
 
@@ -356,7 +343,7 @@ def run_ours(args, wl, mode, rank, world):
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = out_hosts[0].numel() * out_hosts[0].element_size()
     streamed = HostStreamedPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
-                                   dev, depth=2, view_streams=args.view_streams)
+                                   dev, depth=2, view_streams=args.view_streams, fused=fused)
     for s in range(2):  # warm-up of both buffer sets
         streamed.submit(host, out_hosts[s % 2])
     torch.cuda.synchronize()
@@ -417,8 +404,14 @@ def run_ours(args, wl, mode, rank, world):
     split_bytes = (T + pad) * (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4)
     out_bytes = 2 * T * wl.H * wl.Dv * 2
     aux = {}
-    for name, fn, nbytes in (("a2_split", lambda: pipe.split(x["q"], x["q_idx"], x["w"]), split_bytes),
-                             ("a6_rerange", pipe.rerange, out_bytes),
+
+    def split_all():  # a2 as its own pass, q included
+        for t, dst in ((x["q"], pipe.q_split), (x["q_idx"], pipe.qi_split), (x["w"], pipe.w_split)):
+            dsa.dsa_cp_split(t, wl.cp_size, mode, -1, dst)
+
+    for name, fn, nbytes in (("a2_split", split_all, split_bytes),
+                             ("a6_rerange", lambda: dsa.dsa_cp_rerange(pipe.out_split, wl.num_tokens, wl.cp_size, mode,
+                                                                       pipe.out), out_bytes),
                              ("a2a_heads", pipe.all_to_all_heads, out_bytes)):
         ms = timed(fn)
         aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
@@ -440,10 +433,20 @@ def run_ours(args, wl, mode, rank, world):
         pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
 
     aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
+
+    def unfused_step():  # the whole step with the split of q and the rerange as passes of their own
+        pipe.fused = False
+        try:
+            step()
+        finally:
+            pipe.fused = fused
+
+    aux["step_unfused_ms"] = timed(unfused_step, reps=3)
     aux["note"] = ("a2a_heads: all views' [tpr][H][Dv] outputs -> [cp][T][H/cp][Dv] head-sharded; "
                    "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
                    "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
-                   "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views)")
+                   "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
+                   "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own")
     dsa.dsa_poll_device_error()
 
     launches = pipe.launches_per_step() * args.steps
@@ -457,7 +460,7 @@ def run_ours(args, wl, mode, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_rank / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 inputs, shapes of the workload)",
-        "config": dict(config_of(wl, mode), view_streams=args.view_streams),
+        "config": dict(config_of(wl, mode), view_streams=args.view_streams, fused_split_rerange=fused),
         "roofline": {"bound": "tensor", "kernel": "sparse_attn_kernel", "achieved": achieved,
                      "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
                      "peak_source": f"{pk['source']} bf16 sustained", "traffic": profiled_traffic(),

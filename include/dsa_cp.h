@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define DSA_CP_ABI_VERSION 3
+#define DSA_CP_ABI_VERSION 4
 
 typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 
@@ -317,6 +317,23 @@ dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_metadata *md, 
                                                const int32_t *topk_idx, int32_t topk, const float *attn_sink,
                                                float softmax_scale, int32_t H, int32_t D, int32_t Dv,
                                                int32_t cp_size, void *out, dsa_stream_t stream);
+
+/*
+ * dsa_sparse_attn_prefill on the flat token layout: q bf16 [num_tokens][H][D]
+ * and out bf16 [num_tokens][H][Dv] hold every token of the batch in flat
+ * order, and a view reads its local queries and writes its output rows at
+ * local_token_pos[i].  Same arithmetic and results as the split of q
+ * ([blog] "2.B"), dsa_sparse_attn_prefill and the rerange of the outputs
+ * ([blog] "第三部分" step B) in sequence, without the two copies; every view
+ * of a batch writes into the same out, their rows do not overlap, and pad
+ * slots write nothing.  num_tokens = T of the metadata (a local_token_pos
+ * at or beyond it is a DSA_ERR_DEVICE_BOUNDS).
+ */
+dsa_status dsa_sparse_attn_prefill_flat(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                        const void *q, int32_t num_tokens, const void *kv, int32_t num_kv_rows,
+                                        const int32_t *topk_idx, int32_t topk, const float *attn_sink,
+                                        float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
+                                        dsa_stream_t stream);
 
 /*
  * FP8 latent-KV cache ([blog] "1 核心改动总结": round-robin-split lifts the

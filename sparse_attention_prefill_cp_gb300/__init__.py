@@ -295,6 +295,31 @@ def dsa_sparse_attn_prefill_headsharded(md: CPLocalMetadata, q: torch.Tensor, kv
     return out
 
 
+def dsa_sparse_attn_prefill_flat(md: CPLocalMetadata, q: torch.Tensor, kv: torch.Tensor, topk_idx: torch.Tensor,
+                                 softmax_scale: float, Dv: int, out: torch.Tensor,
+                                 attn_sink: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One view's attention on the flat layout: q bf16 [T, H, D] (every token
+    of the batch), out bf16 [T, H, Dv] shared by the views of the batch; the
+    view's rows are reached through its local_token_pos."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv, torch.bfloat16, "kv")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(out, torch.bfloat16, "out")
+    if attn_sink is not None:
+        _need(attn_sink, torch.float32, "attn_sink")
+    T, H, D = q.shape
+    tpr = md.tokens_per_rank
+    if T != md.num_tokens or kv.shape[1] != D or tuple(topk_idx.shape[:1]) != (tpr,):
+        raise ValueError("q / kv / topk_idx shapes do not match the view")
+    if tuple(out.shape) != (T, H, Dv):
+        raise ValueError("out must be [T, H, Dv]")
+    check(load().dsa_sparse_attn_prefill_flat(C.byref(md.struct), md.batch, tpr, _ptr(q), T, _ptr(kv), kv.shape[0],
+                                              _ptr(topk_idx), topk_idx.shape[1], _ptr(attn_sink),
+                                              float(softmax_scale), H, D, Dv, _ptr(out), _stream(stream)),
+          "dsa_sparse_attn_prefill_flat")
+    return out
+
+
 def dsa_kv_fp8_row_bytes(D: int, Dv: int) -> int:
     """Bytes of one FP8 latent-KV cache row (include/dsa_cp.h)."""
     n = C.c_size_t()

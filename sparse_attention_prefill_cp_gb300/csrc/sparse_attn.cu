@@ -47,7 +47,10 @@
 // epilogue's stores, the head-sharded layout that the head/token all-to-all
 // after the attention produces (单层前向数据流 (6)): [cp][T][H / cp][Dv], rank
 // rd holding heads rd * H / cp .. of every real token (pad slots write
-// nothing).
+// nothing).  Flat layout: q [T][H][D] and out [T][H][Dv] in token order, the
+// view's rows reached through local_token_pos -- the split of q before the
+// attention and the rerange after it ([blog] 第三部分) done by the loads and
+// stores themselves.
 //
 // A query's selected rows are KV rows of its own request, whose position 0
 // is KV row local_req_kv_base; with chunked prefill the KV holds the prefix
@@ -121,10 +124,12 @@ struct AttnParams {
   const __nv_bfloat16 *kv;   // [T][D]
   const int32_t *topk_idx;   // [tpr][topk]
   const float *sink;         // [H] or nullptr
-  __nv_bfloat16 *out;        // [tpr][H][Dv], or [cp][T][hc][Dv] when hc > 0
+  __nv_bfloat16 *out;        // [tpr][H][Dv], [cp][T][hc][Dv] when hc > 0, [T][H][Dv] when flat
   float scale_log2;          // softmax_scale * log2(e)
   int32_t topk, H, D, Dv, num_kv_rows;
   int32_t hc;                // heads per rank of the head-sharded output, 0 = view layout
+  int32_t flat;              // 1: q and out in flat token order (rows by local_token_pos)
+  int32_t q_rows;            // rows of q: tpr, or T when flat
   int *err;
 };
 
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int j = find_local_request(P.md.local_query_start_loc, nbatch, slot);
       base = P.md.local_req_kv_base[j];
       p = g - P.md.local_req_pos_base[j];
-      if (p < 0 || base < 0 || base + p >= P.num_kv_rows) {
+      if (p < 0 || base < 0 || base + p >= P.num_kv_rows || (P.flat && g >= P.q_rows)) {
         record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 44, slot);
         p = -1;
       }
@@ -224,11 +229,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int p = misc[2];
   const int n_valid = p >= 0 ? min(p + 1, P.topk) : 0;
   const int nb = (n_valid + C::kBN - 1) / C::kBN;
-  __nv_bfloat16 *out_row = P.out + (static_cast<int64_t>(slot) * P.H) * P.Dv + main_dim0;
+  const int qrow = P.flat ? misc[3] : slot;  // the view's row of q and of the output
+  __nv_bfloat16 *out_row = P.out + (static_cast<int64_t>(qrow) * P.H) * P.Dv + main_dim0;
 
   if (nb == 0) {
     // pad slot: zero output rows (the head-sharded layout has none)
-    if (P.hc == 0 && warp < 4 && tid < P.H) {
+    if (P.hc == 0 && !P.flat && warp < 4 && tid < P.H) {
       __nv_bfloat16 *o = out_row + static_cast<int64_t>(tid) * P.Dv;
       for (int c = 0; c < C::DVC; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
     }
@@ -238,8 +244,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tma_prefetch_desc(&qmain_map);
       mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail);
       for (int i = 0; i < C::NMAIN; ++i)
-        tma_load_3d(smem + C::kOffQStage + i * 16384, &qmain_map, main_dim0 + 64 * i, 0, slot, q_full);
-      if (C::TAIL) tma_load_3d(smem + C::kOffQTail, &qtail_map, tail_dim0, 0, slot, q_full);
+        tma_load_3d(smem + C::kOffQStage + i * 16384, &qmain_map, main_dim0 + 64 * i, 0, qrow, q_full);
+      if (C::TAIL) tma_load_3d(smem + C::kOffQTail, &qtail_map, tail_dim0, 0, qrow, q_full);
       // ---------------- MMA issuer: QK runs two blocks ahead of PV
       const uint32_t st_addr = smem_u32(smem + C::kOffStage);
       const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
@@ -656,7 +662,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 template <class C>
 dsa_status launch_attn(const void *q, int32_t tpr, const AttnParams &P, cudaStream_t stream) {
   CUtensorMap qmain, qtail;
-  uint64_t dims[3] = {static_cast<uint64_t>(P.D), static_cast<uint64_t>(P.H), static_cast<uint64_t>(tpr)};
+  uint64_t dims[3] = {static_cast<uint64_t>(P.D), static_cast<uint64_t>(P.H), static_cast<uint64_t>(P.q_rows)};
   uint64_t strides[2] = {static_cast<uint64_t>(P.D) * 2, static_cast<uint64_t>(P.H) * P.D * 2};
   uint32_t box_main[3] = {64, 128, 1};
   dsa_status st = encode_tensor_map(&qmain, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box_main,
@@ -698,7 +704,7 @@ using namespace dsa;
 static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr, const void *q,
                                    const void *kv, int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
                                    const float *attn_sink, float softmax_scale, int32_t H, int32_t D, int32_t Dv,
-                                   int32_t cp_size, void *out, dsa_stream_t stream) {
+                                   int32_t cp_size, void *out, int32_t flat_tokens, dsa_stream_t stream) {
   if (!md || !q || !kv || !topk_idx || !out) return DSA_ERR_INVALID_ARG;
   if (!md->scalars || !md->local_query_start_loc || !md->local_req_kv_base || !md->local_token_pos ||
       !md->local_req_pos_base)
@@ -708,6 +714,7 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return DSA_ERR_INVALID_ARG;
   if (cp_size < 0) return DSA_ERR_INVALID_ARG;
   if (cp_size > 0 && (H < 1 || H % cp_size != 0)) return DSA_ERR_SHAPE;
+  if (flat_tokens < 0) return DSA_ERR_SHAPE;
   if (tpr == 0) return DSA_OK;
   if (static_cast<int64_t>(tpr) * 2 > INT32_MAX) return DSA_ERR_SHAPE;
   const bool big = H == 128 && D == 576 && Dv == 512 && topk == 2048;
@@ -727,6 +734,8 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
                Dv,
                num_kv_rows,
                cp_size > 0 ? H / cp_size : 0,
+               flat_tokens > 0 ? 1 : 0,
+               flat_tokens > 0 ? flat_tokens : tpr,
                err};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return big ? launch_attn<BigAttn>(q, tpr, P, s) : launch_attn<TinyAttn>(q, tpr, P, s);
@@ -738,7 +747,17 @@ extern "C" dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, i
                                               float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
                                               dsa_stream_t stream) {
   return sparse_attn_impl(md, batch, tpr, q, kv, num_kv_rows, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv, 0,
-                          out, stream);
+                          out, 0, stream);
+}
+
+extern "C" dsa_status dsa_sparse_attn_prefill_flat(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                                   const void *q, int32_t num_tokens, const void *kv,
+                                                   int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
+                                                   const float *attn_sink, float softmax_scale, int32_t H, int32_t D,
+                                                   int32_t Dv, void *out, dsa_stream_t stream) {
+  if (num_tokens < 1) return num_tokens == 0 ? DSA_OK : DSA_ERR_SHAPE;
+  return sparse_attn_impl(md, batch, tpr, q, kv, num_kv_rows, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv, 0,
+                          out, num_tokens, stream);
 }
 
 extern "C" dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_metadata *md, int32_t batch,
@@ -749,5 +768,5 @@ extern "C" dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_met
                                                           dsa_stream_t stream) {
   if (cp_size < 1) return DSA_ERR_INVALID_ARG;
   return sparse_attn_impl(md, batch, tpr, q, kv, num_kv_rows, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv,
-                          cp_size, out, stream);
+                          cp_size, out, 0, stream);
 }

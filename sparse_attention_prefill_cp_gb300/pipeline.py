@@ -22,19 +22,24 @@ import torch
 
 from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_metadata, dsa_cp_geometry,
                dsa_cp_rerange, dsa_cp_split, dsa_indexer_topk, dsa_indexer_topk_workspace_size,
-               dsa_kv_fp8_dequantize, dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_headsharded)
+               dsa_kv_fp8_dequantize, dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_flat,
+               dsa_sparse_attn_prefill_headsharded)
 
 
 class DSAPrefill:
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
                  softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1,
-                 prefix_lens=None, kv_fp8: bool = False):
+                 prefix_lens=None, kv_fp8: bool = False, fused: bool = False):
         """``lengths``: query tokens per request.  ``prefix_lens`` (chunked
         prefill): KV positions per request that precede its queries; the KV
         and index-key tensors passed to ``run`` then hold every request's
         whole sequence (prefix + queries), requests in order.  ``kv_fp8``:
         the latent KV passed to ``run`` is the FP8 cache (uint8 rows of
-        dsa_kv_fp8_row_bytes), dequantised once per batch before the views."""
+        dsa_kv_fp8_row_bytes), dequantised once per batch before the views.
+        ``fused``: ``run`` skips the split of q and the rerange of the
+        outputs; each view's attention reads its queries from the full q and
+        writes its rows of ``out`` in place (dsa_sparse_attn_prefill_flat),
+        with the same results."""
         self.device = torch.device(device or "cuda")
         self.lengths = [int(x) for x in lengths]
         self.prefix_lens = [0] * len(self.lengths) if prefix_lens is None else [int(x) for x in prefix_lens]
@@ -57,11 +62,12 @@ class DSAPrefill:
         self.seq_lens = torch.tensor(self.kv_lens, dtype=torch.int32, device=dev)
         self.md = [CPLocalMetadata(self.B, self.T, cp_size, dev) for _ in range(cp_size)]
         cp, tpr = cp_size, self.tpr
-        self.q_split = torch.empty((cp, tpr, H, D), dtype=torch.bfloat16, device=dev)
+        self.fused = bool(fused)
+        self._q_split = None    # [cp][tpr][H][D] and [cp][tpr][H][Dv], allocated on
+        self._out_split = None  # first use (never by the fused path)
         self.qi_split = torch.empty((cp, tpr, HI, DI), dtype=torch.bfloat16, device=dev)
         self.w_split = torch.empty((cp, tpr, HI), dtype=torch.float32, device=dev)
         self.topk_idx = torch.empty((cp, tpr, topk), dtype=torch.int32, device=dev)
-        self.out_split = torch.empty((cp, tpr, H, Dv), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((self.T, H, Dv), dtype=torch.bfloat16, device=dev)
         ws = workspace_bytes or dsa_indexer_topk_workspace_size(tpr, self.max_kv_len, topk)
         # views on several streams: one score workspace per stream, so that the
@@ -74,16 +80,33 @@ class DSAPrefill:
         self.kv_fp8 = bool(kv_fp8)
         self.kv_rows = (torch.empty((self.num_kv_rows, D), dtype=torch.bfloat16, device=dev) if self.kv_fp8
                         else None)
+        self.attention_events = None  # a list: (view, start, end) CUDA events of every attention launch
+        self._q = None
+
+    @property
+    def q_split(self):
+        if self._q_split is None:
+            self._q_split = torch.empty((self.cp_size, self.tpr, self.H, self.D), dtype=torch.bfloat16,
+                                        device=self.device)
+        return self._q_split
+
+    @property
+    def out_split(self):
+        if self._out_split is None:
+            self._out_split = torch.empty((self.cp_size, self.tpr, self.H, self.Dv), dtype=torch.bfloat16,
+                                          device=self.device)
+        return self._out_split
 
     def launches_per_step(self) -> int:
-        """Kernel launches of one ``run``: metadata per view, 3 splits, the FP8
-        dequantisation (if any), per view (indexer + top-k) per workspace chunk
-        and one attention, 1 rerange."""
+        """Kernel launches of one ``run``: metadata per view, 3 splits (2
+        fused), the FP8 dequantisation (if any), per view (indexer + top-k) per
+        workspace chunk and one attention, 1 rerange (0 fused)."""
         ld = (self.max_kv_len + 3) // 4 * 4
         tile = 8 if self.HI == 64 else 128
         rows_fit = (self.workspace.numel() // (ld * 4)) // tile * tile
         chunks = -(-self.tpr // rows_fit)
-        return self.cp_size + 3 + int(self.kv_fp8) + self.cp_size * (2 * chunks + 1) + 1
+        splits, reranges = (2, 0) if self.fused else (3, 1)
+        return self.cp_size + splits + int(self.kv_fp8) + self.cp_size * (2 * chunks + 1) + reranges
 
     def metadata(self, stream=None):                                     # a1
         for r in range(self.cp_size):
@@ -91,15 +114,28 @@ class DSAPrefill:
                                         self.md[r], stream)
 
     def split(self, q, q_idx, w, stream=None):                          # a2
-        dsa_cp_split(q, self.cp_size, self.mode, -1, self.q_split, stream)
+        if not self.fused:  # the fused attention reads q in place
+            dsa_cp_split(q, self.cp_size, self.mode, -1, self.q_split, stream)
         dsa_cp_split(q_idx, self.cp_size, self.mode, -1, self.qi_split, stream)
         dsa_cp_split(w, self.cp_size, self.mode, -1, self.w_split, stream)
 
     def view(self, r: int, kv, k_idx, sink=None, stream=None, workspace=None):  # a3 + a4 + a5
         dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
                          self.topk_idx[r], self.workspace if workspace is None else workspace, stream)
-        dsa_sparse_attn_prefill(self.md[r], self.q_split[r], kv, self.topk_idx[r], self.scale, self.Dv, sink,
-                                self.out_split[r], stream)
+        st = stream or torch.cuda.current_stream(self.device)
+        ev = self.attention_events
+        if ev is not None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)  # on the stream the attention is launched on
+        if self.fused:
+            dsa_sparse_attn_prefill_flat(self.md[r], self._q, kv, self.topk_idx[r], self.scale, self.Dv, self.out,
+                                         sink, st)
+        else:
+            dsa_sparse_attn_prefill(self.md[r], self.q_split[r], kv, self.topk_idx[r], self.scale, self.Dv, sink,
+                                    self.out_split[r], st)
+        if ev is not None:
+            e1.record(st)
+            ev.append((r, e0, e1))
 
     def latent_kv(self, kv, stream=None):
         """The bf16 latent rows the attention reads: ``kv`` itself, or the
@@ -136,6 +172,8 @@ class DSAPrefill:
             stream.wait_event(join)
 
     def rerange(self, stream=None):                                     # a6
+        if self.fused:  # the fused attention wrote out in place
+            return self.out
         return dsa_cp_rerange(self.out_split, self.T, self.cp_size, self.mode, self.out, stream)
 
     def run(self, q, kv, q_idx, k_idx, w, sink=None, stream=None, events=None):
@@ -150,6 +188,7 @@ class DSAPrefill:
         self.split(q, q_idx, w, stream)
         if "core_start" in ev:
             ev["core_start"].record(s)
+        self._q = q
         kv = self.latent_kv(kv, s)
         self.views(kv, k_idx, sink, s)
         if "core_end" in ev:
@@ -168,7 +207,7 @@ class DSAPrefill:
         return self.out_hs
 
     def all_to_all_heads(self, stream=None):
-        """The per-view outputs of the last ``run`` -> head-sharded [cp, T, H / cp, Dv]."""
+        """The per-view outputs of the last ``run`` (not fused) -> head-sharded [cp, T, H / cp, Dv]."""
         return dsa_cp_all_to_all_heads(self.out_split, self.T, self.cp_size, self.mode, self._head_sharded_buffer(),
                                        stream)
 
@@ -178,6 +217,8 @@ class DSAPrefill:
         out = self._head_sharded_buffer()
         self.metadata(stream)
         self.split(q, q_idx, w, stream)
+        if self.fused:  # the head-sharded attention reads the split q
+            dsa_cp_split(q, self.cp_size, self.mode, -1, self.q_split, stream)
         kv = self.latent_kv(kv, stream)
         for r in range(self.cp_size):
             dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
@@ -203,11 +244,13 @@ class HostStreamedPrefill:
     INPUTS = ("q", "kv", "q_idx", "k_idx", "w", "sink")
 
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
-                 softmax_scale: float, device=None, depth: int = 2, view_streams: int = 1, prefix_lens=None):
+                 softmax_scale: float, device=None, depth: int = 2, view_streams: int = 1, prefix_lens=None,
+                 fused: bool = False):
         if depth < 1:
             raise ValueError("depth must be at least 1")
         self.pipes = [DSAPrefill(lengths, cp_size, mode, H, D, Dv, HI, DI, topk, softmax_scale, device,
-                                 view_streams=view_streams, prefix_lens=prefix_lens) for _ in range(depth)]
+                                 view_streams=view_streams, prefix_lens=prefix_lens, fused=fused)
+                      for _ in range(depth)]
         self.device = self.pipes[0].device
         self.depth = depth
         self.dev_in = [None] * depth

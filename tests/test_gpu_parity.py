@@ -455,6 +455,32 @@ def test_chunked_prefill(wl, prefixes, mode):
     dsa.dsa_poll_device_error()
 
 
+# ------------------------------------------------------------------ fused split / rerange (flat layout)
+
+@pytest.mark.parametrize("wl,mode,prefixes", [(TINY, IN_SEQ_SPLIT, None), (TINY, ROUND_ROBIN, None),
+                                              (TINY, HEAD_TAIL, None), (FLOAT_FULL, ROUND_ROBIN, None),
+                                              (FLOAT_FULL, HEAD_TAIL, (1800, 300)), (LONG_8K, IN_SEQ_SPLIT, None),
+                                              (VARLEN_4, ROUND_ROBIN, None)],
+                         ids=lambda v: v.name if isinstance(v, Workload) else str(v))
+def test_fused_flat_path_is_bit_identical(wl, mode, prefixes):
+    # the attention reading q in place and writing out in place gives the
+    # split -> attention -> rerange output bit for bit, on one and two streams
+    x = draw_inputs(wl, device="cuda")
+    lengths = wl.lengths
+    if prefixes is not None:
+        x, lengths, _ = chunk_inputs(x, wl.lengths, prefixes)
+    args = (lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale)
+    ref = DSAPrefill(*args, prefix_lens=prefixes).run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"],
+                                                       x["sink"]).clone()
+    for streams in (1, 2):
+        pipe = DSAPrefill(*args, prefix_lens=prefixes, fused=True, view_streams=streams)
+        pipe.out.fill_(float("nan"))  # every row must be written
+        out = pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
+        dsa.dsa_poll_device_error()
+        assert pipe._q_split is None and pipe._out_split is None
+        assert torch.equal(out, ref), streams
+
+
 # ------------------------------------------------------------------ FP8 latent-KV cache
 
 @pytest.mark.parametrize("D,Dv,R", [(64, 48, 257), (576, 512, 8192)])
