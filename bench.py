@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--mode", choices=["in-seq", "round-robin", "head-tail"], default=None)
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--core-only", action="store_true",
+                    help="skip the e2e and aux legs (workload sweeps; the default run keeps them)")
     ap.add_argument("--unfused", action="store_true",
                     help="split q and rerange the outputs as separate passes instead of in the attention")
     ap.add_argument("--view-streams", type=int, default=2,
@@ -333,121 +335,124 @@ def run_ours(args, wl, mode, rank, world):
     pk = peaks()
     achieved = (sum(attn_flops) / (sum(attn_ms) / 1e3)) / 1e12
 
-    # end to end: pinned host inputs in, output out, through the same public
-    # calls.  Streamed: batches go through HostStreamedPrefill, whose copies of
-    # batch s+1's inputs (H2D) and batch s-1's output (D2H) overlap the compute
-    # of batch s; every batch's copies are inside the timed region.  Serial:
-    # one batch at a time, copy in, compute, copy out, on one stream.
-    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
-    out_hosts = [torch.empty((wl.num_tokens, wl.H, wl.Dv), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-    d2h = out_hosts[0].numel() * out_hosts[0].element_size()
-    streamed = HostStreamedPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
-                                   dev, depth=2, view_streams=args.view_streams, fused=fused)
-    for s in range(2):  # warm-up of both buffer sets
-        streamed.submit(host, out_hosts[s % 2])
-    torch.cuda.synchronize()
-    n_e2e = max(2, args.e2e_steps)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e0.record(streamed.h2d)
-    for s in range(n_e2e):
-        last = streamed.submit(host, out_hosts[s % 2])
-    e1 = streamed.done_event(last)
-    torch.cuda.synchronize()
-    e2e_stream_ms = e0.elapsed_time(e1) / n_e2e
-    dsa.dsa_poll_device_error()
-    dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in host.items()}
-    e2e_serial = []
-    for s in range(3):
+    e2e_stream_ms = e2e_serial = h2d = d2h = n_e2e = None
+    aux = None
+    if not args.core_only:  # the e2e and aux legs (need about 4x the workload's memory)
+        # end to end: pinned host inputs in, output out, through the same public
+        # calls.  Streamed: batches go through HostStreamedPrefill, whose copies of
+        # batch s+1's inputs (H2D) and batch s-1's output (D2H) overlap the compute
+        # of batch s; every batch's copies are inside the timed region.  Serial:
+        # one batch at a time, copy in, compute, copy out, on one stream.
+        host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
+        out_hosts = [torch.empty((wl.num_tokens, wl.H, wl.Dv), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = out_hosts[0].numel() * out_hosts[0].element_size()
+        streamed = HostStreamedPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                                       dev, depth=2, view_streams=args.view_streams, fused=fused)
+        for s in range(2):  # warm-up of both buffer sets
+            streamed.submit(host, out_hosts[s % 2])
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for k, v in host.items():
-            if v is not None:
-                dev_in[k].copy_(v, non_blocking=True)
-        out = pipe.run(dev_in["q"], dev_in["kv"], dev_in["q_idx"], dev_in["k_idx"], dev_in["w"], dev_in["sink"])
-        out_hosts[0].copy_(out, non_blocking=True)
-        b.record()
+        n_e2e = max(2, args.e2e_steps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(streamed.h2d)
+        for s in range(n_e2e):
+            last = streamed.submit(host, out_hosts[s % 2])
+        e1 = streamed.done_event(last)
         torch.cuda.synchronize()
-        if s > 0:
-            e2e_serial.append(a.elapsed_time(b))
-    del streamed, dev_in
-    dsa.dsa_poll_device_error()
-
-    # data-movement steps and the head-sharded output, each timed on its own
-    # (cold L2, outside the timed step): a2 split, a6 rerange, the head/token
-    # all-to-all as a separate pass, and a3-a5 with the all-to-all fused into
-    # the attention's stores
-    def timed(fn, reps=5):
-        fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
+        e2e_stream_ms = e0.elapsed_time(e1) / n_e2e
+        dsa.dsa_poll_device_error()
+        dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in host.items()}
+        e2e_serial = []
+        for s in range(3):
+            torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            fn()
+            for k, v in host.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            out = pipe.run(dev_in["q"], dev_in["kv"], dev_in["q_idx"], dev_in["k_idx"], dev_in["w"], dev_in["sink"])
+            out_hosts[0].copy_(out, non_blocking=True)
             b.record()
             torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+            if s > 0:
+                e2e_serial.append(a.elapsed_time(b))
+        del streamed, dev_in
+        dsa.dsa_poll_device_error()
 
-    def fused_core():
-        hs = pipe._head_sharded_buffer()
-        for r in range(wl.cp_size):
-            dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], x["k_idx"], pipe.w_split[r], pipe.topk,
-                                 pipe.max_kv_len, pipe.topk_idx[r], pipe.workspace)
-            dsa.dsa_sparse_attn_prefill_headsharded(pipe.md[r], pipe.q_split[r], x["kv"], pipe.topk_idx[r],
-                                                    pipe.scale, pipe.Dv, wl.cp_size, hs, x["sink"])
+        # data-movement steps and the head-sharded output, each timed on its own
+        # (cold L2, outside the timed step): a2 split, a6 rerange, the head/token
+        # all-to-all as a separate pass, and a3-a5 with the all-to-all fused into
+        # the attention's stores
+        def timed(fn, reps=5):
+            fn()
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            return statistics.median(ts)
 
-    pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
-    T, pad = wl.num_tokens, pipe.pad
-    split_bytes = (T + pad) * (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4)
-    out_bytes = 2 * T * wl.H * wl.Dv * 2
-    aux = {}
+        def fused_core():
+            hs = pipe._head_sharded_buffer()
+            for r in range(wl.cp_size):
+                dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], x["k_idx"], pipe.w_split[r], pipe.topk,
+                                     pipe.max_kv_len, pipe.topk_idx[r], pipe.workspace)
+                dsa.dsa_sparse_attn_prefill_headsharded(pipe.md[r], pipe.q_split[r], x["kv"], pipe.topk_idx[r],
+                                                        pipe.scale, pipe.Dv, wl.cp_size, hs, x["sink"])
 
-    def split_all():  # a2 as its own pass, q included
-        for t, dst in ((x["q"], pipe.q_split), (x["q_idx"], pipe.qi_split), (x["w"], pipe.w_split)):
-            dsa.dsa_cp_split(t, wl.cp_size, mode, -1, dst)
+        pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
+        T, pad = wl.num_tokens, pipe.pad
+        split_bytes = (T + pad) * (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4)
+        out_bytes = 2 * T * wl.H * wl.Dv * 2
+        aux = {}
 
-    for name, fn, nbytes in (("a2_split", split_all, split_bytes),
-                             ("a6_rerange", lambda: dsa.dsa_cp_rerange(pipe.out_split, wl.num_tokens, wl.cp_size, mode,
-                                                                       pipe.out), out_bytes),
-                             ("a2a_heads", pipe.all_to_all_heads, out_bytes)):
-        ms = timed(fn)
-        aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
-                     "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
-    aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
-    # FP8 latent-KV cache: quantise / dequantise as HBM passes (bytes read +
-    # written), and the a3-a5 core over the cache (dequantisation + views)
-    cache = dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv)
-    kv_rows = torch.empty_like(x["kv"])
-    fp8_bytes = x["kv"].shape[0] * (wl.D * 2 + cache.shape[1])
-    for name, fn in (("kv_fp8_quantize", lambda: dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv, cache)),
-                     ("kv_fp8_dequantize", lambda: dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows))):
-        ms = timed(fn)
-        aux[name] = {"ms": ms, "bytes": fp8_bytes, "gbs": fp8_bytes / (ms / 1e3) / 1e9,
-                     "frac_hbm": fp8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+        def split_all():  # a2 as its own pass, q included
+            for t, dst in ((x["q"], pipe.q_split), (x["q_idx"], pipe.qi_split), (x["w"], pipe.w_split)):
+                dsa.dsa_cp_split(t, wl.cp_size, mode, -1, dst)
 
-    def fp8_core():
-        rows = dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows)
-        pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
+        for name, fn, nbytes in (("a2_split", split_all, split_bytes),
+                                 ("a6_rerange", lambda: dsa.dsa_cp_rerange(pipe.out_split, wl.num_tokens, wl.cp_size, mode,
+                                                                           pipe.out), out_bytes),
+                                 ("a2a_heads", pipe.all_to_all_heads, out_bytes)):
+            ms = timed(fn)
+            aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+                         "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+        aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
+        # FP8 latent-KV cache: quantise / dequantise as HBM passes (bytes read +
+        # written), and the a3-a5 core over the cache (dequantisation + views)
+        cache = dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv)
+        kv_rows = torch.empty_like(x["kv"])
+        fp8_bytes = x["kv"].shape[0] * (wl.D * 2 + cache.shape[1])
+        for name, fn in (("kv_fp8_quantize", lambda: dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv, cache)),
+                         ("kv_fp8_dequantize", lambda: dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows))):
+            ms = timed(fn)
+            aux[name] = {"ms": ms, "bytes": fp8_bytes, "gbs": fp8_bytes / (ms / 1e3) / 1e9,
+                         "frac_hbm": fp8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
 
-    aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
+        def fp8_core():
+            rows = dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows)
+            pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
 
-    def unfused_step():  # the whole step with the split of q and the rerange as passes of their own
-        pipe.fused = False
-        try:
-            step()
-        finally:
-            pipe.fused = fused
+        aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
 
-    aux["step_unfused_ms"] = timed(unfused_step, reps=3)
-    aux["note"] = ("a2a_heads: all views' [tpr][H][Dv] outputs -> [cp][T][H/cp][Dv] head-sharded; "
-                   "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
-                   "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
-                   "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
-                   "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own")
-    dsa.dsa_poll_device_error()
+        def unfused_step():  # the whole step with the split of q and the rerange as passes of their own
+            pipe.fused = False
+            try:
+                step()
+            finally:
+                pipe.fused = fused
+
+        aux["step_unfused_ms"] = timed(unfused_step, reps=3)
+        aux["note"] = ("a2a_heads: all views' [tpr][H][Dv] outputs -> [cp][T][H/cp][Dv] head-sharded; "
+                       "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
+                       "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
+                       "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
+                       "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own")
+        dsa.dsa_poll_device_error()
 
     launches = pipe.launches_per_step() * args.steps
     if rank != 0:
@@ -473,12 +478,13 @@ def run_ours(args, wl, mode, rank, world):
                  "roofline_ms": roof_s * 1e3, "flops": f_idx + f_att,
                  "view_streams": pipe.view_streams,
                  "ms_per_step_one_stream": (statistics.mean(core_ms_one_stream) if core_ms_one_stream else None)},
-        "e2e": {"value": wl.num_tokens / (e2e_stream_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_stream_ms, "batches": n_e2e,
-                "how": "pinned host inputs -> device -> output back to pinned host, every batch; copies of the "
-                       "neighbouring batches overlap each batch's compute (HostStreamedPrefill, 2 buffer sets)",
-                "serial_ms_per_step": statistics.mean(e2e_serial),
-                "serial_value": wl.num_tokens / (statistics.mean(e2e_serial) / 1e3)},
+        "e2e": None if args.core_only else {
+            "value": wl.num_tokens / (e2e_stream_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_stream_ms, "batches": n_e2e,
+            "how": "pinned host inputs -> device -> output back to pinned host, every batch; copies of the "
+                   "neighbouring batches overlap each batch's compute (HostStreamedPrefill, 2 buffer sets)",
+            "serial_ms_per_step": statistics.mean(e2e_serial),
+            "serial_value": wl.num_tokens / (statistics.mean(e2e_serial) / 1e3)},
         "clocks": clocks,
         "gpu_launches": launches,
         "aux": aux,
