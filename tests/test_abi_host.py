@@ -105,3 +105,33 @@ def test_host_validation_rejects_before_any_launch(lib):
                                                    576, 512, 3, p, None) == 2
     assert lib.dsa_sparse_attn_prefill_headsharded(C.byref(md), 1, 8, p, p, 16, p, 2048, None, C.c_float(0.07), 64,
                                                    576, 512, 2, p, None) == 3
+
+
+def test_flat_attention_and_fp8_cache_validation(lib):
+    md = _lib.LocalMetadata()
+    assert lib.dsa_cp_metadata_bind(C.c_void_p(0x10000), 1, 16, 2, C.byref(md)) == 0
+    p, odd = C.c_void_p(0x10000), C.c_void_p(0x10008)
+    f = C.c_float(0.07)
+    # flat-layout attention: misaligned q, negative token count, nothing to do, uncompiled dims
+    assert lib.dsa_sparse_attn_prefill_flat(C.byref(md), 1, 8, odd, 16, p, 16, p, 2048, None, f, 128, 576, 512, p,
+                                            None) == 1
+    assert lib.dsa_sparse_attn_prefill_flat(C.byref(md), 1, 8, p, -1, p, 16, p, 2048, None, f, 128, 576, 512, p,
+                                            None) == 2
+    assert lib.dsa_sparse_attn_prefill_flat(C.byref(md), 1, 8, p, 0, p, 16, p, 2048, None, f, 128, 576, 512, p,
+                                            None) == 0
+    assert lib.dsa_sparse_attn_prefill_flat(C.byref(md), 1, 8, p, 16, p, 16, p, 2048, None, f, 96, 576, 512, p,
+                                            None) == 3
+    # FP8 cache: row sizes, null / misaligned buffers, shapes, nothing to do
+    n = C.c_size_t()
+    assert lib.dsa_kv_fp8_row_bytes(576, 512, C.byref(n)) == 0 and n.value == 656
+    assert lib.dsa_kv_fp8_row_bytes(64, 48, C.byref(n)) == 0 and n.value == 96 == O.kv_fp8_row_bytes(64, 48)
+    assert lib.dsa_kv_fp8_row_bytes(576, 500, C.byref(n)) == 2
+    assert lib.dsa_kv_fp8_row_bytes(512, 576, C.byref(n)) == 2
+    assert lib.dsa_kv_fp8_row_bytes(576, 512, None) == 1
+    assert lib.dsa_kv_fp8_quantize(None, 4, 576, 512, p, None) == 1
+    assert lib.dsa_kv_fp8_quantize(odd, 4, 576, 512, p, None) == 1
+    assert lib.dsa_kv_fp8_quantize(p, -1, 576, 512, p, None) == 2
+    assert lib.dsa_kv_fp8_quantize(p, 4, 576, 12, p, None) == 2
+    assert lib.dsa_kv_fp8_quantize(p, 0, 576, 512, p, None) == 0
+    assert lib.dsa_kv_fp8_dequantize(p, 4, 576, 512, None, None) == 1
+    assert lib.dsa_kv_fp8_dequantize(p, 0, 64, 48, p, None) == 0
