@@ -422,6 +422,7 @@ def run_ours(args, wl, mode, rank, world):
             aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
                          "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
         aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
+        aux["a1_metadata_ms"] = timed(pipe.metadata)  # every view's build_cp_local_metadata
         # FP8 latent-KV cache: quantise / dequantise as HBM passes (bytes read +
         # written), and the a3-a5 core over the cache (dequantisation + views)
         cache = dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv)
@@ -451,7 +452,8 @@ def run_ours(args, wl, mode, rank, world):
                        "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
                        "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
                        "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
-                       "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own")
+                       "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own; "
+                       "a1_metadata_ms: every view's metadata (one launch per view)")
         dsa.dsa_poll_device_error()
 
     launches = pipe.launches_per_step() * args.steps
