@@ -66,6 +66,16 @@ design notes):
 
   R12 the FP8 latent-KV cache ([blog] 1, named only): the OCP E4M3 row layout
       of the FP8 section at the end of this file.
+  R13 compressed KV ([xLLM] 背景: compress_ratio in {1, 4, 128}; 5: the sparse
+      metadata is built per ratio with the local geometry).  At ratio c a
+      request of seq_len tokens has floor(seq_len / c) compressed entries
+      (latent rows and index keys, given as inputs: the compressor is out of
+      scope); entry e stands for positions [e*c, (e+1)*c).  A query at position
+      p sees the entries whose whole group lies at or before p, e <
+      floor((p + 1) / c); the indexer, top-k and attention run over those
+      entries.  Entries of all requests are stored in request order.  A query
+      that sees no entry selects nothing and its output is zero.  c = 1 is
+      the uncompressed path.
 
 parity pins: every function here is pinned by tests/test_oracle_pins.py
 against worked examples from the pages (tests/golden/), closed forms,
@@ -133,7 +143,8 @@ def local_rows(num_tokens: int, cp_size: int, cp_rank: int, mode: int) -> np.nda
 # build_cp_local_metadata
 # --------------------------------------------------------------------------
 
-def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, mode: int) -> dict:
+def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, mode: int,
+                         compress_ratio: int = 1) -> dict:
     """Local view metadata of one CP rank.
 
     [xLLM] 2: pad to a multiple of cp_size, tokens_per_rank, local_start /
@@ -152,7 +163,15 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
     qs_b minus the request's prefix) and local_token_pos (flat query row of
     every local slot, -1 for pad); num_tokens = T and num_kv_rows = the KV rows
     of the batch (the sum of seq_lens).
+
+    Compressed KV (R13) at ratio c: KV extents, KV bases and the KV row count
+    count compressed entries: local_seq_lens = floor(extent / c) of the token
+    extent above, request b's entries start at the sum of floor(seq_lens / c)
+    before it; query positions stay in tokens.
     """
+    c = int(compress_ratio)
+    if c < 1:
+        raise ValueError("compress_ratio must be at least 1")
     qsl = [int(x) for x in query_start_loc]
     sl = [int(x) for x in seq_lens]
     B = len(sl)
@@ -164,7 +183,7 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
         if q_len < 0 or sl[b] < q_len:
             raise ValueError("seq_lens[b] must be at least the query length of request b (R9)")
         prefix.append(sl[b] - q_len)
-        kv_start.append(kv_start[-1] + sl[b])
+        kv_start.append(kv_start[-1] + sl[b] // c)
     T = qsl[B]
     pad, tpr = padded_geometry(T, cp_size)
     rows = local_rows(T, cp_size, cp_rank, mode)
@@ -188,7 +207,7 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
         if not mine:
             continue  # R5
         q_lens.append(len(mine))
-        kv_lens.append(prefix[b] + max(mine) - qsl[b] + 1)  # R4: last local position + 1
+        kv_lens.append((prefix[b] + max(mine) - qsl[b] + 1) // c)  # R4: last local position + 1 (R13: entries)
         req_id.append(b)
         kv_base.append(kv_start[b])         # R9: KV row of position 0
         pos_base.append(qsl[b] - prefix[b])  # position of flat row g = g - pos_base
@@ -218,6 +237,7 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
         "local_req_pos_base": pos_base,
         "num_tokens": T,
         "num_kv_rows": kv_start[-1],
+        "compress_ratio": c,
     }
 
 
@@ -364,7 +384,9 @@ def view_row(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int,
     The local query of flat row g in request b, at in-request position
     p = g - local_req_pos_base (= g - qs_b without a prefix), sees the keys at
     positions 0 .. p of its own request, KV rows kv_base .. kv_base + p
-    (causal, same request; R8, R9).
+    (causal, same request; R8, R9).  At compress ratio c (R13) it sees the
+    entries 0 .. floor((p + 1) / c) - 1 instead; with none, nothing is selected
+    and the output is zero.
     """
     g = md["local_token_pos"][slot]
     H = np.asarray(q_loc[slot]).shape[0]
@@ -373,7 +395,10 @@ def view_row(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int,
     j = request_of_slot(md, slot)
     base = md["local_req_kv_base"][j]
     p = g - md["local_req_pos_base"][j]
-    keys = np.arange(base, base + p + 1)
+    n = (p + 1) // md.get("compress_ratio", 1)
+    if n == 0:
+        return np.zeros(0, dtype=np.int64), np.zeros(0), np.zeros((H, Dv))
+    keys = np.arange(base, base + n)
     scores = indexer_scores(q_idx_loc[slot], w_loc[slot], np.asarray(k_idx)[keys])
     sel = base + topk_positions(scores, topk)
     out = sparse_attention(q_loc[slot], np.asarray(kv)[sel], scale, Dv, sink)
@@ -398,7 +423,7 @@ def prefill_view(md: dict, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int, scale:
 
 
 def prefill(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mode: int, topk: int,
-            scale: float, Dv: int, sink=None):
+            scale: float, Dv: int, sink=None, compress_ratio: int = 1):
     """The whole prefill through cp_size views: split the local tensors, run
     every view with full KV and index keys, rerange the outputs to flat order
     ([xLLM] 单层前向数据流: q local, KV full).  q, q_idx, w hold the T query
@@ -413,7 +438,7 @@ def prefill(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mod
     _, tpr = padded_geometry(T, cp_size)
     outs = np.zeros((cp_size, tpr, q.shape[1], Dv))
     for r in range(cp_size):
-        md = build_local_metadata(query_start_loc, seq_lens, cp_size, r, mode)
+        md = build_local_metadata(query_start_loc, seq_lens, cp_size, r, mode, compress_ratio)
         _, outs[r] = prefill_view(md, qs[r], qis[r], ws[r], kv, k_idx, topk, scale, Dv, sink)
     return rerange(outs, T, cp_size, mode)
 

@@ -518,3 +518,88 @@ def test_kv_fp8_cache_layout_and_error_bound(D, Dv):
         bound = half_step + np.abs(d[:, cols]) * 2.0 ** -8 + 1e-30
         assert np.all(np.abs(d[:, cols] - x[:, cols]) <= bound)
     assert np.all(c[7, :Dv] == 0) and np.all(d[7] == 0)
+
+
+# ---------------------------------------------------------------- compressed KV (R13)
+
+_COMPRESSED_CASES = {"C": ([9, 6], [9, 6], 2, 4), "D": ([5, 3], [135, 3], 2, 128)}  # q_lens, seq_lens, cp, c
+
+
+def test_metadata_compressed_hand_cases():
+    seen = 0
+    for line in read_golden_lines("metadata_compressed_hand_cases.txt"):
+        head, lqs, kvl, lkv, rid, base, pbase, pos = line.split("|")
+        case, mode_s, rank = head.split()
+        q_lens, seq_lens, cp, c = _COMPRESSED_CASES[case]
+        mode = {"inseq": IN_SEQ_SPLIT, "rr": ROUND_ROBIN}[mode_s]
+        md = O.build_local_metadata(_qsl(q_lens), seq_lens, cp, int(rank), mode, compress_ratio=c)
+        assert md["local_query_start_loc"] == _ints(lqs), line
+        assert md["local_seq_lens"] == _ints(kvl), line
+        assert md["local_kv_start_loc"] == _ints(lkv), line
+        assert md["local_req_id"] == _ints(rid), line
+        assert md["local_req_kv_base"] == _ints(base), line
+        assert md["local_req_pos_base"] == _ints(pbase), line
+        assert md["local_token_pos"] == _ints(pos), line
+        assert md["num_kv_rows"] == sum(n // c for n in seq_lens) and md["compress_ratio"] == c
+        seen += 1
+    assert seen == 6
+
+
+@pytest.mark.parametrize("with_sink", [False, True])
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("c", [1, 4, 7])
+def test_compressed_attention_with_full_topk_is_masked_dense(c, mode, with_sink):
+    # with topk above every entry count, each query attends to all entries it
+    # sees: torch's fp64 scaled_dot_product_attention over the compressed rows
+    # with the mask "entry e visible from position p iff (e + 1) c <= p + 1";
+    # a query that sees no entry outputs zero
+    rng = np.random.default_rng(13)
+    H, D, Dv, HI, DI = 3, 10, 6, 2, 4
+    q_lens, prefixes = [17, 23], [5, 0]
+    seq_lens = [n + p for n, p in zip(q_lens, prefixes)]
+    ents = [n // c for n in seq_lens]
+    T, R = sum(q_lens), sum(ents)
+    q = rng.standard_normal((T, H, D))
+    kv = rng.standard_normal((R, D))
+    qi = rng.standard_normal((T, HI, DI))
+    ki = rng.standard_normal((R, DI))
+    w = rng.standard_normal((T, HI))
+    sink = rng.standard_normal(H) if with_sink else None
+    qsl = _qsl(q_lens)
+    out = O.prefill(q, kv, qi, ki, w, qsl, seq_lens, 3, mode, topk=64, scale=0.3, Dv=Dv, sink=sink,
+                    compress_ratio=c)
+    for b in range(2):
+        rows = kv[sum(ents[:b]): sum(ents[:b]) + ents[b]]
+        for t in range(q_lens[b]):
+            g, p = qsl[b] + t, prefixes[b] + t
+            n = (p + 1) // c
+            if n == 0:
+                assert np.all(out[g] == 0)
+                continue
+            qt = torch.from_numpy(q[g])[None, :, None, :]                    # [1,H,1,D]
+            k = torch.from_numpy(rows)[None, None].expand(1, H, len(rows), D)
+            v = torch.from_numpy(rows[:, :Dv])[None, None].expand(1, H, len(rows), Dv)
+            mask = torch.full((1, H, 1, len(rows)), -math.inf, dtype=torch.float64)
+            mask[..., :n] = 0.0
+            if sink is not None:
+                k = torch.cat([k, torch.zeros(1, H, 1, D, dtype=torch.float64)], dim=2)
+                v = torch.cat([v, torch.zeros(1, H, 1, Dv, dtype=torch.float64)], dim=2)
+                mask = torch.cat([mask, torch.from_numpy(sink)[None, :, None, None]], dim=3)
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, k, v, attn_mask=mask, scale=0.3)
+            assert np.allclose(out[g], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-12), (b, t)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_compressed_metadata_extents(mode):
+    # entry extents stay right-aligned: the widest local extent of a request over
+    # all ranks is its entry count, and every local query sees at most that many
+    q_lens, prefixes, cp, c = [37, 20, 9, 300], [25, 0, 4, 900], 4, 128
+    seq_lens = [n + p for n, p in zip(q_lens, prefixes)]
+    widest = [0] * 4
+    for r in range(cp):
+        md = O.build_local_metadata(_qsl(q_lens), seq_lens, cp, r, mode, compress_ratio=c)
+        for j in range(md["local_batch"]):
+            b = md["local_req_id"][j]
+            widest[b] = max(widest[b], md["local_seq_lens"][j])
+            assert md["local_req_kv_base"][j] == sum(n // c for n in seq_lens[:b])
+    assert widest == [n // c for n in seq_lens]
