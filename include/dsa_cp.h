@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define DSA_CP_ABI_VERSION 4
+#define DSA_CP_ABI_VERSION 5
 
 typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 
@@ -69,8 +69,9 @@ enum {
   DSA_MD_LOCAL_MAX_SEQLEN_Q = 6,
   DSA_MD_LOCAL_MAX_SEQLEN_KV = 7,
   DSA_MD_NUM_TOKENS = 8,   /* query tokens T of the batch        */
-  DSA_MD_NUM_KV_ROWS = 9,  /* KV rows of the batch = sum seq_lens */
-  DSA_MD_NUM_SCALARS = 10
+  DSA_MD_NUM_KV_ROWS = 9,  /* KV rows of the batch = sum seq_lens / ratio */
+  DSA_MD_COMPRESS_RATIO = 10,  /* compress_ratio c (1 = uncompressed) */
+  DSA_MD_NUM_SCALARS = 11
 };
 
 /*
@@ -79,7 +80,7 @@ enum {
  * arrays owned by the caller; dsa_cp_metadata_bind carves them out of one
  * buffer of dsa_cp_metadata_sizes() ints.  B = global batch size,
  * tpr = tokens_per_rank.
- *   scalars[10]                 see DSA_MD_*; in round-robin mode the local
+ *   scalars[11]                 see DSA_MD_*; in round-robin mode the local
  *                               rows are {local_start + i*cp_size < local_end}
  *   local_query_start_loc[B+1]  cu-seqlens of the local queries (first
  *                               local_batch+1 entries valid)
@@ -118,7 +119,7 @@ dsa_status dsa_cp_geometry(int32_t num_tokens, int32_t cp_size, int32_t *num_tok
                            int32_t *tokens_per_rank);
 
 /* Host only.  Number of int32 elements one view's metadata needs:
- * 10 + 2*(batch+1) + 4*batch + tokens_per_rank.  `ints_needed` is a host
+ * 11 + 2*(batch+1) + 4*batch + tokens_per_rank.  `ints_needed` is a host
  * pointer. */
 dsa_status dsa_cp_metadata_sizes(int32_t batch, int32_t num_tokens, int32_t cp_size,
                                  size_t *ints_needed);
@@ -160,6 +161,27 @@ dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc, const int
                                        int32_t batch, int32_t num_tokens, int32_t cp_size,
                                        int32_t cp_rank, dsa_cp_mode mode,
                                        const dsa_cp_local_metadata *out, dsa_stream_t stream);
+
+/*
+ * dsa_cp_build_local_metadata for compressed KV ([xLLM] "背景": compress_ratio
+ * in {1, 4, 128}; "5. 模型前向装配": the sparse metadata of every ratio is
+ * built with the local geometry).  At ratio c (>= 1, else
+ * DSA_ERR_INVALID_ARG) a request of seq_lens[b] tokens has seq_lens[b] / c
+ * (rounded down) compressed entries, entry e standing for positions
+ * [e*c, (e+1)*c); the compressed latent rows and index keys of all requests
+ * are stored in request order.  A query at position p sees the entries
+ * e < (p + 1) / c (rounded down).  local_seq_lens, local_kv_start_loc,
+ * local_req_kv_base and scalars[DSA_MD_NUM_KV_ROWS] count entries; query
+ * positions (local_req_pos_base) stay in tokens; scalars[DSA_MD_COMPRESS_RATIO]
+ * = c.  The indexer, top-k and attention read c from the metadata: their
+ * k_idx / kv are then the compressed rows, and a query that sees no entry
+ * selects nothing (-1) and gets a zero output row.  c = 1 is
+ * dsa_cp_build_local_metadata.
+ */
+dsa_status dsa_cp_build_local_metadata_compressed(const int32_t *query_start_loc, const int32_t *seq_lens,
+                                                  int32_t batch, int32_t num_tokens, int32_t cp_size,
+                                                  int32_t cp_rank, dsa_cp_mode mode, int32_t compress_ratio,
+                                                  const dsa_cp_local_metadata *out, dsa_stream_t stream);
 
 /*
  * Split ([blog] "2.B" and "第三部分" step 1; [sglang] cp_split_and_rebuild):

@@ -66,7 +66,8 @@ class CPLocalMetadata:
     FIELDS = ("local_query_start_loc", "local_seq_lens", "local_kv_start_loc", "local_req_id",
               "local_req_kv_base", "local_token_pos", "local_req_pos_base")
     SCALARS = ("num_tokens_pad", "tokens_per_rank", "local_start", "local_end", "local_batch",
-               "local_num_tokens", "local_max_seqlen_q", "local_max_seqlen_kv", "num_tokens", "num_kv_rows")
+               "local_num_tokens", "local_max_seqlen_q", "local_max_seqlen_kv", "num_tokens", "num_kv_rows",
+               "compress_ratio")
 
     def __init__(self, batch: int, num_tokens: int, cp_size: int, device=None):
         self.batch, self.num_tokens, self.cp_size = int(batch), int(num_tokens), int(cp_size)
@@ -97,7 +98,7 @@ class CPLocalMetadata:
 
 def dsa_cp_build_local_metadata(query_start_loc: torch.Tensor, seq_lens: torch.Tensor, num_tokens: int,
                                 cp_size: int, cp_rank: int, mode: int, md: CPLocalMetadata | None = None,
-                                stream=None) -> CPLocalMetadata:
+                                stream=None, compress_ratio: int = 1) -> CPLocalMetadata:
     _need(query_start_loc, torch.int32, "query_start_loc")
     _need(seq_lens, torch.int32, "seq_lens")
     batch = seq_lens.numel()
@@ -107,8 +108,9 @@ def dsa_cp_build_local_metadata(query_start_loc: torch.Tensor, seq_lens: torch.T
         md = CPLocalMetadata(batch, num_tokens, cp_size, query_start_loc.device)
     elif (md.batch, md.num_tokens, md.cp_size) != (batch, num_tokens, cp_size):
         raise ValueError("metadata buffer was sized for another batch / token count / cp_size")
-    check(load().dsa_cp_build_local_metadata(_ptr(query_start_loc), _ptr(seq_lens), batch, num_tokens, cp_size,
-                                             cp_rank, mode, C.byref(md.struct), _stream(stream)),
+    check(load().dsa_cp_build_local_metadata_compressed(_ptr(query_start_loc), _ptr(seq_lens), batch, num_tokens,
+                                                        cp_size, cp_rank, mode, int(compress_ratio),
+                                                        C.byref(md.struct), _stream(stream)),
           "dsa_cp_build_local_metadata")
     return md
 

@@ -32,6 +32,9 @@ SIGNATURES = {
     "dsa_cp_metadata_bind": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.POINTER(LocalMetadata)]),
     "dsa_cp_build_local_metadata": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                               C.c_int, C.POINTER(LocalMetadata), c_stream]),
+    "dsa_cp_build_local_metadata_compressed": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
+                                                         C.c_int32, C.c_int, C.c_int32, C.POINTER(LocalMetadata),
+                                                         c_stream]),
     "dsa_cp_split": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_int32, C.c_void_p,
                                c_stream]),
     "dsa_cp_rerange": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_void_p, c_stream]),

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slot0 = P.row_begin + blockIdx.x * C::kTileTok;
   const int local_batch = P.md.scalars[DSA_MD_LOCAL_BATCH];
+  const int ratio = max(1, P.md.scalars[DSA_MD_COMPRESS_RATIO]);  // compressed KV: tokens per entry
 
   if (tid == 0) {
     misc[1] = 0x7fffffff;
@@ -102,8 +103,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     misc[3] = 0;  // any valid slot
   }
   __syncthreads();
-  // per-slot causal extent: key rows [base, base + p] (base = KV row of the
-  // request's position 0, p = the query's in-request position)
+  // per-slot causal extent: key rows [base, base + last] (base = KV row of the
+  // request's position 0 or first entry, last = the query's in-request
+  // position, or its last visible entry (p + 1) / ratio - 1 for compressed KV;
+  // -1: no key)
   for (int t = tid; t < C::kTileTok; t += C::kThreads) {
     const int slot = slot0 + t;
     int base = 0, p = -1;
@@ -112,8 +115,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (g >= 0 && local_batch > 0) {
         const int j = find_local_request(P.md.local_query_start_loc, local_batch, slot);
         base = P.md.local_req_kv_base[j];
-        p = g - P.md.local_req_pos_base[j];
-        if (p < 0 || p >= P.max_kv_len || base < 0 || base + p >= P.num_kv_rows) {
+        const int pos = g - P.md.local_req_pos_base[j];
+        p = pos >= 0 ? (pos + 1) / ratio - 1 : -1;
+        if (pos < 0 || p >= P.max_kv_len || base < 0 || base + p >= P.num_kv_rows) {
           record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 41, slot);
           p = -1;
         }
@@ -330,8 +334,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     if (g >= 0 && nb > 0) {
       const int j = find_local_request(md.local_query_start_loc, nb, slot);
       base = md.local_req_kv_base[j];
-      p = g - md.local_req_pos_base[j];
-      if (p < 0 || p >= max_kv_len) {
+      const int pos = g - md.local_req_pos_base[j];
+      const int ratio = max(1, md.scalars[DSA_MD_COMPRESS_RATIO]);
+      p = pos >= 0 ? (pos + 1) / ratio - 1 : -1;  // last visible key / entry, -1: none
+      if (pos < 0 || p >= max_kv_len) {
         record_error(err, DSA_ERR_DEVICE_BOUNDS, 42, slot);
         p = -1;
       }

@@ -59,7 +59,7 @@ __device__ Quad block_exclusive_scan(Quad v, Quad &tot) {
 
 __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__restrict__ qsl,
                                                                const int32_t *__restrict__ seq_lens, int B,
-                                                               int T, int cp, int rank, int mode,
+                                                               int T, int cp, int rank, int mode, int ratio,
                                                                dsa_cp_local_metadata md, int *err) {
   __shared__ int s_bad;
   __shared__ int s_run[4];  // running local_batch, query total, kv extent total, kv rows
@@ -116,8 +116,9 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
       if (b < B) {
         qs = __ldg(qsl + b);
         const int qe = __ldg(qsl + b + 1);
-        v.d = __ldg(seq_lens + b);
-        prefix = v.d - (qe - qs);
+        const int sl = __ldg(seq_lens + b);
+        prefix = sl - (qe - qs);
+        v.d = sl / ratio;  // compressed entries of the request (all of it, c = 1)
         int64_t q_len = 0, last = -1;
         if (mode == DSA_CP_IN_SEQ_SPLIT) {
           const int64_t lo = qs > lo_inseq ? qs : lo_inseq;
@@ -145,8 +146,9 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
             last = g0 + (q_len - 1) * cp;
           }
         }
-        // KV extent: the prefix plus the positions up to the last local query
-        if (q_len > 0) v = {1, static_cast<int>(q_len), static_cast<int>(prefix + last - qs + 1), v.d};
+        // KV extent: the prefix plus the positions up to the last local query,
+        // in entries of `ratio` tokens
+        if (q_len > 0) v = {1, static_cast<int>(q_len), static_cast<int>((prefix + last - qs + 1) / ratio), v.d};
       }
       Quad tot;
       Quad ex = block_exclusive_scan(v, tot);
@@ -193,7 +195,8 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
     s[DSA_MD_LOCAL_MAX_SEQLEN_Q] = s_maxq;
     s[DSA_MD_LOCAL_MAX_SEQLEN_KV] = s_maxkv;
     s[DSA_MD_NUM_TOKENS] = T;
-    s[DSA_MD_NUM_KV_ROWS] = bad ? 0 : static_cast<int32_t>(s_kv_rows);
+    s[DSA_MD_NUM_KV_ROWS] = bad ? 0 : s_run[3];  // sum of the requests' entries
+    s[DSA_MD_COMPRESS_RATIO] = ratio;
   }
 }
 
@@ -202,11 +205,13 @@ __global__ void __launch_bounds__(kThreads) cp_metadata_kernel(const int32_t *__
 
 using namespace dsa;
 
-extern "C" dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc, const int32_t *seq_lens,
-                                                  int32_t batch, int32_t num_tokens, int32_t cp_size,
-                                                  int32_t cp_rank, dsa_cp_mode mode,
-                                                  const dsa_cp_local_metadata *out, dsa_stream_t stream) {
+extern "C" dsa_status dsa_cp_build_local_metadata_compressed(const int32_t *query_start_loc,
+                                                             const int32_t *seq_lens, int32_t batch,
+                                                             int32_t num_tokens, int32_t cp_size, int32_t cp_rank,
+                                                             dsa_cp_mode mode, int32_t compress_ratio,
+                                                             const dsa_cp_local_metadata *out, dsa_stream_t stream) {
   if (!query_start_loc || !seq_lens || !out) return DSA_ERR_INVALID_ARG;
+  if (compress_ratio < 1) return DSA_ERR_INVALID_ARG;
   if (cp_size < 1 || cp_rank < 0 || cp_rank >= cp_size) return DSA_ERR_INVALID_ARG;
   if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN && mode != DSA_CP_HEAD_TAIL)
     return DSA_ERR_INVALID_ARG;
@@ -220,6 +225,15 @@ extern "C" dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
   cp_metadata_kernel<<<1, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      query_start_loc, seq_lens, batch, num_tokens, cp_size, cp_rank, static_cast<int>(mode), *out, err);
+      query_start_loc, seq_lens, batch, num_tokens, cp_size, cp_rank, static_cast<int>(mode), compress_ratio, *out,
+      err);
   return check_launch();
+}
+
+extern "C" dsa_status dsa_cp_build_local_metadata(const int32_t *query_start_loc, const int32_t *seq_lens,
+                                                  int32_t batch, int32_t num_tokens, int32_t cp_size,
+                                                  int32_t cp_rank, dsa_cp_mode mode,
+                                                  const dsa_cp_local_metadata *out, dsa_stream_t stream) {
+  return dsa_cp_build_local_metadata_compressed(query_start_loc, seq_lens, batch, num_tokens, cp_size, cp_rank, mode,
+                                                1, out, stream);
 }

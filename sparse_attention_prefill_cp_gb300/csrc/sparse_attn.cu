@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *stg_free = staged + 2;             // [2] the bulk copy has read our tile (sender)
   uint64_t *fin_full = stg_free + 2;           // both warpgroups' denominators written (8 warps)
   uint64_t *o_staged = fin_full + 1;           // normalised O rows staged in smem (8 warps)
-  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);  // [0] tmem, [1] base, [2] p, [3] g, [4] T
+  // [0] tmem, [1] base, [2] keys the query sees (-1: pad or error), [3] g, [4] T
+  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kOffMisc);
   float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -185,8 +186,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (g >= 0 && nbatch > 0) {
       const int j = find_local_request(P.md.local_query_start_loc, nbatch, slot);
       base = P.md.local_req_kv_base[j];
-      p = g - P.md.local_req_pos_base[j];
-      if (p < 0 || base < 0 || base + p >= P.num_kv_rows || (P.flat && g >= P.q_rows)) {
+      const int pos = g - P.md.local_req_pos_base[j];
+      const int ratio = max(1, P.md.scalars[DSA_MD_COMPRESS_RATIO]);
+      p = pos >= 0 ? (pos + 1) / ratio : -1;  // keys (entries) the query sees
+      if (pos < 0 || base < 0 || base + p > P.num_kv_rows || (P.flat && g >= P.q_rows)) {
         record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 44, slot);
         p = -1;
       }
@@ -227,15 +230,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const int p = misc[2];
-  const int n_valid = p >= 0 ? min(p + 1, P.topk) : 0;
+  const int n_valid = p >= 0 ? min(p, P.topk) : 0;
   const int nb = (n_valid + C::kBN - 1) / C::kBN;
   const int qrow = P.flat ? misc[3] : slot;  // the view's row of q and of the output
   __nv_bfloat16 *out_row = P.out + (static_cast<int64_t>(qrow) * P.H) * P.Dv + main_dim0;
 
   if (nb == 0) {
-    // pad slot: zero output rows (the head-sharded layout has none)
-    if (P.hc == 0 && !P.flat && warp < 4 && tid < P.H) {
+    // a pad slot (zero rows in the view layout; the other layouts have none),
+    // or a token that sees no compressed entry (zero rows in every layout)
+    const bool no_keys = misc[3] >= 0 && p == 0;
+    if ((no_keys || (P.hc == 0 && !P.flat)) && warp < 4 && tid < P.H) {
       __nv_bfloat16 *o = out_row + static_cast<int64_t>(tid) * P.Dv;
+      if (P.hc > 0) {  // head-sharded: rank tid / hc, token g, head tid % hc
+        const int rd = tid / P.hc;
+        o = P.out + ((static_cast<int64_t>(rd) * misc[4] + misc[3]) * P.hc + (tid - rd * P.hc)) * P.Dv + main_dim0;
+      }
       for (int c = 0; c < C::DVC; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
     }
   } else if (warp == 8) {

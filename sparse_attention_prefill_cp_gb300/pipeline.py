@@ -29,7 +29,7 @@ from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_meta
 class DSAPrefill:
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
                  softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1,
-                 prefix_lens=None, kv_fp8: bool = False, fused: bool = False):
+                 prefix_lens=None, kv_fp8: bool = False, fused: bool = False, compress_ratio: int = 1):
         """``lengths``: query tokens per request.  ``prefix_lens`` (chunked
         prefill): KV positions per request that precede its queries; the KV
         and index-key tensors passed to ``run`` then hold every request's
@@ -39,7 +39,9 @@ class DSAPrefill:
         ``fused``: ``run`` skips the split of q and the rerange of the
         outputs; each view's attention reads its queries from the full q and
         writes its rows of ``out`` in place (dsa_sparse_attn_prefill_flat),
-        with the same results."""
+        with the same results.  ``compress_ratio`` c: the latent KV and index
+        keys passed to ``run`` are compressed entries, floor(seq_len / c) per
+        request in request order (dsa_cp_build_local_metadata_compressed)."""
         self.device = torch.device(device or "cuda")
         self.lengths = [int(x) for x in lengths]
         self.prefix_lens = [0] * len(self.lengths) if prefix_lens is None else [int(x) for x in prefix_lens]
@@ -51,8 +53,11 @@ class DSAPrefill:
         self.T = sum(self.lengths)
         self.B = len(self.lengths)
         self.kv_lens = [n + p for n, p in zip(self.lengths, self.prefix_lens)]
-        self.num_kv_rows = sum(self.kv_lens)
-        self.max_kv_len = max(self.kv_lens)
+        self.compress_ratio = int(compress_ratio)
+        if self.compress_ratio < 1:
+            raise ValueError("compress_ratio must be at least 1")
+        self.num_kv_rows = sum(n // self.compress_ratio for n in self.kv_lens)
+        self.max_kv_len = max(1, max(n // self.compress_ratio for n in self.kv_lens))
         self.pad, self.tpr = dsa_cp_geometry(self.T, cp_size)
         qsl = [0]
         for n in self.lengths:
@@ -111,7 +116,7 @@ class DSAPrefill:
     def metadata(self, stream=None):                                     # a1
         for r in range(self.cp_size):
             dsa_cp_build_local_metadata(self.query_start_loc, self.seq_lens, self.T, self.cp_size, r, self.mode,
-                                        self.md[r], stream)
+                                        self.md[r], stream, self.compress_ratio)
 
     def split(self, q, q_idx, w, stream=None):                          # a2
         if not self.fused:  # the fused attention reads q in place

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 4
+    assert lib.dsa_abi_version() == 5
     for code, name in _lib.STATUS.items():
         assert lib.dsa_status_string(code).decode().startswith(name)
 
@@ -49,14 +49,14 @@ def test_metadata_sizes_and_bind(lib):
     B, T, cp = 4, 11805, 4
     n = dsa.dsa_cp_metadata_sizes(B, T, cp)
     tpr = O.padded_geometry(T, cp)[1]
-    assert n == 10 + 2 * (B + 1) + 4 * B + tpr
+    assert n == 11 + 2 * (B + 1) + 4 * B + tpr
     md = _lib.LocalMetadata()
     base = 0x10000
     assert lib.dsa_cp_metadata_bind(C.c_void_p(base), B, T, cp, C.byref(md)) == 0
     offs = [md.scalars, md.local_query_start_loc, md.local_seq_lens, md.local_kv_start_loc, md.local_req_id,
             md.local_req_kv_base, md.local_req_pos_base, md.local_token_pos]
-    assert [(o - base) // 4 for o in offs] == [0, 10, 10 + B + 1, 10 + 2 * B + 1, 10 + 3 * B + 2, 10 + 4 * B + 2,
-                                                10 + 5 * B + 2, 10 + 6 * B + 2]
+    assert [(o - base) // 4 for o in offs] == [0, 11, 11 + B + 1, 11 + 2 * B + 1, 11 + 3 * B + 2, 11 + 4 * B + 2,
+                                                11 + 5 * B + 2, 11 + 6 * B + 2]
     assert (md.local_token_pos - base) // 4 + tpr == n
 
 
@@ -79,6 +79,7 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.dsa_cp_rerange(p, 16, -1, 2, 1, p, None) == 2
     assert lib.dsa_cp_build_local_metadata(p, p, 1, 16, 2, 2, 0, C.byref(md), None) == 1
     assert lib.dsa_cp_build_local_metadata(p, p, 1, 16, 0, 0, 0, C.byref(md), None) == 1
+    assert lib.dsa_cp_build_local_metadata_compressed(p, p, 1, 16, 2, 0, 0, 0, C.byref(md), None) == 1
     assert lib.dsa_cp_geometry(5, 0, C.byref(C.c_int32()), C.byref(C.c_int32())) == 1
     # dimension sets that are not compiled
     assert lib.dsa_indexer_topk(C.byref(md), 1, 8, 16, p, p, p, 16, 32, 128, 2048, p, p, 1 << 20, None) == 3

@@ -455,6 +455,82 @@ def test_chunked_prefill(wl, prefixes, mode):
     dsa.dsa_poll_device_error()
 
 
+# ------------------------------------------------------------------ compressed KV
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("q_lens,prefixes,cp,c", [([9, 6], [0, 0], 2, 4), ([5, 3], [130, 0], 2, 128),
+                                                  ([37, 20, 9, 300], [25, 0, 4, 900], 4, 128),
+                                                  ([8000, 800, 5, 3000], [0, 0, 0, 0], 4, 4)],
+                         ids=lambda v: str(v)[:24])
+def test_metadata_compressed_bit_exact(q_lens, prefixes, cp, c, mode):
+    T = sum(q_lens)
+    seq_lens = [n + p for n, p in zip(q_lens, prefixes)]
+    qsl = torch.tensor(qsl_of(q_lens), dtype=torch.int32, device="cuda")
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    for r in range(cp):
+        got = dsa.dsa_cp_build_local_metadata(qsl, sl, T, cp, r, mode, compress_ratio=c).to_host()
+        ref = O.build_local_metadata(qsl_of(q_lens), seq_lens, cp, r, mode, compress_ratio=c)
+        for k, v in ref.items():
+            assert got[k] == v, (k, r)
+    dsa.dsa_poll_device_error()
+
+
+COMPRESSED_CASES = [(TINY_INT.with_(name="tiny-int-c4", lengths=(600, 100)), 4),
+                    (TINY.with_(name="tiny-c128-sink", lengths=(600, 100), sink=True), 128),
+                    (FLOAT_FULL.with_(name="float-full-c4", lengths=(10000, 1500)), 4),
+                    (FLOAT_FULL.with_(name="float-full-c128", lengths=(10000, 1500)), 128)]
+
+
+@pytest.mark.parametrize("mode", (IN_SEQ_SPLIT, ROUND_ROBIN))
+@pytest.mark.parametrize("wl,c", COMPRESSED_CASES, ids=lambda v: v.name if isinstance(v, Workload) else str(v))
+def test_compressed_prefill(wl, c, mode):
+    # queries of every token; compressed latent rows and index keys: floor(len / c)
+    # per request, taken from the first rows of a draw (any rows serve as entries)
+    x = draw_inputs(wl)
+    R = sum(n // c for n in wl.lengths)
+    x["kv"], x["k_idx"] = x["kv"][:R].contiguous(), x["k_idx"][:R].contiguous()
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    args = (wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale)
+    pipe = DSAPrefill(*args, compress_ratio=c)
+    out = pipe.run(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"]).clone()
+    dsa.dsa_poll_device_error()
+    fused = DSAPrefill(*args, compress_ratio=c, fused=True, view_streams=2)
+    fused.out.fill_(float("nan"))
+    assert torch.equal(fused.run(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"]), out)
+    hs = pipe.run_headsharded(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"]).clone()
+    pipe.run(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"])
+    assert torch.equal(hs, pipe.all_to_all_heads())
+    dsa.dsa_poll_device_error()
+    kv64, ki64 = f64(x["kv"]), f64(x["k_idx"])  # the compressed rows (small); query rows per sample
+    sink = None if x["sink"] is None else f64(x["sink"])
+    idx = pipe.topk_idx.cpu().numpy()
+    rng = np.random.default_rng(5)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode, compress_ratio=c)
+        got = pipe.md[r].to_host()
+        for k, v in md.items():
+            assert got[k] == v, (k, r)
+        slots = range(pipe.tpr) if pipe.tpr <= 400 else sorted(set(rng.choice(pipe.tpr, 40, replace=False)) |
+                                                                 {0, 1, 2, 3, pipe.tpr - 1})
+        for i in slots:
+            g = md["local_token_pos"][i]
+            if g < 0:
+                assert np.all(idx[r, i] == -1)
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            n = (g - md["local_req_pos_base"][j] + 1) // c
+            if n == 0:  # sees no entry: nothing selected, zero output
+                assert np.all(idx[r, i] == -1)
+                assert np.all(pipe.out_split[r, i].cpu().float().numpy() == 0)
+                continue
+            ref_scores = O.indexer_scores(f64(x["q_idx"][g]), f64(x["w"][g]), ki64[base:base + n])
+            check_topk_row(idx[r, i], ref_scores, base, wl.topk, exact=wl.integer)
+            sel = idx[r, i][idx[r, i] >= 0]
+            ref = O.sparse_attention(f64(x["q"][g]), kv64[sel], wl.scale, wl.Dv, sink)
+            check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref)
+
+
 # ------------------------------------------------------------------ fused split / rerange (flat layout)
 
 @pytest.mark.parametrize("wl,mode,prefixes", [(TINY, IN_SEQ_SPLIT, None), (TINY, ROUND_ROBIN, None),
