@@ -69,17 +69,19 @@ def positions(wl):
     return np.concatenate([np.arange(n) for n in wl.lengths])
 
 
-def algorithmic(wl):
+def algorithmic(wl, compress_ratio: int = 1):
     """FLOPs (indexer, attention) and bytes per batch of the a3-a5 core, as
     counted for the roofline: indexer sum over causal pairs of HI*DI*2,
-    attention sum over tokens of min(p+1, topk)*H*(D+Dv)*2; bytes = q, q_idx,
-    w, kv, k_idx read once, output written once, top-k indices written and read."""
-    p = positions(wl).astype(np.float64)
-    f_idx = float(np.sum(p + 1) * wl.HI * wl.DI * 2)
-    f_att = float(np.sum(np.minimum(p + 1, wl.topk)) * wl.H * (wl.D + wl.Dv) * 2)
+    attention sum over tokens of min(p+1, topk)*H*(D+Dv)*2 (with compressed KV
+    at ratio c the keys of position p are its floor((p+1)/c) entries); bytes =
+    q, q_idx, w, kv, k_idx read once, output written once, top-k indices
+    written and read."""
+    n = np.floor((positions(wl).astype(np.float64) + 1) / compress_ratio)
+    f_idx = float(np.sum(n) * wl.HI * wl.DI * 2)
+    f_att = float(np.sum(np.minimum(n, wl.topk)) * wl.H * (wl.D + wl.Dv) * 2)
     T = wl.num_tokens
-    per_tok = (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4 + wl.D * 2 + wl.DI * 2 + wl.H * wl.Dv * 2
-               + 2 * wl.topk * 4)
+    per_tok = (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4 + (wl.D * 2 + wl.DI * 2) / compress_ratio
+               + wl.H * wl.Dv * 2 + 2 * wl.topk * 4)
     return f_idx, f_att, float(T * per_tok)
 
 
@@ -91,6 +93,10 @@ def view_attention_flops(wl, cp, mode):
     for r in range(cp):
         if mode == W.IN_SEQ_SPLIT:
             g = np.arange(r * tpr, min((r + 1) * tpr, wl.num_tokens))
+        elif mode == W.HEAD_TAIL:  # a head chunk of ceil(tpr/2) rows, a tail chunk of floor(tpr/2)
+            h, t = (tpr + 1) // 2, tpr // 2
+            g = np.concatenate([np.arange(r * h, (r + 1) * h), np.arange(cp * h + (cp - 1 - r) * t, cp * h + (cp - r) * t)])
+            g = g[g < wl.num_tokens]
         else:
             g = np.arange(r, wl.num_tokens, cp)
         out.append(float(np.sum(np.minimum(p[g] + 1, wl.topk)) * wl.H * (wl.D + wl.Dv) * 2))
@@ -423,6 +429,26 @@ def run_ours(args, wl, mode, rank, world):
                          "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
         aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
         aux["a1_metadata_ms"] = timed(pipe.metadata)  # every view's build_cp_local_metadata
+
+        # compressed KV: the same queries over floor(T / c) compressed entries
+        # (the first rows of kv and k_idx stand for them), the a3-a5 core timed
+        # with its metadata, against the roofline of its own work
+        for c in (4, 128):
+            rows = wl.num_tokens // c
+            pc = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
+                            view_streams=args.view_streams, fused=True, compress_ratio=c)
+            pc.run(x["q"], x["kv"][:rows], x["q_idx"], x["k_idx"][:rows], x["w"], x["sink"])
+
+            def core_c(pc=pc, rows=rows):
+                pc.metadata()
+                pc._q = x["q"]
+                pc.views(x["kv"][:rows], x["k_idx"][:rows], x["sink"], torch.cuda.current_stream())
+
+            ms = timed(core_c, reps=3)
+            fi, fa, by = algorithmic(wl, c)
+            roof_c = max((fi + fa) / (pk["bf16_tflops_sustained"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+            aux[f"a3_a5_compressed_c{c}"] = {"ms": ms, "flops": fi + fa, "roofline_frac": roof_c / (ms / 1e3)}
+            del pc
         # FP8 latent-KV cache: quantise / dequantise as HBM passes (bytes read +
         # written), and the a3-a5 core over the cache (dequantisation + views)
         cache = dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv)
@@ -453,7 +479,8 @@ def run_ours(args, wl, mode, rank, world):
                        "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
                        "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
                        "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own; "
-                       "a1_metadata_ms: every view's metadata (one launch per view)")
+                       "a1_metadata_ms: every view's metadata (one launch per view); "
+                       "a3_a5_compressed_c*: metadata + core over compressed KV at ratio c (T / c entries)")
         dsa.dsa_poll_device_error()
 
     launches = pipe.launches_per_step() * args.steps

@@ -140,6 +140,20 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
+// Zero one output row of the CTA's value columns: head h of the view-layout or
+// flat row at out_row, or of token g in the head-sharded layout.  Kept out of
+// line: it runs only for pad slots and for queries without keys, and inlined
+// its address arithmetic costs the pipelined part of the kernel registers.
+__device__ __noinline__ void zero_row(const AttnParams &P, __nv_bfloat16 *out_row, int h, int g, int T, int col0,
+                                      int cols) {
+  __nv_bfloat16 *o = out_row + static_cast<int64_t>(h) * P.Dv;
+  if (P.hc > 0) {  // head-sharded: rank h / hc, token g, head h % hc
+    const int rd = h / P.hc;
+    o = P.out + ((static_cast<int64_t>(rd) * T + g) * P.hc + (h - rd * P.hc)) * P.Dv + col0;
+  }
+  for (int c = 0; c < cols; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -238,15 +252,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (nb == 0) {
     // a pad slot (zero rows in the view layout; the other layouts have none),
     // or a token that sees no compressed entry (zero rows in every layout)
-    const bool no_keys = misc[3] >= 0 && p == 0;
-    if ((no_keys || (P.hc == 0 && !P.flat)) && warp < 4 && tid < P.H) {
-      __nv_bfloat16 *o = out_row + static_cast<int64_t>(tid) * P.Dv;
-      if (P.hc > 0) {  // head-sharded: rank tid / hc, token g, head tid % hc
-        const int rd = tid / P.hc;
-        o = P.out + ((static_cast<int64_t>(rd) * misc[4] + misc[3]) * P.hc + (tid - rd * P.hc)) * P.Dv + main_dim0;
-      }
-      for (int c = 0; c < C::DVC; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
-    }
+    if (warp < 4 && tid < P.H && ((misc[3] >= 0 && p == 0) || (P.hc == 0 && !P.flat)))
+      zero_row(P, out_row, tid, misc[3], misc[4], main_dim0, C::DVC);
   } else if (warp == 8) {
     if (lane == 0) {
       // ---------------- TMA: Q (main dims to a staging tile, tail dims in place)
