@@ -24,7 +24,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 // The device error record: err[0] = first dsa_status recorded, err[1] = the
 // site that recorded it, err[2] = a site-specific detail (e.g. block index),
 // err[3] = the CTA (linear block index).  Only the first error is kept.
-__device__ __forceinline__ void record_error(int *err, int code, int site = 0, int detail = 0) {
+// Out of line: error paths are cold, and inlined copies of them cost the
+// pipelined kernels registers and scheduling freedom.
+static __device__ __noinline__ void record_error(int *err, int code, int site = 0, int detail = 0) {
   if (err && atomicCAS(err, 0, code) == 0) {
     err[1] = site;
     err[2] = detail;
@@ -132,10 +134,9 @@ __device__ __forceinline__ bool mbar_try_wait_hint_cluster(uint64_t *bar, uint32
 // limit (record DSA_ERR_DEVICE_TIMEOUT with `site` / `detail` and return
 // false), so a waiter notices its phase completing without a memory round
 // trip, and a stuck pipeline still drains within about a second.
-template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int site = 0,
-                                          int detail = 0) {
-  if (kCluster ? mbar_try_wait_hint_cluster(bar, parity) : mbar_try_wait_hint(bar, parity)) return true;
+// The slow part of mbar_wait, out of line (the fast path is one try_wait).
+template <bool kCluster>
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int *err, int site, int detail) {
   const long long t0 = clock64();
   long long t_check = t0;
   while (true) {
@@ -150,6 +151,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
       t_check = now;
     }
   }
+}
+
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int site = 0,
+                                          int detail = 0) {
+  if (kCluster ? mbar_try_wait_hint_cluster(bar, parity) : mbar_try_wait_hint(bar, parity)) return true;
+  return mbar_wait_slow<kCluster>(bar, parity, err, site, detail);
 }
 
 // ------------------------------------------------------------------ cluster

@@ -154,6 +154,22 @@ __device__ __noinline__ void zero_row(const AttnParams &P, __nv_bfloat16 *out_ro
   for (int c = 0; c < cols; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0, 0, 0, 0);
 }
 
+// Multiply TMEM columns [c0, c1) of the warp's lanes by alpha (the lazy
+// rescale of O).  Out of line: it runs only when a row's max grows by more
+// than 2^8.  Warp-collective (tcgen05.ld/st .sync.aligned): the whole warp calls it.
+__device__ __noinline__ void scale_o_cols(uint32_t lane_base, int c0, int c1, float alpha) {
+#pragma unroll 1
+  for (int c = c0; c < c1; c += 32) {
+    uint32_t r[32];
+    tmem_ld32(lane_base + c, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+    tmem_st32(lane_base + c, r);
+  }
+  tmem_st_wait();
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -542,16 +558,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, P.err, 30, i));
           if (!ok) break;
           tc_fence_after();
-#pragma unroll 1
-          for (int c = w * (C::kOCols / 2); c < (w + 1) * (C::kOCols / 2); c += 32) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + c, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-            tmem_st32(lane_base + c, r);
-          }
-          tmem_st_wait();
+          scale_o_cols(lane_base, w * (C::kOCols / 2), (w + 1) * (C::kOCols / 2), alpha);
         }
         l *= alpha;
         m_used = m_new;
