@@ -24,6 +24,11 @@ NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")] + ARCH
 
 
+# Per-source ptxas settings, measured: the attention kernel's pipelined loop
+# runs ~1 % faster with ptxas -O1 than with the default -O3 (same registers).
+SOURCE_FLAGS = {"sparse_attn.cu": ["-Xptxas", "-O1"]}
+
+
 def nvcc() -> str:
     path = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(path):
@@ -52,7 +57,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc()] + NVCC_FLAGS + list(extra_flags) + ["-c", src, "-o", obj]
+            cmd = [nvcc()] + NVCC_FLAGS + SOURCE_FLAGS.get(os.path.basename(src), []) + list(extra_flags) + \
+                ["-c", src, "-o", obj]
             if verbose:
                 print(" ".join(cmd), flush=True)
             procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
