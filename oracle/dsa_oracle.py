@@ -76,6 +76,13 @@ design notes):
       entries.  Entries of all requests are stored in request order.  A query
       that sees no entry selects nothing and its output is zero.  c = 1 is
       the uncompressed path.
+  R14 FP8 indexer operands (the FP8 path of [blog] 1 applied to the index
+      query and keys; the pages fix no format): each DI-wide index row (a key
+      k_I[s], or one head q_I[t, j]) is stored like an R12 cache row with
+      D = Dv = DI (codes, one fp32 scale per 128 columns, zero padding), and
+      stands for the real values decode(code) * scale, taken exactly (no
+      rounding to bf16).  The FP8 indexer score is the indexer score of those
+      values.
 
 parity pins: every function here is pinned by tests/test_oracle_pins.py
 against worked examples from the pages (tests/golden/), closed forms,
@@ -546,3 +553,29 @@ def kv_fp8_dequantize(cache, D: int, Dv: int) -> np.ndarray:
     rope16 = np.ascontiguousarray(b[:, off: off + 2 * (D - Dv)]).view(np.uint16).astype(np.uint32) << 16
     out[:, Dv:] = rope16.view(np.float32)
     return out
+
+
+# --------------------------------------------------------------------------
+# FP8 indexer operands (R14)
+# --------------------------------------------------------------------------
+
+def index_fp8_values(rows, DI: int) -> np.ndarray:
+    """FP8 index rows [R, kv_fp8_row_bytes(DI, DI)] -> the values they stand
+    for, [R, DI] float64: decode(code) * scale of the code's 128-column tile,
+    exact (an E4M3 value has 4 significant bits, an fp32 scale 24)."""
+    b = np.asarray(rows, dtype=np.uint8)
+    R = b.shape[0]
+    tiles = -(-DI // FP8_TILE)
+    out = np.zeros((R, DI), dtype=np.float64)
+    for t in range(tiles):
+        cols = slice(t * FP8_TILE, min((t + 1) * FP8_TILE, DI))
+        scale = np.ascontiguousarray(b[:, DI + 4 * t: DI + 4 * t + 4]).view(np.float32).reshape(R)
+        out[:, cols] = e4m3_decode(b[:, cols]) * scale.astype(np.float64)[:, None]
+    return out
+
+
+def indexer_scores_fp8(q_idx_row8, w_row, k_idx_keys8, DI: int) -> np.ndarray:
+    """The indexer score (indexer_scores) of the values FP8 index rows stand
+    for: q_idx_row8 [HI, row_bytes] (one query's heads), k_idx_keys8
+    [n, row_bytes] -> fp64 [n]."""
+    return indexer_scores(index_fp8_values(q_idx_row8, DI), w_row, index_fp8_values(k_idx_keys8, DI))

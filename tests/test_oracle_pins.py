@@ -520,6 +520,76 @@ def test_kv_fp8_cache_layout_and_error_bound(D, Dv):
     assert np.all(c[7, :Dv] == 0) and np.all(d[7] == 0)
 
 
+# ---------------------------------------------------------------- FP8 indexer operands (R14)
+# Index rows in the FP8 cache row format with D = Dv = DI; the score is the
+# indexer score of decode(code) * scale.  Pins: the hand example with its
+# operands as hand-encoded bytes, a closed form with distinct per-row scales,
+# and exact agreement with the plain indexer where quantisation is exact.
+
+def _golden_fp8_rows(name):
+    out = {}
+    for line in read_golden_lines(name):
+        k, v = (x.strip() for x in line.split("=", 1))
+        out[k] = v.split()
+    return out
+
+
+def test_indexer_fp8_hand_example():
+    g = _golden_fp8_rows("indexer_fp8_hand_example.txt")
+    q8 = np.array([int(x, 16) for x in g["q_rows"]], dtype=np.uint8).reshape(2, 16)
+    k8 = np.array([int(x, 16) for x in g["k_rows"]], dtype=np.uint8).reshape(5, 16)
+    assert O.kv_fp8_row_bytes(2, 2) == 16
+    assert np.array_equal(O.index_fp8_values(q8, 2).reshape(-1), np.array(g["values_q"], dtype=float))
+    assert np.array_equal(O.index_fp8_values(k8, 2).reshape(-1), np.array(g["values_k"], dtype=float))
+    w = np.array(g["w"], dtype=float)
+    assert np.array_equal(O.indexer_scores_fp8(q8, w, k8, 2), np.array(g["scores"], dtype=float))
+    # the same scores as the plain hand example
+    assert np.array_equal(O.indexer_scores_fp8(q8, w, k8, 2),
+                          np.array(read_golden("indexer_hand_example.txt")["scores"], dtype=float))
+
+
+def test_indexer_fp8_closed_form_row_scales():
+    # every code 1.0 (0x38); head j has scale a_j, key s scale b_s: q . k = DI a_j b_s,
+    # so I[s] = DI b_s sum_j w_j a_j (all dots positive).  A scale read from the
+    # wrong row or operand, or a dropped scale, breaks it.
+    HI, DI, n = 3, 128, 5
+    a = np.array([0.5, 2.0, 0.125], dtype=np.float32)
+    b = np.array([1.0, 0.25, 4.0, 3.0, 0.75], dtype=np.float32)
+    def rows(scales):
+        r = np.zeros((len(scales), O.kv_fp8_row_bytes(DI, DI)), dtype=np.uint8)
+        r[:, :DI] = 0x38
+        r[:, DI:DI + 4] = scales.view(np.uint8).reshape(-1, 4)
+        return r
+    w = np.array([1.0, -0.5, 3.0])
+    expect = DI * b.astype(float) * float((w * a).sum())
+    assert np.array_equal(O.indexer_scores_fp8(rows(a), w, rows(b), DI), expect)
+    assert O.indexer_scores_fp8(rows(a), w, rows(b), DI).shape == (n,)
+
+
+def test_indexer_fp8_exact_where_quantisation_is_exact():
+    # rows made of E4M3 values times a power of two, each row holding +-448 times
+    # it: the quantiser's scale is that power of two and every code is exact, so
+    # the FP8 score equals the plain indexer score of the original rows.
+    rng = np.random.default_rng(21)
+    HI, DI, n = 4, 128, 40
+    def exact_rows(R):
+        vals = O.e4m3_decode(rng.integers(0, 0x7F, size=(R, DI)).astype(np.uint8) | (rng.integers(0, 2, (R, DI)) << 7).astype(np.uint8))
+        vals[:, 5] = 448.0 * np.where(rng.integers(0, 2, R) == 1, 1.0, -1.0)
+        return vals * np.exp2(rng.integers(-12, -4, size=(R, 1)))
+    q, k = exact_rows(HI), exact_rows(n)
+    q8, k8 = O.kv_fp8_quantize(q.astype(np.float32), DI), O.kv_fp8_quantize(k.astype(np.float32), DI)
+    assert np.array_equal(O.index_fp8_values(q8, DI), q) and np.array_equal(O.index_fp8_values(k8, DI), k)
+    w = rng.standard_normal(HI)
+    assert np.array_equal(O.indexer_scores_fp8(q8, w, k8, DI), O.indexer_scores(q, w, k))
+    # general rows: within the quantisation error of the plain score
+    qf = O.bf16_round(rng.standard_normal((HI, DI)).astype(np.float32)).astype(float)
+    kf = O.bf16_round(rng.standard_normal((n, DI)).astype(np.float32)).astype(float)
+    s8 = O.indexer_scores_fp8(O.kv_fp8_quantize(qf.astype(np.float32), DI), w, O.kv_fp8_quantize(kf.astype(np.float32), DI), DI)
+    s = O.indexer_scores(qf, w, kf)
+    bound = np.abs(w) @ (np.abs(qf) @ np.abs(kf).T) * (2 * 2.0 ** -4 + 2.0 ** -8)
+    assert np.all(np.abs(s8 - s) <= bound) and not np.array_equal(s8, s)
+
+
 # ---------------------------------------------------------------- compressed KV (R13)
 
 _COMPRESSED_CASES = {"C": ([9, 6], [9, 6], 2, 4), "D": ([5, 3], [135, 3], 2, 128)}  # q_lens, seq_lens, cp, c
