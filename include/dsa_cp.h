@@ -296,6 +296,35 @@ dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, in
                               int32_t row_count, float *scores, dsa_stream_t stream);
 
 /*
+ * FP8 indexer operands (the FP8 path that "[DeepSeek v3.2] 上下文并行详解",
+ * section 1, opens with round-robin-split, applied to the index query and
+ * keys; the page fixes no format).  q_idx8 and k_idx8 hold every DI-wide
+ * index row -- one head of one local query, or one key -- in the FP8 cache
+ * row format with D = Dv = DI (dsa_kv_fp8_quantize with D = Dv = DI writes
+ * it): DI OCP E4M3 codes, the row's fp32 scale, zero bytes to a multiple of
+ * 16 (144 bytes at DI = 128).  A row stands for decode(code) * scale, and
+ * the score is the indexer score of those values:
+ *   I[i, s] = sum_j w[i, j] * sq[i, j] * sk[kb + s]
+ *                           * ReLU(codes_q[i, j, :] . codes_k[kb + s, :])
+ * (sq, sk the row scales, positive), with the E4M3 products accumulated in
+ * fp32 by tcgen05 kind::f8f6f4.  Otherwise the same as dsa_indexer_topk:
+ *   q_idx8       FP8 rows [tpr][HI][row_bytes]          (local, split)
+ *   k_idx8       FP8 rows [num_kv_rows][row_bytes]      (full)
+ * Only HI = 64, DI = 128, topk = 2048 is compiled (DSA_ERR_UNSUPPORTED
+ * otherwise).  Same workspace rule, same errors.
+ */
+dsa_status dsa_indexer_topk_fp8(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                int32_t max_kv_len, const void *q_idx8, const void *k_idx8, const float *w,
+                                int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t topk, int32_t *topk_idx,
+                                void *workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/* Test hook: dsa_indexer_scores over FP8 operands (inputs as dsa_indexer_topk_fp8). */
+dsa_status dsa_indexer_scores_fp8(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                  int32_t max_kv_len, const void *q_idx8, const void *k_idx8, const float *w,
+                                  int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t row_begin,
+                                  int32_t row_count, float *scores, dsa_stream_t stream);
+
+/*
  * MLA sparse attention prefill for one CP view ([xLLM] 单层前向数据流 (4):
  * local queries, full latent KV, output [T_local, num_heads_FULL, Dv]).
  * For every local slot i and head h over the valid selected rows J of

@@ -23,7 +23,8 @@ __all__ = [
     "IN_SEQ_SPLIT", "ROUND_ROBIN", "HEAD_TAIL", "DSAError", "CPLocalMetadata", "load",
     "dsa_cp_geometry", "dsa_cp_metadata_sizes", "dsa_cp_build_local_metadata", "dsa_cp_split",
     "dsa_cp_rerange", "dsa_cp_all_to_all_heads", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk",
-    "dsa_indexer_scores", "dsa_sparse_attn_prefill", "dsa_sparse_attn_prefill_headsharded", "dsa_poll_device_error",
+    "dsa_indexer_scores", "dsa_indexer_fp8_rows", "dsa_indexer_topk_fp8", "dsa_indexer_scores_fp8",
+    "dsa_sparse_attn_prefill", "dsa_sparse_attn_prefill_headsharded", "dsa_poll_device_error",
 ]
 
 
@@ -247,6 +248,71 @@ def dsa_indexer_scores(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Te
                                     _ptr(w), k_idx.shape[0], HI, DI, row_begin, row_count, _ptr(out),
                                     _stream(stream)),
           "dsa_indexer_scores")
+    return out
+
+
+def dsa_indexer_fp8_rows(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Index rows bf16 [..., DI] -> FP8 index rows uint8 [..., row_bytes]: the
+    FP8 cache row with D = Dv = DI (E4M3 codes, one fp32 scale, zero padding),
+    written by dsa_kv_fp8_quantize."""
+    _need(x, torch.bfloat16, "x")
+    DI = x.shape[-1]
+    rb = dsa_kv_fp8_row_bytes(DI, DI)
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (rb,), dtype=torch.uint8, device=x.device)
+    _need(out, torch.uint8, "out")
+    if tuple(out.shape) != tuple(x.shape[:-1]) + (rb,):
+        raise ValueError("out must have x's leading shape and FP8 rows")
+    dsa_kv_fp8_quantize(x.reshape(-1, DI), DI, out.view(-1, rb), stream=stream)
+    return out
+
+
+def _fp8_index_shapes(md, q_idx8, k_idx8, w, DI):
+    _need(q_idx8, torch.uint8, "q_idx8")
+    _need(k_idx8, torch.uint8, "k_idx8")
+    _need(w, torch.float32, "w")
+    rb = dsa_kv_fp8_row_bytes(DI, DI)
+    tpr, HI, qrb = q_idx8.shape
+    if qrb != rb or k_idx8.dim() != 2 or k_idx8.shape[1] != rb or tuple(w.shape) != (tpr, HI):
+        raise ValueError("q_idx8 / k_idx8 must be FP8 index rows of DI and w [tpr, HI]")
+    if tpr != md.tokens_per_rank:
+        raise ValueError("q_idx8 rows do not match the view")
+    return tpr, HI
+
+
+def dsa_indexer_topk_fp8(md: CPLocalMetadata, q_idx8: torch.Tensor, k_idx8: torch.Tensor, w: torch.Tensor,
+                         topk: int, max_kv_len: int, DI: int = 128, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q_idx8 uint8 [tpr, HI, row_bytes], k_idx8 uint8 [T, row_bytes] (FP8 index
+    rows, dsa_indexer_fp8_rows), w fp32 [tpr, HI] -> int32 [tpr, topk]."""
+    tpr, HI = _fp8_index_shapes(md, q_idx8, k_idx8, w, DI)
+    if out is None:
+        out = torch.empty((tpr, topk), dtype=torch.int32, device=q_idx8.device)
+    _need(out, torch.int32, "out")
+    if workspace is None:
+        workspace = torch.empty(dsa_indexer_topk_workspace_size(tpr, max_kv_len, topk), dtype=torch.uint8,
+                                device=q_idx8.device)
+    check(load().dsa_indexer_topk_fp8(C.byref(md.struct), md.batch, tpr, max_kv_len, _ptr(q_idx8), _ptr(k_idx8),
+                                      _ptr(w), k_idx8.shape[0], HI, DI, topk, _ptr(out), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+          "dsa_indexer_topk_fp8")
+    return out
+
+
+def dsa_indexer_scores_fp8(md: CPLocalMetadata, q_idx8: torch.Tensor, k_idx8: torch.Tensor, w: torch.Tensor,
+                           max_kv_len: int, DI: int = 128, row_begin: int = 0, row_count: int | None = None,
+                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Test hook: dsa_indexer_scores over FP8 index rows."""
+    tpr, HI = _fp8_index_shapes(md, q_idx8, k_idx8, w, DI)
+    if row_count is None:
+        row_count = tpr - row_begin
+    if out is None:
+        out = torch.empty((row_count, max_kv_len), dtype=torch.float32, device=q_idx8.device)
+    _need(out, torch.float32, "out")
+    check(load().dsa_indexer_scores_fp8(C.byref(md.struct), md.batch, tpr, max_kv_len, _ptr(q_idx8),
+                                        _ptr(k_idx8), _ptr(w), k_idx8.shape[0], HI, DI, row_begin, row_count,
+                                        _ptr(out), _stream(stream)),
+          "dsa_indexer_scores_fp8")
     return out
 
 

@@ -28,27 +28,32 @@
 namespace dsa {
 namespace {
 
-template <int HI_, int DI_>
+template <int HI_, int DI_, bool FP8_ = false>
 struct IdxCfg {
   static constexpr int HI = HI_, DI = DI_;
+  // FP8: q_I and k_I are E4M3 rows with one fp32 scale each (the FP8 cache row
+  // with D = Dv = DI: DI codes, the scale, zero bytes to a multiple of 16)
+  static constexpr bool FP8 = FP8_;
+  static constexpr int kEB = FP8 ? 1 : 2;                // bytes per element
+  static constexpr int kRowBytes = FP8 ? (DI + 4 + 15) / 16 * 16 : DI * 2;  // global row stride
   static constexpr int kTokPerGroup = 256 / HI;          // tokens in one N = 256 MMA
   static constexpr int kTileTok = 2 * kTokPerGroup;      // two TMEM accumulators
   static constexpr int kRowsQ = kTileTok * HI;           // 512 B-operand rows
-  static constexpr int kCW = DI >= 64 ? 64 : DI;         // elements per swizzle row
-  static constexpr int kCWB = kCW * 2;                   // 128 B (SW128) or 64 B (SW64)
+  static constexpr int kCW = DI * kEB >= 128 ? 128 / kEB : DI;  // elements per swizzle row
+  static constexpr int kCWB = kCW * kEB;                 // 128 B (SW128) or 64 B (SW64)
   static constexpr int kNCh = DI / kCW;
   static constexpr uint32_t kLayout = kCWB == 128 ? kLayoutSW128 : kLayoutSW64;
   static constexpr uint32_t kSBO = 8 * kCWB;             // 8-row swizzle atom
   static constexpr int kBK = 128;                        // keys per block (M)
-  static constexpr int kStages = DI >= 128 ? 2 : 4;
+  static constexpr int kStages = FP8 || DI < 128 ? 4 : 2;
   static constexpr int kQBytes = kNCh * kRowsQ * kCWB;
   static constexpr int kKStageBytes = kNCh * kBK * kCWB;
-  static constexpr int kKSteps = DI / 16;
-  static constexpr int kStepsPerChunk = kCW / 16;
+  static constexpr int kKSteps = DI * kEB / 32;          // MMA K steps of 32 bytes (16 bf16 or 32 E4M3)
+  static constexpr int kStepsPerChunk = kCWB / 32;
   static constexpr int kKeyChunk = 2048;                 // keys per CTA (smallest; see key_chunk)
   static constexpr int kTokPerHalf = kTokPerGroup / 2;   // tokens per epilogue half
   static constexpr int kThreads = 320;                   // 0 TMA, 1 MMA, 2..9 epilogue
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  static constexpr uint32_t kIdesc = FP8 ? idesc_e4m3(128, 256) : idesc_bf16(128, 256, false, false);
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
@@ -63,11 +68,14 @@ struct IdxCfg {
   static_assert(HI * kTokPerGroup == 256, "HI must divide 256");
   static_assert(kTokPerGroup % 2 == 0, "two epilogue halves");
   static_assert((128 / HI) * HI == 128, "an epilogue half covers 128 columns");
+  static_assert(!FP8 || DI == 128, "FP8 rows: one 128-code scale tile");
 };
 
 struct IdxParams {
   dsa_cp_local_metadata md;
   const float *w;      // [tpr][HI]
+  const uint8_t *q8;   // FP8 only: q_I rows [tpr * HI][kRowBytes] (their scales)
+  const uint8_t *k8;   // FP8 only: k_I rows [num_kv_rows][kRowBytes]
   float *scores;       // [rows][ld]
   int64_t ld;          // score row stride (floats)
   int32_t tpr, row_begin, row_end, max_kv_len, num_kv_rows;
@@ -132,9 +140,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       misc[3] = 1;
     }
   }
+  // head weights; with FP8 operands each carries its query row's scale
+  // (ReLU(a * x) = a * ReLU(x) for a scale a > 0)
   for (int i = tid; i < C::kTileTok * C::HI; i += C::kThreads) {
     const int slot = slot0 + i / C::HI;
-    w_s[i] = slot < P.row_end ? P.w[static_cast<int64_t>(slot) * C::HI + (i % C::HI)] : 0.f;
+    float wv = 0.f;
+    if (slot < P.row_end) {
+      const int64_t r = static_cast<int64_t>(slot) * C::HI + (i % C::HI);
+      wv = P.w[r];
+      if constexpr (C::FP8) wv *= *reinterpret_cast<const float *>(P.q8 + r * C::kRowBytes + C::DI);
+    }
+    w_s[i] = wv;
   }
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -206,7 +222,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                          C::kSBO, C::kLayout);
             const uint64_t b = smem_desc(q_addr + ch * C::kRowsQ * C::kCWB + g * 256 * C::kCWB + sub * 32, 16,
                                          C::kSBO, C::kLayout);
-            mma_ss(tmem + g * 256, a, b, C::kIdesc, k > 0 ? 1u : 0u);
+            if constexpr (C::FP8) mma_ss_f8(tmem + g * 256, a, b, C::kIdesc, k > 0 ? 1u : 0u);
+            else mma_ss(tmem + g * 256, a, b, C::kIdesc, k > 0 ? 1u : 0u);
           }
           mma_commit(&t_full[g]);
         }
@@ -221,6 +238,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
       for (int j = 0; j < nblk; ++j) {
         const int key = kstart + j * C::kBK + row_in_blk;
+        // FP8: the key row's scale multiplies the whole head sum
+        float kscale = 1.f;
+        if constexpr (C::FP8)
+          kscale = key < P.num_kv_rows ? *reinterpret_cast<const float *>(P.k8 + static_cast<int64_t>(key) * C::kRowBytes + C::DI)
+                                       : 0.f;
         bool ok = true;
         for (int g = 0; g < 2; ++g) {
           // tcgen05.ld is warp-collective: keep the exit decision warp-uniform
@@ -253,6 +275,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             float lo, hi;
             f2_unpack(acc2[u], lo, hi);
             acc[u] = lo + hi;
+            if constexpr (C::FP8) acc[u] *= kscale;
           }
           tc_fence_before();
           mbar_arrive(&t_empty[g]);
@@ -466,14 +489,16 @@ template <class C>
 dsa_status make_maps(const void *q_idx, const void *k_idx, int32_t tpr, int32_t num_kv_rows, CUtensorMap *qmap,
                      CUtensorMap *kmap) {
   const CUtensorMapSwizzle sw = C::kCWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapDataType dt = C::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // the rows' DI elements; the FP8 row's scale and padding lie beyond them in the stride
   uint64_t qdims[2] = {static_cast<uint64_t>(C::DI), static_cast<uint64_t>(tpr) * C::HI};
-  uint64_t qstr[1] = {static_cast<uint64_t>(C::DI) * 2};
+  uint64_t qstr[1] = {static_cast<uint64_t>(C::kRowBytes)};
   uint32_t qbox[2] = {static_cast<uint32_t>(C::kCW), 256};
-  dsa_status st = encode_tensor_map(qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_idx, qdims, qstr, qbox, sw);
+  dsa_status st = encode_tensor_map(qmap, dt, 2, q_idx, qdims, qstr, qbox, sw);
   if (st != DSA_OK) return st;
   uint64_t kdims[2] = {static_cast<uint64_t>(C::DI), static_cast<uint64_t>(num_kv_rows)};
   uint32_t kbox[2] = {static_cast<uint32_t>(C::kCW), 128};
-  return encode_tensor_map(kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k_idx, kdims, qstr, kbox, sw);
+  return encode_tensor_map(kmap, dt, 2, k_idx, kdims, qstr, kbox, sw);
 }
 
 template <class C>
@@ -519,6 +544,7 @@ dsa_status validate(const Args &a) {
 
 using BigIdx = IdxCfg<64, 128>;
 using TinyIdx = IdxCfg<4, 32>;
+using BigIdx8 = IdxCfg<64, 128, true>;
 
 template <class C>
 dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *out, int64_t ld,
@@ -528,7 +554,8 @@ dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *
   if (st != DSA_OK) return st;
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
-  IdxParams P{*a.md, a.w, out, ld, a.tpr, row_begin, row_end, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, err};
+  IdxParams P{*a.md, a.w, static_cast<const uint8_t *>(a.q_idx), static_cast<const uint8_t *>(a.k_idx), out, ld,
+              a.tpr, row_begin, row_end, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, err};
   return launch_indexer<C>(qmap, kmap, P, stream);
 }
 
@@ -566,8 +593,8 @@ dsa_status run_topk(const Args &a, int32_t *topk_idx, void *ws, size_t ws_bytes,
   float *scores = static_cast<float *>(ws);
   for (int64_t r0 = 0; r0 < a.tpr; r0 += rows_fit) {
     const int32_t r1 = static_cast<int32_t>(r0 + rows_fit < a.tpr ? r0 + rows_fit : a.tpr);
-    IdxParams P{*a.md, a.w, scores, ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows,
-                C::kKeyChunk, err};
+    IdxParams P{*a.md, a.w, static_cast<const uint8_t *>(a.q_idx), static_cast<const uint8_t *>(a.k_idx), scores,
+                ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, err};
     st = launch_indexer<C>(qmap, kmap, P, stream);
     if (st != DSA_OK) return st;
     st = launch_topk<TOPK>(*a.md, static_cast<int32_t>(r0), r1 - static_cast<int32_t>(r0), a.max_kv_len, scores, ld,
@@ -596,20 +623,62 @@ extern "C" dsa_status dsa_indexer_topk_workspace_size(int32_t tokens_per_rank, i
   return DSA_OK;
 }
 
+namespace dsa {
+namespace {
+
+// The bf16 and FP8 entry points share validation and dispatch.
+dsa_status indexer_topk_entry(bool fp8, const Args &a, int32_t topk, int32_t *topk_idx, void *workspace,
+                              size_t ws_bytes, cudaStream_t s) {
+  dsa_status st = validate(a);
+  if (st != DSA_OK) return st;
+  if (!topk_idx || !workspace || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+  if (a.tpr == 0) return DSA_OK;
+  const bool big = a.HI == 64 && a.DI == 128 && topk == 2048, tiny = a.HI == 4 && a.DI == 32 && topk == 64;
+  if (fp8) return big ? run_topk<BigIdx8, 2048>(a, topk_idx, workspace, ws_bytes, s) : DSA_ERR_UNSUPPORTED;
+  if (big) return run_topk<BigIdx, 2048>(a, topk_idx, workspace, ws_bytes, s);
+  if (tiny) return run_topk<TinyIdx, 64>(a, topk_idx, workspace, ws_bytes, s);
+  return DSA_ERR_UNSUPPORTED;
+}
+
+dsa_status indexer_scores_entry(bool fp8, const Args &a, int32_t row_begin, int32_t row_count, float *scores,
+                                cudaStream_t s) {
+  dsa_status st = validate(a);
+  if (st != DSA_OK) return st;
+  if (!scores) return DSA_ERR_INVALID_ARG;
+  if (row_begin < 0 || row_count < 0 || static_cast<int64_t>(row_begin) + row_count > a.tpr) return DSA_ERR_SHAPE;
+  if (row_count == 0) return DSA_OK;
+  const bool big = a.HI == 64 && a.DI == 128, tiny = a.HI == 4 && a.DI == 32;
+  if (fp8 ? !big : !(big || tiny)) return DSA_ERR_UNSUPPORTED;
+  const int64_t n = static_cast<int64_t>(row_count) * a.max_kv_len;
+  fill_kernel<<<static_cast<unsigned>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, s>>>(
+      scores, n, -__builtin_huge_valf());
+  st = check_launch();
+  if (st != DSA_OK) return st;
+  const int32_t row_end = row_begin + row_count;
+  if (fp8) return run_scores<BigIdx8>(a, row_begin, row_end, scores, a.max_kv_len, s);
+  return big ? run_scores<BigIdx>(a, row_begin, row_end, scores, a.max_kv_len, s)
+             : run_scores<TinyIdx>(a, row_begin, row_end, scores, a.max_kv_len, s);
+}
+
+}  // namespace
+}  // namespace dsa
+
 extern "C" dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
                                        int32_t max_kv_len, const void *q_idx, const void *k_idx, const float *w,
                                        int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t topk,
                                        int32_t *topk_idx, void *workspace, size_t ws_bytes,
                                        dsa_stream_t stream) {
   Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx, k_idx, w};
-  dsa_status st = validate(a);
-  if (st != DSA_OK) return st;
-  if (!topk_idx || !workspace || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
-  if (tpr == 0) return DSA_OK;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (HI == 64 && DI == 128 && topk == 2048) return run_topk<BigIdx, 2048>(a, topk_idx, workspace, ws_bytes, s);
-  if (HI == 4 && DI == 32 && topk == 64) return run_topk<TinyIdx, 64>(a, topk_idx, workspace, ws_bytes, s);
-  return DSA_ERR_UNSUPPORTED;
+  return indexer_topk_entry(false, a, topk, topk_idx, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsa_status dsa_indexer_topk_fp8(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                           int32_t max_kv_len, const void *q_idx8, const void *k_idx8,
+                                           const float *w, int32_t num_kv_rows, int32_t HI, int32_t DI,
+                                           int32_t topk, int32_t *topk_idx, void *workspace, size_t ws_bytes,
+                                           dsa_stream_t stream) {
+  Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx8, k_idx8, w};
+  return indexer_topk_entry(true, a, topk, topk_idx, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
@@ -617,21 +686,16 @@ extern "C" dsa_status dsa_indexer_scores(const dsa_cp_local_metadata *md, int32_
                                          int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t row_begin,
                                          int32_t row_count, float *scores, dsa_stream_t stream) {
   Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx, k_idx, w};
-  dsa_status st = validate(a);
-  if (st != DSA_OK) return st;
-  if (!scores) return DSA_ERR_INVALID_ARG;
-  if (row_begin < 0 || row_count < 0 || static_cast<int64_t>(row_begin) + row_count > tpr) return DSA_ERR_SHAPE;
-  if (row_count == 0) return DSA_OK;
-  const bool big = HI == 64 && DI == 128, tiny = HI == 4 && DI == 32;
-  if (!big && !tiny) return DSA_ERR_UNSUPPORTED;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t n = static_cast<int64_t>(row_count) * max_kv_len;
-  fill_kernel<<<static_cast<unsigned>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, s>>>(
-      scores, n, -__builtin_huge_valf());
-  st = check_launch();
-  if (st != DSA_OK) return st;
-  return big ? run_scores<BigIdx>(a, row_begin, row_begin + row_count, scores, max_kv_len, s)
-             : run_scores<TinyIdx>(a, row_begin, row_begin + row_count, scores, max_kv_len, s);
+  return indexer_scores_entry(false, a, row_begin, row_count, scores, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsa_status dsa_indexer_scores_fp8(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                             int32_t max_kv_len, const void *q_idx8, const void *k_idx8,
+                                             const float *w, int32_t num_kv_rows, int32_t HI, int32_t DI,
+                                             int32_t row_begin, int32_t row_count, float *scores,
+                                             dsa_stream_t stream) {
+  Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx8, k_idx8, w};
+  return indexer_scores_entry(true, a, row_begin, row_count, scores, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ no-allocation variant

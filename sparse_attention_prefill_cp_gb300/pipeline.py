@@ -21,15 +21,16 @@ from __future__ import annotations
 import torch
 
 from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_metadata, dsa_cp_geometry,
-               dsa_cp_rerange, dsa_cp_split, dsa_indexer_topk, dsa_indexer_topk_workspace_size,
-               dsa_kv_fp8_dequantize, dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_flat,
+               dsa_cp_rerange, dsa_cp_split, dsa_indexer_topk, dsa_indexer_topk_fp8,
+               dsa_indexer_topk_workspace_size, dsa_kv_fp8_dequantize, dsa_kv_fp8_row_bytes, dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_flat,
                dsa_sparse_attn_prefill_headsharded)
 
 
 class DSAPrefill:
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
                  softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1,
-                 prefix_lens=None, kv_fp8: bool = False, fused: bool = False, compress_ratio: int = 1):
+                 prefix_lens=None, kv_fp8: bool = False, fused: bool = False, compress_ratio: int = 1,
+                 index_fp8: bool = False):
         """``lengths``: query tokens per request.  ``prefix_lens`` (chunked
         prefill): KV positions per request that precede its queries; the KV
         and index-key tensors passed to ``run`` then hold every request's
@@ -41,7 +42,10 @@ class DSAPrefill:
         writes its rows of ``out`` in place (dsa_sparse_attn_prefill_flat),
         with the same results.  ``compress_ratio`` c: the latent KV and index
         keys passed to ``run`` are compressed entries, floor(seq_len / c) per
-        request in request order (dsa_cp_build_local_metadata_compressed)."""
+        request in request order (dsa_cp_build_local_metadata_compressed).
+        ``index_fp8``: q_idx and k_idx passed to ``run`` are FP8 index rows
+        (uint8 [T, HI, row_bytes] and [R, row_bytes], dsa_indexer_fp8_rows)
+        and the indexer runs on them (dsa_indexer_topk_fp8)."""
         self.device = torch.device(device or "cuda")
         self.lengths = [int(x) for x in lengths]
         self.prefix_lens = [0] * len(self.lengths) if prefix_lens is None else [int(x) for x in prefix_lens]
@@ -70,7 +74,11 @@ class DSAPrefill:
         self.fused = bool(fused)
         self._q_split = None    # [cp][tpr][H][D] and [cp][tpr][H][Dv], allocated on
         self._out_split = None  # first use (never by the fused path)
-        self.qi_split = torch.empty((cp, tpr, HI, DI), dtype=torch.bfloat16, device=dev)
+        self.index_fp8 = bool(index_fp8)
+        if self.index_fp8:
+            self.qi_split = torch.empty((cp, tpr, HI, dsa_kv_fp8_row_bytes(DI, DI)), dtype=torch.uint8, device=dev)
+        else:
+            self.qi_split = torch.empty((cp, tpr, HI, DI), dtype=torch.bfloat16, device=dev)
         self.w_split = torch.empty((cp, tpr, HI), dtype=torch.float32, device=dev)
         self.topk_idx = torch.empty((cp, tpr, topk), dtype=torch.int32, device=dev)
         self.out = torch.empty((self.T, H, Dv), dtype=torch.bfloat16, device=dev)
@@ -124,9 +132,17 @@ class DSAPrefill:
         dsa_cp_split(q_idx, self.cp_size, self.mode, -1, self.qi_split, stream)
         dsa_cp_split(w, self.cp_size, self.mode, -1, self.w_split, stream)
 
+    def indexer(self, r: int, k_idx, stream=None, workspace=None):     # a3 + a4
+        ws = self.workspace if workspace is None else workspace
+        if self.index_fp8:
+            dsa_indexer_topk_fp8(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
+                                 self.DI, self.topk_idx[r], ws, stream)
+        else:
+            dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
+                             self.topk_idx[r], ws, stream)
+
     def view(self, r: int, kv, k_idx, sink=None, stream=None, workspace=None):  # a3 + a4 + a5
-        dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
-                         self.topk_idx[r], self.workspace if workspace is None else workspace, stream)
+        self.indexer(r, k_idx, stream, workspace)
         st = stream or torch.cuda.current_stream(self.device)
         ev = self.attention_events
         if ev is not None:
@@ -226,8 +242,7 @@ class DSAPrefill:
             dsa_cp_split(q, self.cp_size, self.mode, -1, self.q_split, stream)
         kv = self.latent_kv(kv, stream)
         for r in range(self.cp_size):
-            dsa_indexer_topk(self.md[r], self.qi_split[r], k_idx, self.w_split[r], self.topk, self.max_kv_len,
-                             self.topk_idx[r], self.workspace, stream)
+            self.indexer(r, k_idx, stream)
             dsa_sparse_attn_prefill_headsharded(self.md[r], self.q_split[r], kv, self.topk_idx[r], self.scale,
                                                 self.Dv, self.cp_size, out, sink, stream)
         return out

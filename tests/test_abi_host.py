@@ -136,3 +136,22 @@ def test_flat_attention_and_fp8_cache_validation(lib):
     assert lib.dsa_kv_fp8_quantize(p, 0, 576, 512, p, None) == 0
     assert lib.dsa_kv_fp8_dequantize(p, 4, 576, 512, None, None) == 1
     assert lib.dsa_kv_fp8_dequantize(p, 0, 64, 48, p, None) == 0
+
+
+def test_fp8_indexer_validation(lib):
+    md = _lib.LocalMetadata()
+    assert lib.dsa_cp_metadata_bind(C.c_void_p(0x10000), 1, 16, 2, C.byref(md)) == 0
+    p, odd = C.c_void_p(0x10000), C.c_void_p(0x10008)
+    # null / misaligned operands, then dimension sets without an FP8 build (tiny shapes, other topk)
+    assert lib.dsa_indexer_topk_fp8(C.byref(md), 1, 8, 16, None, p, p, 16, 64, 128, 2048, p, p, 1 << 20, None) == 1
+    assert lib.dsa_indexer_topk_fp8(C.byref(md), 1, 8, 16, odd, p, p, 16, 64, 128, 2048, p, p, 1 << 20, None) == 1
+    assert lib.dsa_indexer_topk_fp8(C.byref(md), 1, 8, 16, p, p, p, 16, 4, 32, 64, p, p, 1 << 20, None) == 3
+    assert lib.dsa_indexer_topk_fp8(C.byref(md), 1, 8, 16, p, p, p, 16, 64, 128, 1024, p, p, 1 << 20, None) == 3
+    assert lib.dsa_indexer_topk_fp8(C.byref(md), 1, 0, 16, p, p, p, 16, 64, 128, 2048, p, p, 1 << 20, None) == 0
+    assert lib.dsa_indexer_scores_fp8(C.byref(md), 1, 8, 16, p, p, p, 16, 4, 32, 0, 8, p, None) == 3
+    assert lib.dsa_indexer_scores_fp8(C.byref(md), 1, 8, 16, p, p, p, 16, 64, 128, 4, 8, p, None) == 2
+    assert lib.dsa_indexer_scores_fp8(C.byref(md), 1, 8, 16, p, p, None, 16, 64, 128, 0, 8, p, None) == 1
+    # the FP8 index row is the FP8 cache row with D = Dv = DI
+    n = C.c_size_t()
+    assert lib.dsa_kv_fp8_row_bytes(128, 128, C.byref(n)) == 0 and n.value == 144 == O.kv_fp8_row_bytes(128, 128)
+

@@ -658,3 +658,140 @@ def test_full_size_sampled_rows(wl, mode):
         check_attention(out[g].cpu().float().numpy(), ref)
         assert torch.equal(out[g], pipe.out_split[r, i])
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------------ FP8 indexer operands
+
+def _exact_fp8_rows(vals: np.ndarray, scales: np.ndarray) -> torch.Tensor:
+    """FP8 index rows [R, row_bytes] of values that are exact E4M3 numbers (codes
+    by torch's float8_e4m3fn conversion) and the given fp32 row scales."""
+    R, DI = vals.shape
+    out = torch.zeros((R, dsa.dsa_kv_fp8_row_bytes(DI, DI)), dtype=torch.uint8)
+    out[:, :DI] = torch.from_numpy(vals.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    out[:, DI:DI + 4] = torch.from_numpy(scales.astype(np.float32).copy()).view(torch.uint8).reshape(R, 4)
+    return out
+
+
+def _fp8_index_inputs(wl, x):
+    """(q8 [T, HI, rb], k8 [R, rb]) on the GPU.  Integer workloads: their small
+    integers as exact codes with power-of-two row scales 2^-2 .. 2^2, so every
+    score stays exact in fp32.  Float workloads: the GPU quantiser's rows
+    (checked bit-exact against the oracle's by test_index_fp8_rows_bit_exact)."""
+    T, HI, DI = x["q_idx"].shape
+    if wl.integer:
+        rng = np.random.default_rng(wl.seed + 100)
+        qv = x["q_idx"].float().numpy().reshape(T * HI, DI)
+        kv = x["k_idx"].float().numpy()
+        q8 = _exact_fp8_rows(qv, np.exp2(rng.integers(-2, 3, T * HI).astype(np.float64))).reshape(T, HI, -1)
+        k8 = _exact_fp8_rows(kv, np.exp2(rng.integers(-2, 3, kv.shape[0]).astype(np.float64)))
+        return q8.cuda(), k8.cuda()
+    return dsa.dsa_indexer_fp8_rows(x["q_idx"].cuda()), dsa.dsa_indexer_fp8_rows(x["k_idx"].cuda())
+
+
+def test_index_fp8_rows_bit_exact():
+    x = draw_inputs(FLOAT_FULL)
+    for name in ("q_idx", "k_idx"):
+        got = dsa.dsa_indexer_fp8_rows(x[name].cuda()).cpu().numpy()
+        ref = O.kv_fp8_quantize(x[name].float().numpy().reshape(-1, FLOAT_FULL.DI), FLOAT_FULL.DI)
+        assert np.array_equal(got.reshape(ref.shape), ref), name
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("wl", [INT_FULL, FLOAT_FULL], ids=lambda w: w.name)
+def test_indexer_fp8_scores(wl, mode):
+    x = draw_inputs(wl)
+    q8, k8 = _fp8_index_inputs(wl, x)
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      index_fp8=True)
+    pipe.metadata()
+    pipe.split(x["q"].cuda(), q8, x["w"].cuda())
+    q8_all, k8_h = q8.cpu().numpy(), k8.cpu().numpy()
+    rng = np.random.default_rng(2)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
+        scores = dsa.dsa_indexer_scores_fp8(pipe.md[r], pipe.qi_split[r], k8, pipe.w_split[r], pipe.max_kv_len,
+                                            wl.DI)
+        dsa.dsa_poll_device_error()
+        sc = scores.cpu().numpy().astype(np.float64)
+        q8_loc = O.split(q8_all, wl.cp_size, mode)[r]
+        w_loc = O.split(f64(x["w"]), wl.cp_size, mode)[r]
+        slots = sorted(set(rng.choice(pipe.tpr, 150, replace=False)) | {0, pipe.tpr - 1})
+        for i in slots:
+            g = md["local_token_pos"][i]
+            if g < 0:
+                assert np.all(np.isneginf(sc[i]))
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            p = g - md["local_req_pos_base"][j]
+            ref = O.indexer_scores_fp8(q8_loc[i], w_loc[i], k8_h[base:base + p + 1], wl.DI)
+            got = sc[i, :p + 1]
+            if wl.integer:
+                assert np.array_equal(got, ref), (r, i)
+            else:
+                tol = SCORE_TOL * max(1e-30, np.abs(ref).max())
+                assert np.abs(got - ref).max() <= tol, (r, i, np.abs(got - ref).max(), tol)
+            assert np.all(np.isneginf(sc[i, p + 1:]))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("wl", [INT_FULL, FLOAT_FULL], ids=lambda w: w.name)
+def test_topk_fp8_and_whole_path(wl, mode):
+    # top-k over FP8 index rows: bit-exact sets on the integer variant, the
+    # float property otherwise; the attention over the selected rows within
+    # the attention bar; bf16 and FP8 paths agree where the FP8 rows are exact
+    x = draw_inputs(wl)
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    q8, k8 = _fp8_index_inputs(wl, x)
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      index_fp8=True, fused=True)
+    out = pipe.run(xd["q"], xd["kv"], q8, k8, xd["w"], xd["sink"]).clone()
+    dsa.dsa_poll_device_error()
+    idx = pipe.topk_idx.cpu().numpy()
+    q8_all, k8_h = q8.cpu().numpy(), k8.cpu().numpy()
+    kv = f64(x["kv"])
+    sink = None if x["sink"] is None else f64(x["sink"])
+    rng = np.random.default_rng(3)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
+        q8_loc = O.split(q8_all, wl.cp_size, mode)[r]
+        w_loc = O.split(f64(x["w"]), wl.cp_size, mode)[r]
+        slots = sorted(set(rng.choice(pipe.tpr, 100, replace=False)) | {0, pipe.tpr - 1})
+        for n_att, i in enumerate(slots):
+            g = md["local_token_pos"][i]
+            if g < 0:
+                assert np.all(idx[r, i] == -1)
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            p = g - md["local_req_pos_base"][j]
+            ref = O.indexer_scores_fp8(q8_loc[i], w_loc[i], k8_h[base:base + p + 1], wl.DI)
+            check_topk_row(idx[r, i], ref, base, wl.topk, exact=wl.integer)
+            if n_att < 12:
+                sel = idx[r, i][idx[r, i] >= 0]
+                check_attention(out[g].cpu().double().numpy(),
+                                O.sparse_attention(f64(x["q"][g]), kv[sel], wl.scale, wl.Dv, sink))
+
+
+def test_fp8_index_rows_at_full_size_sampled():
+    # 1 x 8192, cp 8 in-seq: the GPU quantiser's rows through the FP8 indexer;
+    # sampled rows against the oracle on the oracle's own quantised rows
+    wl, mode = LONG_8K, IN_SEQ_SPLIT
+    xd = _device_inputs(wl)
+    q8, k8 = dsa.dsa_indexer_fp8_rows(xd["q_idx"]), dsa.dsa_indexer_fp8_rows(xd["k_idx"])
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      index_fp8=True, fused=True)
+    pipe.run(xd["q"], xd["kv"], q8, k8, xd["w"], xd["sink"])
+    dsa.dsa_poll_device_error()
+    k8_ref = O.kv_fp8_quantize(xd["k_idx"].float().cpu().numpy(), wl.DI)
+    assert np.array_equal(k8.cpu().numpy(), k8_ref)
+    md_all = [O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
+              for r in range(wl.cp_size)]
+    rows = sample_rows(wl.num_tokens, 20, seed=5, must=[0, wl.topk - 1, wl.topk, wl.num_tokens - 1])
+    for g in rows:
+        g = int(g)
+        r = next(rr for rr in range(wl.cp_size) if g in md_all[rr]["local_token_pos"])
+        i = md_all[r]["local_token_pos"].index(g)
+        q8_ref = O.kv_fp8_quantize(xd["q_idx"][g].float().cpu().numpy(), wl.DI)
+        ref = O.indexer_scores_fp8(q8_ref, f64(xd["w"][g]), k8_ref[:g + 1], wl.DI)
+        check_topk_row(pipe.topk_idx[r, i].cpu().numpy(), ref, 0, wl.topk, exact=False)
