@@ -16,10 +16,11 @@
 // Scores (fp32) go to a workspace row per query, indexed by in-request key
 // position.
 //
-// topk_kernel (one CTA per query row): 4-pass 8-bit radix select of the
-// topk-th largest score (scores mapped to order-preserving uint32 keys, -0
-// folded into +0), then a block-scan compaction in ascending key order that
-// takes every score above the threshold and the lowest-index ties.
+// topk_kernel (one CTA per query row): radix select of the topk-th largest
+// score in three digits (11, 11, 10 bits of order-preserving uint32 keys, -0
+// folded into +0), the last two over the short list of keys that share the
+// threshold's first digit, then a block-scan compaction in ascending key
+// order that takes every score above the threshold and the lowest-index ties.
 #include <mutex>
 
 #include "dsa_common.cuh"
@@ -339,15 +340,32 @@ __device__ __forceinline__ void scan2(int a, int b, int &ea, int &eb, int &ta, i
   eb = pb + ib - b;
 }
 
-// CACHE: the row's order keys are kept in shared memory (dynamic, n words)
-// after the first pass, so the row is read from L2 once instead of five times.
-template <int TOPK, bool CACHE>
+// Radix select in three digits of the order key: bits 31..21 (2048 bins),
+// 20..10 (2048) and 9..0 (1024).  The first digit is counted while the row
+// is read; when the bin that holds the topk-th largest key has at most
+// kCandMax keys, they are collected and the last two digits are counted over
+// that short list only, otherwise over the whole row (keys whose higher
+// digits match).  Then one compaction pass in ascending key order takes every
+// key above the threshold and the lowest-index keys equal to it (one block
+// scan per chunk when every equal key is taken, the common case for float
+// scores; two otherwise).  The first cache_words keys of the row stay in
+// shared memory after the first pass; the rest of a longer row is read again
+// from global memory by the later passes.
+constexpr int kBins = 2048;
+constexpr int kCandMax = 4096;
+constexpr int kTopkFixedWords = kBins + kCandMax;  // dynamic shared memory before the key cache
+
+template <int TOPK>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_metadata md, int32_t row_begin,
                                                             int32_t max_kv_len, const float *__restrict__ scores,
-                                                            int64_t ld, int32_t *__restrict__ topk_idx, int *err) {
-  __shared__ uint32_t hist[256];
+                                                            int64_t ld, int32_t *__restrict__ topk_idx,
+                                                            int32_t cache_words, int *err) {
+  extern __shared__ uint32_t dyn_smem[];
+  uint32_t *hist = dyn_smem;               // [kBins]
+  uint32_t *cand = dyn_smem + kBins;       // [kCandMax]
+  uint32_t *s_keys = cand + kCandMax;      // [cache_words]
   __shared__ int2 warp_tot[kTopkThreads / 32];
-  __shared__ int s_base, s_p, s_digit, s_krem;
+  __shared__ int s_base, s_p, s_digit, s_krem, s_cnt, s_ncand;
   const int tid = threadIdx.x;
   const int slot = row_begin + blockIdx.x;
   int32_t *out = topk_idx + static_cast<int64_t>(slot) * TOPK;
@@ -368,7 +386,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     }
     s_base = base;
     s_p = p;
+    s_ncand = 0;
   }
+  for (int i = tid; i < kBins; i += kTopkThreads) hist[i] = 0;
   __syncthreads();
   const int base = s_base, n = s_p + 1;
   if (n <= TOPK) {  // pad slot or short row: every causal key, then -1
@@ -376,93 +396,145 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     return;
   }
   const float *row = scores + static_cast<int64_t>(blockIdx.x) * ld;
-  extern __shared__ uint32_t s_keys[];  // CACHE: [n] order keys
-  auto key_at = [&](int i) -> uint32_t { return CACHE ? s_keys[i] : order_key(row[i]); };
-
-  uint32_t prefix = 0, mask = 0;
-  int krem = TOPK;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-    if (CACHE && pass == 0) {
-      // first pass: read the row (16-byte loads; rows start 16-byte aligned), keep its keys
-      for (int i = tid * 4; i < n; i += kTopkThreads * 4) {
-        if (i + 3 < n) {
-          const float4 v = *reinterpret_cast<const float4 *>(row + i);
-          const uint32_t k4[4] = {order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w)};
-          *reinterpret_cast<uint4 *>(s_keys + i) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+  // cached: a multiple of 4 (cache_words is), so a 4-key group is wholly
+  // cached or wholly in global memory; rows start 16-byte aligned
+  const int cached = min(n, cache_words) & ~3;
+  // keys i .. i + 3 (i a multiple of 4); keys at or past n read as 0
+  auto keys4_at = [&](int i, uint32_t (&k4)[4]) {
+    if (i + 3 < cached) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(s_keys + i);
+      k4[0] = v.x, k4[1] = v.y, k4[2] = v.z, k4[3] = v.w;
+    } else if (i + 3 < n) {
+      const float4 v = *reinterpret_cast<const float4 *>(row + i);
+      k4[0] = order_key(v.x), k4[1] = order_key(v.y), k4[2] = order_key(v.z), k4[3] = order_key(v.w);
+    } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) atomicAdd(&hist[k4[k] >> 24], 1u);
-        } else {
-          for (int k = i; k < n; ++k) {
-            const uint32_t key = order_key(row[k]);
-            s_keys[k] = key;
-            atomicAdd(&hist[key >> 24], 1u);
-          }
-        }
+      for (int k = 0; k < 4; ++k) k4[k] = i + k < n ? order_key(row[i + k]) : 0u;
+    }
+  };
+
+  // pass 1: read the row, cache its first keys, count the first digit; each
+  // thread has kLoads 16-byte loads in flight before it uses any
+  constexpr int kLoads = 4;
+  for (int i0 = tid * 4; i0 < n; i0 += kTopkThreads * 4 * kLoads) {
+    float4 v[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = i0 + u * kTopkThreads * 4;
+      if (i + 3 < n) v[u] = *reinterpret_cast<const float4 *>(row + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = i0 + u * kTopkThreads * 4;
+      if (i >= n) break;
+      uint32_t k4[4];
+      if (i + 3 < n) {
+        k4[0] = order_key(v[u].x), k4[1] = order_key(v[u].y), k4[2] = order_key(v[u].z), k4[3] = order_key(v[u].w);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) k4[k] = i + k < n ? order_key(row[i + k]) : 0u;
+      }
+      if (i + 3 < cached) *reinterpret_cast<uint4 *>(s_keys + i) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (i + k < n) atomicAdd(&hist[k4[k] >> 21], 1u);
+    }
+  }
+  __syncthreads();
+
+  // the digit (of nbins, counted in hist) holding the krem-th largest key:
+  // each thread sums nbins / 512 consecutive bins from the top, one block scan
+  int krem = TOPK;
+  auto find_digit = [&](int nbins) {
+    const int per = nbins / kTopkThreads;
+    int local = 0;
+    for (int k = 0; k < per; ++k) local += static_cast<int>(hist[nbins - 1 - (tid * per + k)]);
+    int cum, dummy, tot, tot2;
+    scan2(local, 0, cum, dummy, tot, tot2, warp_tot);
+    for (int k = 0; k < per; ++k) {
+      const int c = static_cast<int>(hist[nbins - 1 - (tid * per + k)]);
+      if (cum < krem && cum + c >= krem) {
+        s_digit = nbins - 1 - (tid * per + k);
+        s_krem = krem - cum;
+        s_cnt = c;
+      }
+      cum += c;
+    }
+    __syncthreads();
+    krem = s_krem;
+  };
+  find_digit(kBins);
+  uint32_t prefix = static_cast<uint32_t>(s_digit) << 21, mask = 0xFFE00000u;
+  const bool use_cand = s_cnt <= kCandMax;
+  if (use_cand) {  // pass 2: the keys of that bin
+    for (int i = tid * 4; i < n; i += kTopkThreads * 4) {
+      uint32_t k4[4];
+      keys4_at(i, k4);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (i + k < n && (k4[k] & mask) == prefix) cand[atomicAdd(&s_ncand, 1)] = k4[k];
+    }
+  }
+  // digits 2 and 3 over the candidates (or the whole row)
+#pragma unroll
+  for (int d = 0; d < 2; ++d) {
+    const int shift = d == 0 ? 10 : 0, nbins = d == 0 ? 2048 : 1024;
+    __syncthreads();  // candidates complete, previous digit read
+    for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    if (use_cand) {
+      const int nc = s_ncand;
+      for (int i = tid; i < nc; i += kTopkThreads) {
+        const uint32_t key = cand[i];
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
       }
     } else {
-      for (int i = tid; i < n; i += kTopkThreads) {
-        const uint32_t key = key_at(i);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      for (int i = tid * 4; i < n; i += kTopkThreads * 4) {
+        uint32_t k4[4];
+        keys4_at(i, k4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (i + k < n && (k4[k] & mask) == prefix) atomicAdd(&hist[(k4[k] >> shift) & (nbins - 1)], 1u);
       }
     }
     __syncthreads();
-    if (tid < 32) {
-      // warp 0 finds the digit holding the krem-th largest key: suffix sums over 8 digits per lane
-      uint32_t local[8], sum = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        local[k] = hist[255 - (tid * 8 + k)];
-        sum += local[k];
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, off);
-        if (tid >= off) incl += x;
-      }
-      uint32_t cum = incl - sum;  // count of keys in higher digits than this lane's first
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (cum < static_cast<uint32_t>(krem) && cum + local[k] >= static_cast<uint32_t>(krem)) {
-          s_digit = 255 - (tid * 8 + k);
-          s_krem = krem - static_cast<int>(cum);
-        }
-        cum += local[k];
-      }
-    }
-    __syncthreads();
+    find_digit(nbins);
     prefix |= static_cast<uint32_t>(s_digit) << shift;
-    mask |= 255u << shift;
-    krem = s_krem;
-    __syncthreads();
+    mask |= static_cast<uint32_t>(nbins - 1) << shift;
   }
-  // prefix is the threshold key; take every key above it and the first krem equal ones
+  // prefix is the threshold key; s_cnt keys equal it, krem of them are taken
   const uint32_t thr = prefix;
+  const bool take_all_eq = s_cnt == krem;
   int run_sel = 0, run_eq = 0;
   for (int t0 = 0; t0 < n; t0 += kTopkThreads * 4) {
     const int i0 = t0 + tid * 4;
     uint32_t keys[4];
-    int c_eq = 0;
+    keys4_at(i0 < n ? i0 : n, keys);  // past the end: all invalid below
+    int sel[4], c_sel = 0;
+    int e_sel, t_sel, e_dummy, t_dummy;
+    if (take_all_eq) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      keys[k] = (i0 + k < n) ? key_at(i0 + k) : 0u;
-      c_eq += (i0 + k < n && keys[k] == thr);
-    }
-    int e_eq, e_dummy, t_eq, t_dummy;
-    scan2(c_eq, 0, e_eq, e_dummy, t_eq, t_dummy, warp_tot);
-    int sel[4], c_sel = 0, r_eq = run_eq + e_eq;
+      for (int k = 0; k < 4; ++k) {
+        sel[k] = i0 + k < n && keys[k] >= thr;
+        c_sel += sel[k];
+      }
+    } else {
+      int c_eq = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const bool valid = i0 + k < n;
-      const bool eq = valid && keys[k] == thr;
-      sel[k] = valid && (keys[k] > thr || (eq && r_eq < krem));
-      r_eq += eq;
-      c_sel += sel[k];
+      for (int k = 0; k < 4; ++k) c_eq += (i0 + k < n && keys[k] == thr);
+      int e_eq, t_eq;
+      scan2(c_eq, 0, e_eq, e_dummy, t_eq, t_dummy, warp_tot);
+      int r_eq = run_eq + e_eq;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool valid = i0 + k < n;
+        const bool eq = valid && keys[k] == thr;
+        sel[k] = valid && (keys[k] > thr || (eq && r_eq < krem));
+        r_eq += eq;
+        c_sel += sel[k];
+      }
+      run_eq += t_eq;
     }
-    int e_sel, t_sel;
     scan2(c_sel, 0, e_sel, e_dummy, t_sel, t_dummy, warp_tot);
     int pos = run_sel + e_sel;
 #pragma unroll
@@ -474,7 +546,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
       }
     }
     run_sel += t_sel;
-    run_eq += t_eq;
   }
 }
 
@@ -559,23 +630,22 @@ dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *
   return launch_indexer<C>(qmap, kmap, P, stream);
 }
 
-// Rows of up to kTopkCacheMax bytes of scores keep their keys in shared memory.
-constexpr int64_t kTopkCacheMax = 160 * 1024;
+// Dynamic shared memory of one top-k CTA at most: the histogram, the
+// candidate list and up to 22,016 cached keys of the row.  Two CTAs then fit
+// on an SM even for long rows; measured on 64K-token rows, two CTAs with the
+// shorter cache beat one CTA caching 45K keys by 8 %.
+constexpr int64_t kTopkSmemMax = 110 * 1024;
 
 template <int TOPK>
 dsa_status launch_topk(const dsa_cp_local_metadata &md, int32_t row_begin, int32_t rows, int32_t max_kv_len,
                        const float *scores, int64_t ld, int32_t *topk_idx, int *err, cudaStream_t stream) {
-  const int64_t cache_bytes = ld * 4;
-  if (cache_bytes <= kTopkCacheMax) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<TOPK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(cache_bytes));
-    if (e != cudaSuccess) return cuda_fail(e);
-    topk_kernel<TOPK, true><<<static_cast<unsigned>(rows), kTopkThreads, static_cast<size_t>(cache_bytes), stream>>>(
-        md, row_begin, max_kv_len, scores, ld, topk_idx, err);
-  } else {
-    topk_kernel<TOPK, false><<<static_cast<unsigned>(rows), kTopkThreads, 0, stream>>>(md, row_begin, max_kv_len,
-                                                                                        scores, ld, topk_idx, err);
-  }
+  const int64_t cap = kTopkSmemMax / 4 - kTopkFixedWords;
+  const int32_t cache_words = static_cast<int32_t>(ld < cap ? ld : cap);
+  const int smem = (kTopkFixedWords + cache_words) * 4;
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<TOPK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  topk_kernel<TOPK><<<static_cast<unsigned>(rows), kTopkThreads, static_cast<size_t>(smem), stream>>>(
+      md, row_begin, max_kv_len, scores, ld, topk_idx, cache_words, err);
   return check_launch();
 }
 
