@@ -465,6 +465,23 @@ def run_ours(args, wl, mode, rank, world):
             pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
 
         aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
+        # FP8 index rows: q_I and k_I quantised (HBM passes, bytes read +
+        # written), and the a3-a5 core with the indexer over them beside the
+        # same core over bf16 index rows, timed the same way
+        q8, k8 = dsa.dsa_indexer_fp8_rows(x["q_idx"]), dsa.dsa_indexer_fp8_rows(x["k_idx"])
+        idx8_bytes = x["q_idx"].numel() * 2 + q8.numel() + x["k_idx"].numel() * 2 + k8.numel()
+        ms = timed(lambda: (dsa.dsa_indexer_fp8_rows(x["q_idx"], q8), dsa.dsa_indexer_fp8_rows(x["k_idx"], k8)))
+        aux["index_fp8_quantize"] = {"ms": ms, "bytes": idx8_bytes, "gbs": idx8_bytes / (ms / 1e3) / 1e9,
+                                     "frac_hbm": idx8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+        p8 = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
+                        view_streams=args.view_streams, fused=True, index_fp8=True)
+        p8.run(x["q"], x["kv"], q8, k8, x["w"], x["sink"])
+        aux["a3_a5_fp8index_ms"] = timed(lambda: p8.views(x["kv"], k8, x["sink"], torch.cuda.current_stream()),
+                                         reps=3)
+        pipe._q = x["q"]
+        aux["a3_a5_bf16index_ms"] = timed(lambda: pipe.views(x["kv"], x["k_idx"], x["sink"],
+                                                             torch.cuda.current_stream()), reps=3)
+        del p8
 
         def unfused_step():  # the whole step with the split of q and the rerange as passes of their own
             pipe.fused = False
@@ -480,7 +497,9 @@ def run_ours(args, wl, mode, rank, world):
                        "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
                        "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own; "
                        "a1_metadata_ms: every view's metadata (one launch per view); "
-                       "a3_a5_compressed_c*: metadata + core over compressed KV at ratio c (T / c entries)")
+                       "a3_a5_compressed_c*: metadata + core over compressed KV at ratio c (T / c entries); "
+                       "index_fp8_quantize: q_I and k_I to FP8 index rows; a3_a5_fp8index_ms / a3_a5_bf16index_ms: "
+                       "the core with the indexer over FP8 / bf16 index rows")
         dsa.dsa_poll_device_error()
 
     launches = pipe.launches_per_step() * args.steps
