@@ -256,18 +256,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int u = 0; u < C::kTokPerHalf; ++u) acc2[u] = 0;  // +0.0f pairs
           const int tok0 = g * C::kTokPerGroup + half * C::kTokPerHalf;
-          const float2 *wrow2 = reinterpret_cast<const float2 *>(w_s + tok0 * C::HI);
+          // the weights of 4 consecutive columns per 16-byte shared-memory load (a broadcast)
+          const float4 *wrow4 = reinterpret_cast<const float4 *>(w_s + tok0 * C::HI);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t r[32];
             tmem_ld32(lane_base + g * 256 + half * 128 + c4 * 32, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
+            for (int c = 0; c < 32; c += 4) {
               const int col = c4 * 32 + c;
-              const float2 wv = wrow2[col >> 1];
+              const float4 wv = wrow4[col >> 2];
               acc2[col / C::HI] = f2_fma(f2_pack(fmaxf(__uint_as_float(r[c]), 0.f), fmaxf(__uint_as_float(r[c + 1]), 0.f)),
                                          f2_pack(wv.x, wv.y), acc2[col / C::HI]);
+              acc2[col / C::HI] = f2_fma(f2_pack(fmaxf(__uint_as_float(r[c + 2]), 0.f), fmaxf(__uint_as_float(r[c + 3]), 0.f)),
+                                         f2_pack(wv.z, wv.w), acc2[col / C::HI]);
             }
           }
           float acc[C::kTokPerHalf];
@@ -348,7 +351,7 @@ __device__ __forceinline__ void scan2(int a, int b, int &ea, int &eb, int &ta, i
 // digits match).  Then one compaction pass in ascending key order takes every
 // key above the threshold and the lowest-index keys equal to it (one block
 // scan per chunk when every equal key is taken, the common case for float
-// scores; two otherwise).  The first cache_words keys of the row stay in
+// scores; two otherwise; 4096 keys per chunk).  The first cache_words keys of the row stay in
 // shared memory after the first pass; the rest of a longer row is read again
 // from global memory by the later passes.
 constexpr int kBins = 2048;
@@ -506,27 +509,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
   const uint32_t thr = prefix;
   const bool take_all_eq = s_cnt == krem;
   int run_sel = 0, run_eq = 0;
-  for (int t0 = 0; t0 < n; t0 += kTopkThreads * 4) {
-    const int i0 = t0 + tid * 4;
-    uint32_t keys[4];
-    keys4_at(i0 < n ? i0 : n, keys);  // past the end: all invalid below
-    int sel[4], c_sel = 0;
+  constexpr int kPer = 8;  // keys per thread and chunk
+  for (int t0 = 0; t0 < n; t0 += kTopkThreads * kPer) {
+    const int i0 = t0 + tid * kPer;
+    uint32_t keys[kPer];
+    keys4_at(i0 < n ? i0 : n, *reinterpret_cast<uint32_t(*)[4]>(keys));  // past the end: all invalid below
+    keys4_at(i0 + 4 < n ? i0 + 4 : n, *reinterpret_cast<uint32_t(*)[4]>(keys + 4));
+    int sel[kPer], c_sel = 0;
     int e_sel, t_sel, e_dummy, t_dummy;
     if (take_all_eq) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kPer; ++k) {
         sel[k] = i0 + k < n && keys[k] >= thr;
         c_sel += sel[k];
       }
     } else {
       int c_eq = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) c_eq += (i0 + k < n && keys[k] == thr);
+      for (int k = 0; k < kPer; ++k) c_eq += (i0 + k < n && keys[k] == thr);
       int e_eq, t_eq;
       scan2(c_eq, 0, e_eq, e_dummy, t_eq, t_dummy, warp_tot);
       int r_eq = run_eq + e_eq;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kPer; ++k) {
         const bool valid = i0 + k < n;
         const bool eq = valid && keys[k] == thr;
         sel[k] = valid && (keys[k] > thr || (eq && r_eq < krem));
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
     scan2(c_sel, 0, e_sel, e_dummy, t_sel, t_dummy, warp_tot);
     int pos = run_sel + e_sel;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kPer; ++k) {
       if (sel[k]) {
         if (pos < TOPK) out[pos] = base + i0 + k;
         else record_error(err, DSA_ERR_DEVICE_BOUNDS, 43, slot);
