@@ -6,15 +6,18 @@
 // 单层前向数据流 (2)(3) and 4. Indexer full/local 分离), then the topk
 // largest I[t,s] over s <= t with ties to the lower s.
 //
-// indexer_kernel (tcgen05, one CTA per 2 x (256/HI) local queries and up to
-// 2048 keys): the key block (128 keys) is the MMA's M side, the query tile's
+// indexer_kernel (tcgen05, one CTA per 2 x (256/HI) local queries and a chunk
+// of 2048, 4096 or 8192 keys chosen per launch): the key block (128 keys) is
+// the MMA's M side, the query tile's
 // (token, head) rows are N = 256, the indexer dim is K.  Each TMEM lane is
 // then one key holding every head of a token in its own columns, so the
 // weighted-ReLU head sum is a per-thread loop.  Two TMEM accumulators of
 // 256 columns alternate between the two token groups so the epilogue of one
 // overlaps the MMA of the other.  K tiles arrive by TMA (128B swizzle).
 // Scores (fp32) go to a workspace row per query, indexed by in-request key
-// position.
+// position.  FP8 operands (IdxCfg<..., true>): E4M3 index rows with one fp32
+// scale each, tcgen05.mma kind::f8f6f4; the query rows' scales fold into the
+// head weights and each key's scale multiplies its head sums.
 //
 // topk_kernel (one CTA per query row): radix select of the topk-th largest
 // score in three digits (11, 11, 10 bits of order-preserving uint32 keys, -0

@@ -795,3 +795,33 @@ def test_fp8_index_rows_at_full_size_sampled():
         q8_ref = O.kv_fp8_quantize(xd["q_idx"][g].float().cpu().numpy(), wl.DI)
         ref = O.indexer_scores_fp8(q8_ref, f64(xd["w"][g]), k8_ref[:g + 1], wl.DI)
         check_topk_row(pipe.topk_idx[r, i].cpu().numpy(), ref, 0, wl.topk, exact=False)
+
+
+def test_topk_dense_bin_and_ties_bit_exact():
+    # every score in one first-digit bin of the top-k's radix select (more than
+    # its 4096-key candidate list holds), with heavy ties: q_I all ones, k_I in
+    # {1, 2} (about 10 % ones), w all ones -> I = 64 * (sum of k_I) in
+    # [12288, 16384), integers, exact in fp32; rows of up to 12,000 keys. The
+    # selected sets (ties to the lower index) must be the oracle's, bit-exact.
+    wl = LONG_8K.with_(name="dense-bin", lengths=(12000,), cp_size=2, modes=(ROUND_ROBIN,))
+    T, HI, DI = wl.num_tokens, wl.HI, wl.DI
+    gen = torch.Generator().manual_seed(17)
+    q_idx = torch.ones(T, HI, DI, dtype=torch.bfloat16)
+    k_idx = (1 + (torch.rand(T, DI, generator=gen) >= 0.1).float()).to(torch.bfloat16)
+    w = torch.ones(T, HI, dtype=torch.float32)
+    ks = k_idx.float().sum(1)
+    assert ks.min() >= 192 and ks.max() < 256  # one exponent, top two mantissa bits fixed or nearly
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, ROUND_ROBIN, wl.H, wl.D, wl.Dv, HI, DI, wl.topk, wl.scale)
+    pipe.metadata()
+    pipe.split(torch.zeros(T, wl.H, wl.D, dtype=torch.bfloat16, device="cuda"), q_idx.cuda(), w.cuda())
+    for r in range(wl.cp_size):
+        pipe.indexer(r, k_idx.cuda())
+    dsa.dsa_poll_device_error()
+    idx = pipe.topk_idx.cpu().numpy()
+    kf = f64(k_idx)
+    rows = sample_rows(T, 24, seed=6, must=[wl.topk, wl.topk + 1, 4200, 8191, 8192, T - 2, T - 1])
+    for g in rows:
+        g = int(g)
+        r, i = g % wl.cp_size, g // wl.cp_size
+        ref = O.indexer_scores(np.ones((HI, DI)), np.ones(HI), kf[:g + 1])
+        check_topk_row(idx[r, i], ref, 0, wl.topk, exact=True)
