@@ -8,8 +8,8 @@
 //
 // indexer_kernel (tcgen05, one CTA per 2 x (256/HI) local queries and a chunk
 // of 2048, 4096 or 8192 keys chosen per launch): the key block (128 keys) is
-// the MMA's M side, the query tile's
-// (token, head) rows are N = 256, the indexer dim is K.  Each TMEM lane is
+// the MMA's M side, the query tile's (token, head) rows are N = 256, the
+// indexer dim is K.  Each TMEM lane is
 // then one key holding every head of a token in its own columns, so the
 // weighted-ReLU head sum is a per-thread loop.  Two TMEM accumulators of
 // 256 columns alternate between the two token groups so the epilogue of one
