@@ -825,3 +825,47 @@ def test_topk_dense_bin_and_ties_bit_exact():
         r, i = g % wl.cp_size, g // wl.cp_size
         ref = O.indexer_scores(np.ones((HI, DI)), np.ones(HI), kf[:g + 1])
         check_topk_row(idx[r, i], ref, 0, wl.topk, exact=True)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("kind", ["chunked", "compressed"])
+def test_fp8_index_rows_with_prefix_and_compressed_kv(kind, mode):
+    # the FP8 indexer over the other geometries: a chunked batch (prefix KV) and
+    # compressed entries at c = 4; integer variant with power-of-two row scales,
+    # so the selected sets must be the oracle's, bit-exact
+    wl = INT_FULL.with_(name="int-fp8-" + kind, lengths=(4600, 900))
+    x = draw_inputs(wl)
+    if kind == "chunked":
+        prefixes, c = (3000, 200), 1
+        xc, q_lens, seq_lens = chunk_inputs(x, wl.lengths, prefixes)
+        x = dict(xc)
+    else:
+        prefixes, c = None, 4
+        q_lens, seq_lens = list(wl.lengths), list(wl.lengths)
+        R = sum(n // c for n in wl.lengths)
+        x["k_idx"], x["kv"] = x["k_idx"][:R].contiguous(), x["kv"][:R].contiguous()
+    q8, k8 = _fp8_index_inputs(wl, x)
+    pipe = DSAPrefill(q_lens, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      prefix_lens=prefixes, compress_ratio=c, index_fp8=True, fused=True)
+    pipe.run(x["q"].cuda(), x["kv"].cuda(), q8, k8, x["w"].cuda(), None)
+    dsa.dsa_poll_device_error()
+    idx = pipe.topk_idx.cpu().numpy()
+    q8_all, k8_h = q8.cpu().numpy(), k8.cpu().numpy()
+    rng = np.random.default_rng(8)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(qsl_of(q_lens), seq_lens, wl.cp_size, r, mode, compress_ratio=c)
+        q8_loc = O.split(q8_all, wl.cp_size, mode)[r]
+        w_loc = O.split(f64(x["w"]), wl.cp_size, mode)[r]
+        for i in sorted(set(rng.choice(pipe.tpr, 60, replace=False)) | {0, pipe.tpr - 1}):
+            g = md["local_token_pos"][i]
+            if g < 0:
+                assert np.all(idx[r, i] == -1)
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            n = (g - md["local_req_pos_base"][j] + 1) // c
+            if n == 0:
+                assert np.all(idx[r, i] == -1)
+                continue
+            ref = O.indexer_scores_fp8(q8_loc[i], w_loc[i], k8_h[base:base + n], wl.DI)
+            check_topk_row(idx[r, i], ref, base, wl.topk, exact=True)
