@@ -55,8 +55,13 @@ struct IdxCfg {
   static constexpr int kKSteps = DI * kEB / 32;          // MMA K steps of 32 bytes (16 bf16 or 32 E4M3)
   static constexpr int kStepsPerChunk = kCWB / 32;
   static constexpr int kKeyChunk = 2048;                 // keys per CTA (smallest; see key_chunk)
-  static constexpr int kTokPerHalf = kTokPerGroup / 2;   // tokens per epilogue half
-  static constexpr int kThreads = 320;                   // 0 TMA, 1 MMA, 2..9 epilogue
+  // epilogue: kEpiParts warps per TMEM lane quarter, each taking 256 / kEpiParts
+  // columns (kTokPerPart tokens) of an accumulator
+  static constexpr int kEpiParts = 4;
+  static constexpr int kEpiWarps = 4 * kEpiParts;
+  static constexpr int kColsPerPart = 256 / kEpiParts;
+  static constexpr int kTokPerPart = kTokPerGroup / kEpiParts;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;   // warp 0 TMA, 1 MMA, 2.. epilogue
   static constexpr uint32_t kIdesc = FP8 ? idesc_e4m3(128, 256) : idesc_bf16(128, 256, false, false);
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kOffQ = 0;
@@ -70,8 +75,8 @@ struct IdxCfg {
   // every CTA allocates all 512 TMEM columns: ask for enough smem to keep one CTA per SM
   static constexpr int kSmemBytes = kSmemUsed < 120 * 1024 ? 120 * 1024 : kSmemUsed;
   static_assert(HI * kTokPerGroup == 256, "HI must divide 256");
-  static_assert(kTokPerGroup % 2 == 0, "two epilogue halves");
-  static_assert((128 / HI) * HI == 128, "an epilogue half covers 128 columns");
+  static_assert(kTokPerGroup % kEpiParts == 0 && kTokPerPart * HI == kColsPerPart, "whole tokens per part");
+  static_assert(kColsPerPart % 32 == 0, "32-column TMEM loads");
   static_assert(!FP8 || DI == 128, "FP8 rows: one 128-code scale tile");
 };
 
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&t_full[b], 1);
-      mbar_init(&t_empty[b], 256);
+      mbar_init(&t_empty[b], 32 * C::kEpiWarps);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_wait(mma_done, 0, P.err, 17);
     } else if (warp >= 2) {
       // ---------------- epilogue: one TMEM lane (= one key) per thread
-      const int quad = warp & 3, half = (warp - 2) >> 2;
+      const int quad = warp & 3, part = (warp - 2) >> 2;
       const int row_in_blk = quad * 32 + lane;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
       for (int j = 0; j < nblk; ++j) {
@@ -255,16 +260,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_after();
           // per token, even and odd heads accumulate in the two halves of a
           // packed fp32 pair (fma.rn.f32x2), summed at the end
-          uint64_t acc2[C::kTokPerHalf];
+          uint64_t acc2[C::kTokPerPart];
 #pragma unroll
-          for (int u = 0; u < C::kTokPerHalf; ++u) acc2[u] = 0;  // +0.0f pairs
-          const int tok0 = g * C::kTokPerGroup + half * C::kTokPerHalf;
+          for (int u = 0; u < C::kTokPerPart; ++u) acc2[u] = 0;  // +0.0f pairs
+          const int tok0 = g * C::kTokPerGroup + part * C::kTokPerPart;
           // the weights of 4 consecutive columns per 16-byte shared-memory load (a broadcast)
           const float4 *wrow4 = reinterpret_cast<const float4 *>(w_s + tok0 * C::HI);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c4 = 0; c4 < C::kColsPerPart / 32; ++c4) {
             uint32_t r[32];
-            tmem_ld32(lane_base + g * 256 + half * 128 + c4 * 32, r);
+            tmem_ld32(lane_base + g * 256 + part * C::kColsPerPart + c4 * 32, r);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
@@ -276,9 +281,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                          f2_pack(wv.z, wv.w), acc2[col / C::HI]);
             }
           }
-          float acc[C::kTokPerHalf];
+          float acc[C::kTokPerPart];
 #pragma unroll
-          for (int u = 0; u < C::kTokPerHalf; ++u) {
+          for (int u = 0; u < C::kTokPerPart; ++u) {
             float lo, hi;
             f2_unpack(acc2[u], lo, hi);
             acc[u] = lo + hi;
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_before();
           mbar_arrive(&t_empty[g]);
 #pragma unroll
-          for (int u = 0; u < C::kTokPerHalf; ++u) {
+          for (int u = 0; u < C::kTokPerPart; ++u) {
             const int t = tok0 + u;
             const int ks = key - s_base[t];
             if (ks >= 0 && ks <= s_p[t])
