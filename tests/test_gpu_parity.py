@@ -625,6 +625,16 @@ def _device_inputs(wl):
 def test_full_size_sampled_rows(wl, mode):
     xd = _device_inputs(wl)
     pipe, out = run_pipeline(wl, mode, xd)
+    if wl is LONG_8K and mode == IN_SEQ_SPLIT:
+        # the launch configuration the bench times (fused split / rerange, views on
+        # two streams) gives the same bits as the plain path checked below
+        bench_cfg = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                               fused=True, view_streams=2)
+        bench_cfg.out.fill_(float("nan"))
+        got = bench_cfg.run(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"])
+        dsa.dsa_poll_device_error()
+        assert torch.equal(got, out) and torch.equal(bench_cfg.topk_idx, pipe.topk_idx)
+        del bench_cfg, got
     md_all = [O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
               for r in range(wl.cp_size)]
     for r in range(wl.cp_size):
