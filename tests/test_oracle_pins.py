@@ -553,7 +553,9 @@ def test_indexer_fp8_closed_form_row_scales():
     # so I[s] = DI b_s sum_j w_j a_j (all dots positive).  A scale read from the
     # wrong row or operand, or a dropped scale, breaks it.
     HI, DI, n = 3, 128, 5
-    a = np.array([0.5, 2.0, 0.125], dtype=np.float32)
+    # 1 + 2^-10 has more significant bits than bf16: values decode(code) * scale
+    # are taken exactly, so rounding them to bf16 would also break the form
+    a = np.array([0.5, 2.0, 1 + 2.0 ** -10], dtype=np.float32)
     b = np.array([1.0, 0.25, 4.0, 3.0, 0.75], dtype=np.float32)
     def rows(scales):
         r = np.zeros((len(scales), O.kv_fp8_row_bytes(DI, DI)), dtype=np.uint8)
