@@ -76,6 +76,16 @@ design notes):
       entries.  Entries of all requests are stored in request order.  A query
       that sees no entry selects nothing and its output is zero.  c = 1 is
       the uncompressed path.
+  R15 sliding window (SWA; [xLLM] 背景 names it beside the compressed KV, and
+      单层前向数据流 (4) gives the attention the original KV's geometry,
+      cu_seqlens_ori_kv / seqused_kv, besides the sparse selection; nothing
+      says how the two combine).  Reading taken: a query at position p also
+      attends to the original (uncompressed) latent rows of its own request
+      at positions max(0, p - W + 1) .. p, and one softmax covers the selected
+      entries and those window rows together; at c = 1 the entries are the
+      original rows and a row both selected and in the window counts once.
+      The original rows are every request's whole sequence in request order
+      (R9).  W = 0 is the plain sparse path.
   R14 FP8 indexer operands (the FP8 path of [blog] 1 applied to the index
       query and keys; the pages fix no format): each DI-wide index row (a key
       k_I[s], or one head q_I[t, j]) is stored like an R12 cache row with
@@ -579,3 +589,61 @@ def indexer_scores_fp8(q_idx_row8, w_row, k_idx_keys8, DI: int) -> np.ndarray:
     for: q_idx_row8 [HI, row_bytes] (one query's heads), k_idx_keys8
     [n, row_bytes] -> fp64 [n]."""
     return indexer_scores(index_fp8_values(q_idx_row8, DI), w_row, index_fp8_values(k_idx_keys8, DI))
+
+
+# --------------------------------------------------------------------------
+# Sliding window over the original KV (R15)
+# --------------------------------------------------------------------------
+
+def window_rows(p: int, ori_start: int, window: int) -> np.ndarray:
+    """Original KV rows of the positions max(0, p - W + 1) .. p of a request
+    whose position 0 is original row ori_start (none for W = 0)."""
+    if window <= 0:
+        return np.zeros(0, dtype=np.int64)
+    return np.arange(ori_start + max(0, p - window + 1), ori_start + p + 1, dtype=np.int64)
+
+
+def view_row_swa(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int, scale: float, Dv: int,
+                 window: int, kv_ori, ori_starts, sink=None):
+    """One local slot with the sliding window (R15): the selection of view_row
+    over the (compressed) rows ``kv``, plus the window rows of ``kv_ori``
+    (the original rows; request b starts at ori_starts[b]), one softmax over
+    both.  Returns (selected rows, window rows, output fp64 [H, Dv]); (None,
+    None, zeros) for a pad slot."""
+    sel, _, _ = view_row(md, slot, q_loc, q_idx_loc, w_loc, kv, k_idx, topk, scale, Dv, sink)
+    H = np.asarray(q_loc[slot]).shape[0]
+    if sel is None:
+        return None, None, np.zeros((H, Dv))
+    j = request_of_slot(md, slot)
+    p = md["local_token_pos"][slot] - md["local_req_pos_base"][j]
+    win = window_rows(p, ori_starts[md["local_req_id"][j]], window)
+    if md.get("compress_ratio", 1) == 1:  # the same rows: their union
+        rows = np.asarray(kv)[np.union1d(sel, win)]
+    else:
+        rows = np.concatenate([np.asarray(kv)[sel], np.asarray(kv_ori)[win]])
+    if rows.shape[0] == 0:
+        return sel, win, np.zeros((H, Dv))
+    return sel, win, sparse_attention(q_loc[slot], rows, scale, Dv, sink)
+
+
+def prefill_swa(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mode: int, topk: int,
+                scale: float, Dv: int, window: int, kv_ori=None, sink=None, compress_ratio: int = 1):
+    """prefill with the sliding window (R15): ``kv`` / ``k_idx`` are the rows
+    the indexer selects from (compressed entries at compress_ratio > 1),
+    ``kv_ori`` the original rows of every request's whole sequence (``kv``
+    itself when omitted, as at c = 1).  Returns out [T, H, Dv] fp64."""
+    q = np.asarray(q, dtype=np.float64)
+    q_idx = np.asarray(q_idx, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    kv_ori = kv if kv_ori is None else kv_ori
+    ori_starts = np.concatenate([[0], np.cumsum(seq_lens)]).astype(np.int64)
+    T = q.shape[0]
+    qs, qis, ws = split(q, cp_size, mode), split(q_idx, cp_size, mode), split(w, cp_size, mode)
+    _, tpr = padded_geometry(T, cp_size)
+    outs = np.zeros((cp_size, tpr, q.shape[1], Dv))
+    for r in range(cp_size):
+        md = build_local_metadata(query_start_loc, seq_lens, cp_size, r, mode, compress_ratio)
+        for i in range(tpr):
+            _, _, outs[r, i] = view_row_swa(md, i, qs[r], qis[r], ws[r], kv, k_idx, topk, scale, Dv, window,
+                                            kv_ori, ori_starts, sink)
+    return rerange(outs, T, cp_size, mode)

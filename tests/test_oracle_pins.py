@@ -675,3 +675,114 @@ def test_compressed_metadata_extents(mode):
             widest[b] = max(widest[b], md["local_seq_lens"][j])
             assert md["local_req_kv_base"][j] == sum(n // c for n in seq_lens[:b])
     assert widest == [n // c for n in seq_lens]
+
+
+# ---------------------------------------------------------------- sliding window (R15)
+# A query at position p also attends to the original rows of positions
+# max(0, p - W + 1) .. p; one softmax over the selected entries and the window
+# rows (a row both selected and in the window counts once at c = 1).
+
+def test_swa_hand_example():
+    # 1 request of 3 tokens, H = 1, D = Dv = 1, q = 1, latent rows [1], [2], [3],
+    # scale 1 (logit = row value); index keys 3, 2, 1 with q_I = w = 1 -> scores
+    # 3, 2, 1: the top-1 is always key 0.  Window W = 2:
+    #   p = 0: {0}             -> out = 1
+    #   p = 1: {0} u {0, 1}    -> (1 e + 2 e^2) / (e + e^2) = (1 + 2e) / (1 + e)
+    #          (counting key 0 twice would give (2 + 2e) / (2 + e) instead)
+    #   p = 2: {0} u {1, 2}    -> (e + 2 e^2 + 3 e^3) / (e + e^2 + e^3)
+    e = math.e
+    q, kv = np.ones((3, 1, 1)), np.array([[1.0], [2.0], [3.0]])
+    qi, ki, w = np.ones((3, 1, 1)), np.array([[3.0], [2.0], [1.0]]), np.ones((3, 1))
+    out = O.prefill_swa(q, kv, qi, ki, w, [0, 3], [3], 1, O.IN_SEQ_SPLIT, topk=1, scale=1.0, Dv=1, window=2)
+    expect = [1.0, (1 + 2 * e) / (1 + e), (e + 2 * e ** 2 + 3 * e ** 3) / (e + e ** 2 + e ** 3)]
+    assert np.allclose(out[:, 0, 0], expect, rtol=1e-15, atol=0)
+    assert not np.isclose(out[1, 0, 0], (2 + 2 * e) / (2 + e))
+
+
+def _swa_case(c, seed=17, prefixes=(0, 0)):
+    """Queries of two requests (lengths 19, 26) after the given prefixes; the
+    original rows hold the whole sequences, the entries floor(seq_len / c)
+    rows per request (the original rows themselves at c = 1)."""
+    rng = np.random.default_rng(seed)
+    H, D, Dv, HI, DI = 3, 10, 6, 2, 4
+    lens = [19, 26]
+    seq = [n + p for n, p in zip(lens, prefixes)]
+    ents = [n // c for n in seq]
+    T, S, R = sum(lens), sum(seq), sum(ents)
+    x = dict(q=rng.standard_normal((T, H, D)), kv_ori=rng.standard_normal((S, D)),
+             qi=rng.standard_normal((T, HI, DI)), w=rng.standard_normal((T, HI)), sink=rng.standard_normal(H))
+    x["kv"] = x["kv_ori"] if c == 1 else rng.standard_normal((R, D))
+    x["ki"] = rng.standard_normal((S if c == 1 else R, DI))
+    return x, lens, seq, ents, (H, D, Dv)
+
+
+@pytest.mark.parametrize("c", [1, 4])
+@pytest.mark.parametrize("mode", [O.IN_SEQ_SPLIT, O.ROUND_ROBIN, O.HEAD_TAIL])
+def test_swa_window_zero_is_the_sparse_path(c, mode):
+    x, lens, _, _, (H, D, Dv) = _swa_case(c)
+    qsl = _qsl(lens)
+    a = O.prefill_swa(x["q"], x["kv"], x["qi"], x["ki"], x["w"], qsl, lens, 3, mode, topk=5, scale=0.3, Dv=Dv,
+                      window=0, kv_ori=x["kv_ori"], sink=x["sink"], compress_ratio=c)
+    b = O.prefill(x["q"], x["kv"], x["qi"], x["ki"], x["w"], qsl, lens, 3, mode, topk=5, scale=0.3, Dv=Dv,
+                  sink=x["sink"], compress_ratio=c)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("prefixes", [(0, 0), (6, 3)])
+@pytest.mark.parametrize("c,window", [(1, 4), (4, 3), (4, 7)])
+@pytest.mark.parametrize("mode", [O.IN_SEQ_SPLIT, O.ROUND_ROBIN])
+def test_swa_is_masked_dense_attention(c, window, mode, prefixes):
+    # against torch's fp64 scaled_dot_product_attention over all candidate rows
+    # (the compressed entries, then the original rows) with the mask "selected
+    # entry, or original position in the window"; the selection is the plain
+    # path's (view_row), the sink an extra key of zero value; with a prefix the
+    # original rows of request b start at the sum of the earlier seq_lens
+    x, lens, seq, ents, (H, D, Dv) = _swa_case(c, seed=23, prefixes=prefixes)
+    qsl, topk, scale = _qsl(lens), 5, 0.3
+    out = O.prefill_swa(x["q"], x["kv"], x["qi"], x["ki"], x["w"], qsl, seq, 2, mode, topk=topk, scale=scale,
+                        Dv=Dv, window=window, kv_ori=x["kv_ori"], sink=x["sink"], compress_ratio=c)
+    for r in range(2):
+        md = O.build_local_metadata(qsl, seq, 2, r, mode, compress_ratio=c)
+        qs, qis, ws = (O.split(x[k], 2, mode)[r] for k in ("q", "qi", "w"))
+        for i, g in enumerate(md["local_token_pos"]):
+            if g < 0:
+                continue
+            sel, _, _ = O.view_row(md, i, qs, qis, ws, x["kv"], x["ki"], topk, scale, Dv, x["sink"])
+            b = 0 if g < lens[0] else 1
+            p = prefixes[b] + g - qsl[b]
+            ent0, ori0 = sum(ents[:b]), sum(seq[:b])
+            if c == 1:
+                keys = x["kv_ori"][ori0: ori0 + p + 1]
+                allowed = np.zeros(p + 1, dtype=bool)
+                allowed[sel - ori0] = True
+                allowed[max(0, p - window + 1):] = True
+            else:
+                keys = np.concatenate([x["kv"][ent0: ent0 + ents[b]], x["kv_ori"][ori0: ori0 + p + 1]])
+                allowed = np.zeros(keys.shape[0], dtype=bool)
+                allowed[sel - ent0] = True
+                allowed[ents[b] + max(0, p - window + 1):] = True
+            qt = torch.from_numpy(x["q"][g])[None, :, None, :]
+            k = torch.from_numpy(keys)[None, None].expand(1, H, len(keys), D)
+            v = torch.from_numpy(keys[:, :Dv])[None, None].expand(1, H, len(keys), Dv)
+            mask = torch.where(torch.from_numpy(allowed), 0.0, -math.inf).to(torch.float64)
+            mask = mask[None, None, None].expand(1, H, 1, len(keys))
+            k = torch.cat([k, torch.zeros(1, H, 1, D, dtype=torch.float64)], dim=2)
+            v = torch.cat([v, torch.zeros(1, H, 1, Dv, dtype=torch.float64)], dim=2)
+            mask = torch.cat([mask, torch.from_numpy(x["sink"])[None, :, None, None]], dim=3)
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, k, v, attn_mask=mask, scale=scale)
+            assert np.allclose(out[g], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-12), (r, i)
+
+
+def test_swa_full_window_is_dense_causal():
+    # c = 1 and a window as long as the request: every causal key, whatever the
+    # selection -- torch's causal attention
+    x, lens, _, _, (H, D, Dv) = _swa_case(1, seed=29)
+    qsl = _qsl(lens)
+    out = O.prefill_swa(x["q"], x["kv"], x["qi"], x["ki"], x["w"], qsl, lens, 4, O.ROUND_ROBIN, topk=2,
+                        scale=0.3, Dv=Dv, window=max(lens))
+    for b in range(2):
+        qb = torch.from_numpy(x["q"][qsl[b]: qsl[b + 1]]).permute(1, 0, 2)[None]          # [1,H,n,D]
+        kb = torch.from_numpy(x["kv"][qsl[b]: qsl[b + 1]])[None, None].expand(1, H, lens[b], D)
+        vb = torch.from_numpy(x["kv"][qsl[b]: qsl[b + 1], :Dv])[None, None].expand(1, H, lens[b], Dv)
+        ref = torch.nn.functional.scaled_dot_product_attention(qb, kb, vb, is_causal=True, scale=0.3)
+        assert np.allclose(out[qsl[b]: qsl[b + 1]], ref[0].permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
