@@ -381,12 +381,16 @@ def test_empty_view_and_pad_slots():
         assert torch.isfinite(out.float()).all()
 
 
-def test_out_of_range_index_is_reported_not_read():
+@pytest.mark.parametrize("bad_row", [10 ** 6, -1], ids=["past-the-rows", "minus-one"])
+def test_out_of_range_index_is_reported_not_read(bad_row):
+    # a selected index past the KV rows, or -1 inside the query's valid
+    # entries, is recorded as a device bounds error and not read
     wl = TINY
     xd = {k: (v.cuda() if v is not None else None) for k, v in draw_inputs(wl).items()}
     pipe, _ = run_pipeline(wl, IN_SEQ_SPLIT, xd)
     bad = pipe.topk_idx[0].clone()
-    bad[5, 0] = 10 ** 6   # past the KV rows
+    assert int(bad[5, 0]) >= 0  # slot 5 sees 6 keys: entry 0 is valid
+    bad[5, 0] = bad_row
     dsa.dsa_sparse_attn_prefill(pipe.md[0], pipe.q_split[0], xd["kv"], bad, wl.scale, wl.Dv)
     with pytest.raises(dsa.DSAError) as e:
         dsa.dsa_poll_device_error()
