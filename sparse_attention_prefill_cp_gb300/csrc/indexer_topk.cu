@@ -68,7 +68,10 @@ struct IdxCfg {
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffW = kOffK + kStages * kKStageBytes;
   static constexpr int kOffSlot = kOffW + kTileTok * HI * 4;
-  static constexpr int kOffBar = kOffSlot + kTileTok * 8;
+  // key segments of the tile: one per local request with a slot to score
+  // (base row, keys, first chunk index), kTileTok + 1 entries each
+  static constexpr int kOffSeg = kOffSlot + kTileTok * 8;
+  static constexpr int kOffBar = kOffSeg + (3 * (kTileTok + 1) * 4 + 7) / 8 * 8;
   static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 64 + 1024;  // + alignment slack
@@ -88,7 +91,8 @@ struct IdxParams {
   float *scores;       // [rows][ld]
   int64_t ld;          // score row stride (floats)
   int32_t tpr, row_begin, row_end, max_kv_len, num_kv_rows;
-  int32_t key_chunk;   // keys per CTA (blockIdx.y): a multiple of kKeyChunk, set at launch
+  int32_t key_chunk;   // keys per chunk: a multiple of kKeyChunk, set at launch
+  int32_t min_keys;    // slots that see at most this many keys are not scored (the top-k takes them all)
   int *err;
 };
 
@@ -108,19 +112,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *t_full = k_empty + C::kStages;
   uint64_t *t_empty = t_full + 2;
   uint64_t *mma_done = t_empty + 2;
-  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);  // [0] tmem base, [1] lo, [2] hi
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);  // [0] tmem base, [1] segments, [2] chunks
+  int32_t *seg_base = reinterpret_cast<int32_t *>(smem + C::kOffSeg);  // [kTileTok + 1]
+  int32_t *seg_len = seg_base + (C::kTileTok + 1);
+  int32_t *seg_chunk0 = seg_len + (C::kTileTok + 1);                  // first chunk index; [nseg] = total
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slot0 = P.row_begin + blockIdx.x * C::kTileTok;
   const int local_batch = P.md.scalars[DSA_MD_LOCAL_BATCH];
   const int ratio = max(1, P.md.scalars[DSA_MD_COMPRESS_RATIO]);  // compressed KV: tokens per entry
 
-  if (tid == 0) {
-    misc[1] = 0x7fffffff;
-    misc[2] = 0;
-    misc[3] = 0;  // any valid slot
-  }
-  __syncthreads();
   // per-slot causal extent: key rows [base, base + last] (base = KV row of the
   // request's position 0 or first entry, last = the query's in-request
   // position, or its last visible entry (p + 1) / ratio - 1 for compressed KV;
@@ -143,11 +144,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     s_base[t] = base;
     s_p[t] = p;
-    if (p >= 0) {
-      atomicMin(reinterpret_cast<int *>(&misc[1]), base);
-      atomicMax(reinterpret_cast<int *>(&misc[2]), base + p);
-      misc[3] = 1;
-    }
   }
   // head weights; with FP8 operands each carries its query row's scale
   // (ReLU(a * x) = a * ReLU(x) for a scale a > 0)
@@ -161,7 +157,34 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     w_s[i] = wv;
   }
+  __syncthreads();
   if (tid == 0) {
+    // The tile's slots may belong to several local requests whose key rows lie
+    // far apart (a head-tail view's head and tail chunks, a request with a long
+    // prefix after a short one).  Each request with a slot to score is one
+    // segment [base, base + most keys of its slots); slots of one request are
+    // consecutive, so one pass builds the list.  The segments are cut into
+    // chunks of key_chunk keys, numbered across segments.
+    int nseg = 0;
+    for (int t = 0; t < C::kTileTok; ++t) {
+      const int keys = s_p[t] + 1;
+      if (keys <= P.min_keys || keys <= 0) continue;
+      if (nseg > 0 && seg_base[nseg - 1] == s_base[t]) {
+        seg_len[nseg - 1] = max(seg_len[nseg - 1], keys);
+      } else {
+        seg_base[nseg] = s_base[t];
+        seg_len[nseg] = keys;
+        ++nseg;
+      }
+    }
+    int chunks = 0;
+    for (int sg = 0; sg < nseg; ++sg) {
+      seg_chunk0[sg] = chunks;
+      chunks += (seg_len[sg] + P.key_chunk - 1) / P.key_chunk;
+    }
+    seg_chunk0[nseg] = chunks;
+    misc[1] = static_cast<uint32_t>(nseg);
+    misc[2] = static_cast<uint32_t>(chunks);
     mbar_init(q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&k_full[s], 1);
@@ -174,6 +197,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
+  __syncthreads();
+  const int nseg = static_cast<int>(misc[1]), nchunks = static_cast<int>(misc[2]);
+  // this CTA's chunks: blockIdx.y, blockIdx.y + gridDim.y, ...
+  if (static_cast<int>(blockIdx.y) >= nchunks) return;  // nothing to score (before any TMEM is held)
+  // key rows [kstart, kend) of chunk c
+  auto chunk_range = [&](int c, int &kstart, int &kend) {
+    int sg = 0;
+    while (sg + 1 < nseg && seg_chunk0[sg + 1] <= c) ++sg;
+    kstart = seg_base[sg] + (c - seg_chunk0[sg]) * P.key_chunk;
+    kend = min(seg_base[sg] + seg_len[sg], kstart + P.key_chunk);
+  };
   if (warp == 1) {
     tmem_alloc(&misc[0], 512);
     tmem_relinquish();
@@ -182,13 +216,31 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const int lo = static_cast<int>(misc[1]), hi = static_cast<int>(misc[2]);
-  const int kstart = lo + static_cast<int>(blockIdx.y) * P.key_chunk;
-  const bool active = misc[3] != 0 && kstart <= hi;
-  const int kend = active ? min(hi + 1, kstart + P.key_chunk) : kstart;
-  const int nblk = active ? (kend - kstart + C::kBK - 1) / C::kBK : 0;
+  // key blocks of this CTA, over all its chunks (the pipeline's block count)
+  int nblk = 0;
+  for (int c = blockIdx.y; c < nchunks; c += gridDim.y) {
+    int ks, ke;
+    chunk_range(c, ks, ke);
+    nblk += (ke - ks + C::kBK - 1) / C::kBK;
+  }
+  // first key row of each block in turn: the blocks of chunk blockIdx.y, then
+  // of chunk blockIdx.y + gridDim.y, ...
+  struct BlockCursor {
+    int c, ks, ke;
+  };
+  auto cursor_begin = [&](BlockCursor &cur) {
+    cur.c = blockIdx.y;
+    chunk_range(cur.c, cur.ks, cur.ke);
+  };
+  auto cursor_next = [&](BlockCursor &cur) {
+    cur.ks += C::kBK;
+    if (cur.ks >= cur.ke) {
+      cur.c += gridDim.y;
+      if (cur.c < nchunks) chunk_range(cur.c, cur.ks, cur.ke);
+    }
+  };
 
-  if (nblk > 0) {
+  {
     if (warp == 0 && lane == 0) {
       // ---------------- TMA producer
       tma_prefetch_desc(&qmap);
@@ -199,13 +251,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tma_load_2d(smem + C::kOffQ + (c * C::kRowsQ + h * 256) * C::kCWB, &qmap, c * C::kCW,
                       slot0 * C::HI + h * 256, q_full);
       int issued = 0;
-      for (int j = 0; j < nblk; ++j) {
+      BlockCursor cur;
+      cursor_begin(cur);
+      for (int j = 0; j < nblk; ++j, cursor_next(cur)) {
         const int s = j % C::kStages;
         if (!mbar_wait(&k_empty[s], ((j / C::kStages) & 1) ^ 1, P.err, 11, j)) break;
         mbar_arrive_expect_tx(&k_full[s], C::kKStageBytes);
         uint8_t *dst = smem + C::kOffK + s * C::kKStageBytes;
         for (int c = 0; c < C::kNCh; ++c)
-          tma_load_2d(dst + c * C::kBK * C::kCWB, &kmap, c * C::kCW, kstart + j * C::kBK, &k_full[s]);
+          tma_load_2d(dst + c * C::kBK * C::kCWB, &kmap, c * C::kCW, cur.ks, &k_full[s]);
         issued = j + 1;
       }
       // drain: every armed load has landed before the CTA can exit
@@ -245,8 +299,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int quad = warp & 3, part = (warp - 2) >> 2;
       const int row_in_blk = quad * 32 + lane;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-      for (int j = 0; j < nblk; ++j) {
-        const int key = kstart + j * C::kBK + row_in_blk;
+      BlockCursor cur;
+      cursor_begin(cur);
+      for (int j = 0; j < nblk; ++j, cursor_next(cur)) {
+        const int key = cur.ks + row_in_blk;
         // FP8: the key row's scale multiplies the whole head sum
         float kscale = 1.f;
         if constexpr (C::FP8)
@@ -639,7 +695,7 @@ dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
   IdxParams P{*a.md, a.w, static_cast<const uint8_t *>(a.q_idx), static_cast<const uint8_t *>(a.k_idx), out, ld,
-              a.tpr, row_begin, row_end, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, err};
+              a.tpr, row_begin, row_end, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, 0, err};
   return launch_indexer<C>(qmap, kmap, P, stream);
 }
 
@@ -677,7 +733,7 @@ dsa_status run_topk(const Args &a, int32_t *topk_idx, void *ws, size_t ws_bytes,
   for (int64_t r0 = 0; r0 < a.tpr; r0 += rows_fit) {
     const int32_t r1 = static_cast<int32_t>(r0 + rows_fit < a.tpr ? r0 + rows_fit : a.tpr);
     IdxParams P{*a.md, a.w, static_cast<const uint8_t *>(a.q_idx), static_cast<const uint8_t *>(a.k_idx), scores,
-                ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, err};
+                ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, TOPK, err};
     st = launch_indexer<C>(qmap, kmap, P, stream);
     if (st != DSA_OK) return st;
     st = launch_topk<TOPK>(*a.md, static_cast<int32_t>(r0), r1 - static_cast<int32_t>(r0), a.max_kv_len, scores, ld,

@@ -17,7 +17,7 @@ import sparse_attention_prefill_cp_gb300 as dsa
 from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill, HostStreamedPrefill
 from oracle import dsa_oracle as O
 from workloads import (HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, TINY, TINY_INT, LONG_8K, VARLEN_4, LONG_64K, MIXED_16,
-                       Workload, chunk_inputs, draw_inputs, sample_rows)
+                       Workload, chunk_inputs, draw_index_inputs, draw_inputs, sample_rows)
 
 pytestmark = pytest.mark.gpu
 MODES = (IN_SEQ_SPLIT, ROUND_ROBIN, HEAD_TAIL)
@@ -179,6 +179,10 @@ def test_fused_headsharded_attention_is_bit_identical(wl, mode):
 
 
 # ------------------------------------------------------------------ indexer scores
+
+# query slots per indexer CTA at the DeepSeek-V3.2 shapes (two groups of 256 / HI
+# tokens): the unit whose slots may belong to several requests
+INDEX_TILE = 8
 
 INT_FULL = LONG_8K.with_(name="int-full-2x", lengths=(2500, 700), cp_size=2, modes=MODES, integer=True, seed=9)
 FLOAT_FULL = LONG_8K.with_(name="float-full-2x", lengths=(2500, 700), cp_size=2, modes=MODES, sink=True, seed=10)
@@ -649,11 +653,17 @@ def test_full_size_sampled_rows(wl, mode):
     k_idx = f64(xd["k_idx"])
     sink = None if xd["sink"] is None else f64(xd["sink"])
     qsl = wl.query_start_loc()
-    # sampled flat rows: request boundaries, rows around t = topk, the last row, plus random ones
+    # sampled flat rows: request boundaries, rows around t = topk, the last row,
+    # on every rank the first slot of up to two local requests that share an
+    # indexer tile with another request (and the slot before it), plus random ones
     must = [0, wl.num_tokens - 1]
     for b in range(wl.batch):
         must += [qsl[b], qsl[b] + 1, qsl[b] + wl.topk - 1, qsl[b] + wl.topk, qsl[b + 1] - 1]
-    rows = sample_rows(wl.num_tokens, 24, seed=wl.seed, must=must)
+    for md in md_all:
+        lqs, ltp = md["local_query_start_loc"], md["local_token_pos"]
+        starts = [s for s in lqs[1:md["local_batch"]] if s % INDEX_TILE != 0][:2]
+        must += [ltp[s] for s in starts] + [ltp[s - 1] for s in starts]
+    rows = sample_rows(wl.num_tokens, 64 + len(must), seed=wl.seed, must=must)
     _, tpr = O.padded_geometry(wl.num_tokens, wl.cp_size)
     for g in rows:
         g = int(g)
@@ -883,3 +893,180 @@ def test_fp8_index_rows_with_prefix_and_compressed_kv(kind, mode):
                 continue
             ref = O.indexer_scores_fp8(q8_loc[i], w_loc[i], k8_h[base:base + n], wl.DI)
             check_topk_row(idx[r, i], ref, base, wl.topk, exact=True)
+
+
+# ------------------------------------------------------------------ indexer tiles across requests, long top-k rows
+
+def _index_views(wl, mode, xi):
+    """a1, the split of q_idx and w, and every view's indexer + top-k (no attention)."""
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, fused=True)
+    pipe.metadata()
+    pipe.split(None, xi["q_idx"], xi["w"])
+    for r in range(wl.cp_size):
+        pipe.indexer(r, xi["k_idx"])
+    dsa.dsa_poll_device_error()
+    return pipe
+
+
+def _check_rows_exact(pipe, wl, md_all, xi, slots_by_view):
+    """Integer variant: every listed slot's top-k set equals the oracle's."""
+    k_idx = f64(xi["k_idx"])
+    checked = 0
+    for r, slots in enumerate(slots_by_view):
+        md = md_all[r]
+        idx = pipe.topk_idx[r].cpu().numpy()
+        for i in sorted(set(int(i) for i in slots if 0 <= i < pipe.tpr)):
+            g = md["local_token_pos"][i]
+            if g < 0:
+                assert np.all(idx[i] == -1), (r, i)
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            n = g - md["local_req_pos_base"][j] + 1
+            # rows of at most topk keys select every key whatever their scores
+            ref = (O.indexer_scores(f64(xi["q_idx"][g]), f64(xi["w"][g]), k_idx[base:base + n]) if n > wl.topk
+                   else np.zeros(n))
+            check_topk_row(idx[i], ref, base, wl.topk, exact=True)
+            checked += 1
+    return checked
+
+
+def _straddling_slots(md, tpr, tile, per_view):
+    """Slots of the indexer tiles that hold slots of more than one local
+    request, widest key span first (at most ``per_view`` tiles), with the
+    slot before and after each tile."""
+    spans = []
+    for t0 in range(0, tpr, tile):
+        lo, hi, reqs = None, None, set()
+        for i in range(t0, min(t0 + tile, tpr)):
+            g = md["local_token_pos"][i]
+            if g < 0:
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            last = base + g - md["local_req_pos_base"][j]
+            lo = base if lo is None else min(lo, base)
+            hi = last if hi is None else max(hi, last)
+            reqs.add(j)
+        if len(reqs) > 1:
+            spans.append((hi - lo + 1, t0))
+    spans.sort(reverse=True)
+    out = []
+    for _, t0 in spans[:per_view]:
+        out += list(range(t0 - 1, t0 + tile + 1))
+    return out
+
+
+@pytest.mark.parametrize("lengths,cp,mode", [
+    (MIXED_16.lengths, 16, HEAD_TAIL),      # a tail chunk starts far into another request than the head chunk
+    (MIXED_16.lengths, 16, ROUND_ROBIN),
+    (MIXED_16.lengths, 16, IN_SEQ_SPLIT),
+    ((3000, 3000), 8, HEAD_TAIL),
+    ((8000, 800, 5, 3000), 4, HEAD_TAIL),
+], ids=lambda v: str(v)[:20])
+def test_topk_tiles_across_requests_bit_exact(lengths, cp, mode):
+    # An indexer CTA scores a tile of 8 consecutive slots; when they belong to
+    # several local requests, every request's keys must be scored (its key
+    # rows may lie far from the other request's).  Integer variant: the sets of
+    # the rows in the widest such tiles must be the oracle's, bit-exact.
+    wl = LONG_8K.with_(name="int-straddle", lengths=tuple(lengths), cp_size=cp, modes=(mode,), integer=True, seed=31)
+    xi = draw_index_inputs(wl, device="cuda")
+    pipe = _index_views(wl, mode, xi)
+    md_all = [O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), cp, r, mode) for r in range(cp)]
+    rng = np.random.default_rng(3)
+    slots = []
+    for md in md_all:
+        sl = _straddling_slots(md, pipe.tpr, INDEX_TILE, per_view=3)
+        slots.append(sl + [0, pipe.tpr - 1] + list(rng.choice(pipe.tpr, 4, replace=False)))
+    assert _check_rows_exact(pipe, wl, md_all, xi, slots) > 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_indexer_scores_cover_tiles_across_requests(mode):
+    # the scores test hook over the same geometry: every causal score of every
+    # slot is written (none left at -inf), integer variant, exact
+    wl = LONG_8K.with_(name="int-straddle-scores", lengths=(3000, 3000), cp_size=8, modes=(mode,), integer=True,
+                       seed=32)
+    xi = draw_index_inputs(wl, device="cuda")
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, fused=True)
+    pipe.metadata()
+    pipe.split(None, xi["q_idx"], xi["w"])
+    k_idx = f64(xi["k_idx"])
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
+        sc = dsa.dsa_indexer_scores(pipe.md[r], pipe.qi_split[r], xi["k_idx"], pipe.w_split[r],
+                                    pipe.max_kv_len).cpu().numpy().astype(np.float64)
+        dsa.dsa_poll_device_error()
+        for i in range(pipe.tpr):
+            g = md["local_token_pos"][i]
+            if g < 0:
+                assert np.all(np.isneginf(sc[i]))
+                continue
+            j = O.request_of_slot(md, i)
+            base = md["local_req_kv_base"][j]
+            n = g - md["local_req_pos_base"][j] + 1
+            ref = O.indexer_scores(f64(xi["q_idx"][g]), f64(xi["w"][g]), k_idx[base:base + n])
+            assert np.array_equal(sc[i, :n], ref), (r, i)
+            assert np.all(np.isneginf(sc[i, n:]))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_topk_long_rows_bit_exact(mode):
+    # rows longer than the top-k's shared-memory key cache (22,016 keys: the
+    # rest of the row is read again from global memory), integer variant;
+    # rows at 22,015 / 22,016 / 22,017 keys, each request's last row and 48
+    # sampled slots per view must select the oracle's sets, bit-exact
+    wl = INT_FULL.with_(name="int-long-rows", lengths=(30000, 4000), cp_size=2, seed=33)
+    xi = draw_index_inputs(wl, device="cuda")
+    pipe = _index_views(wl, mode, xi)
+    md_all = [O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
+              for r in range(wl.cp_size)]
+    want = {22014, 22015, 22016, 29999, 33999}
+    rng = np.random.default_rng(4)
+    slots = []
+    for md in md_all:
+        ltp = md["local_token_pos"]
+        slots.append([i for i, g in enumerate(ltp) if g in want] + list(rng.choice(pipe.tpr, 48, replace=False)))
+    assert sum(len(s) for s in slots) >= 96
+    _check_rows_exact(pipe, wl, md_all, xi, slots)
+
+
+def test_topk_64k_rows_bit_exact():
+    # one 65,536-token request on 8 round-robin views (rows up to 65,536 keys),
+    # integer variant (|I| <= 64 * 3 * 128 * 9 = 221,184: exact in fp32);
+    # 48 sampled slots per view and each view's last slot
+    wl = LONG_64K.with_(name="int-64k", integer=True, seed=34)
+    xi = draw_index_inputs(wl, device="cuda")
+    pipe = _index_views(wl, ROUND_ROBIN, xi)
+    md_all = [O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, ROUND_ROBIN)
+              for r in range(wl.cp_size)]
+    rng = np.random.default_rng(5)
+    slots = [list(rng.choice(pipe.tpr, 48, replace=False)) + [pipe.tpr - 1, 2047, 2048] for _ in md_all]
+    _check_rows_exact(pipe, wl, md_all, xi, slots)
+
+
+def test_topk_dense_bin_long_rows_bit_exact():
+    # the dense-bin construction of test_topk_dense_bin_and_ties_bit_exact on
+    # rows of up to 30,000 keys: more than 4,096 keys share the threshold's
+    # first digit (the candidate list overflows) and the rows run past the
+    # shared-memory key cache
+    wl = LONG_8K.with_(name="dense-bin-long", lengths=(30000,), cp_size=2, modes=(ROUND_ROBIN,))
+    T, HI, DI = wl.num_tokens, wl.HI, wl.DI
+    gen = torch.Generator().manual_seed(18)
+    q_idx = torch.ones(T, HI, DI, dtype=torch.bfloat16)
+    k_idx = (1 + (torch.rand(T, DI, generator=gen) >= 0.1).float()).to(torch.bfloat16)
+    w = torch.ones(T, HI, dtype=torch.float32)
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, ROUND_ROBIN, wl.H, wl.D, wl.Dv, HI, DI, wl.topk, wl.scale, fused=True)
+    pipe.metadata()
+    pipe.split(None, q_idx.cuda(), w.cuda())
+    for r in range(wl.cp_size):
+        pipe.indexer(r, k_idx.cuda())
+    dsa.dsa_poll_device_error()
+    idx = pipe.topk_idx.cpu().numpy()
+    kf = f64(k_idx)
+    rows = sample_rows(T, 40, seed=7, must=[22014, 22015, 22016, 22017, 24000, T - 2, T - 1])
+    for g in rows:
+        g = int(g)
+        r, i = g % wl.cp_size, g // wl.cp_size
+        ref = O.indexer_scores(np.ones((HI, DI)), np.ones(HI), kf[:g + 1])
+        check_topk_row(idx[r, i], ref, 0, wl.topk, exact=True)

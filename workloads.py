@@ -148,6 +148,28 @@ def draw_inputs(wl: Workload, device: str | torch.device = "cpu", seed_offset: i
     return {"q": q, "kv": kv, "q_idx": q_idx, "k_idx": k_idx, "w": w.contiguous(), "sink": sink}
 
 
+def draw_index_inputs(wl: Workload, device: str | torch.device = "cpu", seed_offset: int = 0) -> dict:
+    """Only the indexer's inputs of ``wl``: q_idx [T,HI,DI], k_idx [T,DI] bf16
+    and w [T,HI] fp32, drawn with their own generator (seed ``wl.seed +
+    seed_offset + 7919``) in that order; from {-3..3} when ``wl.integer``
+    (every score an exact integer), N(0,1) (w: N(0,1) * w_std) otherwise.
+    For indexer / top-k tests at sizes where the attention's q would be
+    gigabytes."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed + seed_offset + 7919)
+    T = wl.num_tokens
+    if wl.integer:
+        q_idx = _small_ints((T, wl.HI, wl.DI), gen, dev).to(torch.bfloat16)
+        k_idx = _small_ints((T, wl.DI), gen, dev).to(torch.bfloat16)
+        w = _small_ints((T, wl.HI), gen, dev)
+    else:
+        q_idx = _normal((T, wl.HI, wl.DI), gen, dev).to(torch.bfloat16)
+        k_idx = _normal((T, wl.DI), gen, dev).to(torch.bfloat16)
+        w = _normal((T, wl.HI), gen, dev, std=wl.w_std)
+    return {"q_idx": q_idx, "k_idx": k_idx, "w": w.contiguous()}
+
+
 def sample_rows(n_rows_total: int, count: int, seed: int, must=()) -> np.ndarray:
     """A fixed, seeded sample of row indices in [0, n_rows_total): the indices in
     ``must`` that are in range, topped up to ``count`` from a seeded permutation.
