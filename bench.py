@@ -16,7 +16,6 @@ one JSON line.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import math
 import os
@@ -36,10 +35,9 @@ import workloads as W  # noqa: E402
 
 METRIC = "DSA prefill query-tokens/s (indexer+top-k+sparse attn), % of roofline"
 UNIT = "query-tokens/s"
-DEFAULT_WORKLOAD = W.LONG_8K.name
+DEFAULT_WORKLOAD = W.MIXED_16.name
+AUX_WORKLOAD = W.LONG_8K.name
 L2_BYTES = 126 * 1024 * 1024
-PROFILE_FILE = os.path.join(ROOT, "profiles", "sparse_attn_kernel_long8k.md")
-ATTN_SRC = os.path.join(ROOT, "sparse_attention_prefill_cp_gb300", "csrc", "sparse_attn.cu")
 
 
 def parse():
@@ -50,9 +48,11 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--mode", choices=["in-seq", "round-robin", "head-tail"], default=None)
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--core-only", action="store_true",
                     help="skip the e2e and aux legs (workload sweeps; the default run keeps them)")
+    ap.add_argument("--aux-workload", default=AUX_WORKLOAD, choices=sorted(W.ALL),
+                    help="workload of the aux legs (byte kernels, NEXT-row variants)")
     ap.add_argument("--unfused", action="store_true",
                     help="split q and rerange the outputs as separate passes instead of in the attention")
     ap.add_argument("--view-streams", type=int, default=2,
@@ -112,21 +112,6 @@ def peaks():
                 "source": "measured"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
-
-
-def profiled_traffic():
-    """dram bytes per attention launch from the committed ncu summary, only if
-    it was taken on the current kernel source (same hash)."""
-    try:
-        h = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
-        txt = open(PROFILE_FILE).read()
-        kv = dict(l.split(":", 1) for l in txt.splitlines() if l.startswith(("traffic_bytes_per_launch:",
-                                                                              "kernel_source_sha256_16:")))
-        if kv.get("kernel_source_sha256_16", "").strip() == h:
-            return float(kv["traffic_bytes_per_launch"].strip())
-    except Exception:
-        pass
-    return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -270,9 +255,226 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def default_mode(wl):
+    """The split mode a workload is benched in: round-robin where the workload
+    lists it (the pages' load-balanced split), else its first mode."""
+    return W.ROUND_ROBIN if W.ROUND_ROBIN in wl.modes else wl.modes[0]
+
+
+def e2e_leg(args, wl, mode, dev, x, pk):
+    """End to end from page-locked host buffers through the public calls
+    (HostStreamedPrefill: per view, the copy engines take its rows of q and
+    q_idx up while earlier views compute and bring finished views' outputs
+    back into token order), every batch's copies inside the timed region; and
+    the same copies on their own, timed the same way (what bounds it)."""
+    import sparse_attention_prefill_cp_gb300 as dsa
+    from sparse_attention_prefill_cp_gb300.pipeline import HostStreamedPrefill
+
+    host = {}
+    for k, v in x.items():
+        if v is None:
+            host[k] = None
+            continue
+        h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        h.copy_(v)
+        host[k] = h
+    out_host = torch.empty((wl.num_tokens, wl.H, wl.Dv), dtype=torch.bfloat16, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out_host.numel() * out_host.element_size()
+    streamed = HostStreamedPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                                   dev, depth=3)
+    for _ in range(2):  # warm-up
+        streamed.submit(host, out_host)
+    torch.cuda.synchronize()
+    n = max(2, args.e2e_steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(streamed.h2d)
+    for _ in range(n):
+        last = streamed.submit(host, out_host)
+    e1 = streamed.done_event(last)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n
+    dsa.dsa_poll_device_error()
+
+    # the same bytes through the copy engines alone: full-token inputs, then
+    # per view its q and q_idx rows up and its output rows down, on the same
+    # two copy streams (view v's read-back after view v's upload)
+    cp = wl.cp_size
+    full = {k: torch.empty_like(x[k]) for k in ("kv", "k_idx", "w")}
+    qv, qiv, ov = streamed.q_v[0], streamed.qi_v[0], streamed.out_v[0]
+    up, down = streamed.h2d, streamed.d2h
+
+    def copies():
+        with torch.cuda.stream(up):
+            for k, t in full.items():
+                t.copy_(host[k], non_blocking=True)
+        for r in range(cp):
+            dsa.dsa_cp_split_from_host(host["q"], cp, mode, r, qv, up)
+            dsa.dsa_cp_split_from_host(host["q_idx"], cp, mode, r, qiv, up)
+            ev = torch.cuda.Event()
+            ev.record(up)
+            down.wait_event(ev)
+            dsa.dsa_cp_rerange_to_host(ov, wl.num_tokens, cp, mode, r, out_host, down)
+
+    copies()
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(up)
+    for _ in range(n):
+        copies()
+    down.wait_stream(up)
+    c1.record(down)
+    torch.cuda.synchronize()
+    copy_ms = c0.elapsed_time(c1) / n
+    del streamed, full, host, out_host
+    torch.cuda.empty_cache()
+    return {
+        "value": wl.num_tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        "ms_per_step": e2e_ms, "batches": n,
+        "how": "page-locked host inputs -> device -> output back to page-locked host, every batch: full-token inputs "
+               "(kv, k_idx, w, sink) up first, then per CP view its q and q_idx rows taken up by the copy engines "
+               "(dsa_cp_split_from_host) while earlier views compute, and its output rows copied back into token "
+               "order (dsa_cp_rerange_to_host); HostStreamedPrefill, 3 view buffer sets",
+        "copies_only_ms_per_step": copy_ms,
+        "copies_gbs": (h2d + d2h) / (copy_ms / 1e3) / 1e9,
+    }
+
+
+def aux_legs(args, wl, mode, dev, pk):
+    """Byte-moving steps and the NEXT-row variants, each timed on its own
+    (cold L2, outside the timed step) on ``wl``."""
+    import sparse_attention_prefill_cp_gb300 as dsa
+    from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill
+
+    x = W.draw_inputs(wl, device=dev)
+    pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
+                      view_streams=args.view_streams, fused=True)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn, reps=5):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def step():
+        return pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
+
+    def fused_core():
+        hs = pipe._head_sharded_buffer()
+        for r in range(wl.cp_size):
+            dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], x["k_idx"], pipe.w_split[r], pipe.topk,
+                                 pipe.max_kv_len, pipe.topk_idx[r], pipe.workspace)
+            dsa.dsa_sparse_attn_prefill_headsharded(pipe.md[r], pipe.q_split[r], x["kv"], pipe.topk_idx[r],
+                                                    pipe.scale, pipe.Dv, wl.cp_size, hs, x["sink"])
+
+    step()
+    T, pad = wl.num_tokens, pipe.pad
+    split_bytes = (T + pad) * (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4)
+    out_bytes = 2 * T * wl.H * wl.Dv * 2
+    aux = {"workload": wl.name, "mode": W.MODE_NAMES[mode]}
+
+    def split_all():  # a2 as its own pass, q included
+        for t, dst in ((x["q"], pipe.q_split), (x["q_idx"], pipe.qi_split), (x["w"], pipe.w_split)):
+            dsa.dsa_cp_split(t, wl.cp_size, mode, -1, dst)
+
+    for name, fn, nbytes in (("a2_split", split_all, split_bytes),
+                             ("a6_rerange", lambda: dsa.dsa_cp_rerange(pipe.out_split, wl.num_tokens, wl.cp_size, mode,
+                                                                       pipe.out), out_bytes),
+                             ("a2a_heads", pipe.all_to_all_heads, out_bytes)):
+        ms = timed(fn)
+        aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+                     "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
+    aux["a1_metadata_ms"] = timed(pipe.metadata)  # every view's build_cp_local_metadata
+
+    # compressed KV: the same queries over floor(T / c) compressed entries
+    # (the first rows of kv and k_idx stand for them), the a3-a5 core timed
+    # with its metadata, against the roofline of its own work
+    for c in (4, 128):
+        rows = wl.num_tokens // c
+        pc = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
+                        view_streams=args.view_streams, fused=True, compress_ratio=c)
+        pc.run(x["q"], x["kv"][:rows], x["q_idx"], x["k_idx"][:rows], x["w"], x["sink"])
+
+        def core_c(pc=pc, rows=rows):
+            pc.metadata()
+            pc._q = x["q"]
+            pc.views(x["kv"][:rows], x["k_idx"][:rows], x["sink"], torch.cuda.current_stream())
+
+        ms = timed(core_c, reps=3)
+        fi, fa, by = algorithmic(wl, c)
+        roof_c = max((fi + fa) / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+        aux[f"a3_a5_compressed_c{c}"] = {"ms": ms, "flops": fi + fa, "roofline_frac": roof_c / (ms / 1e3)}
+        del pc
+    # FP8 latent-KV cache: quantise / dequantise as HBM passes (bytes read +
+    # written), and the a3-a5 core over the cache (dequantisation + views)
+    cache = dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv)
+    kv_rows = torch.empty_like(x["kv"])
+    fp8_bytes = x["kv"].shape[0] * (wl.D * 2 + cache.shape[1])
+    for name, fn in (("kv_fp8_quantize", lambda: dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv, cache)),
+                     ("kv_fp8_dequantize", lambda: dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows))):
+        ms = timed(fn)
+        aux[name] = {"ms": ms, "bytes": fp8_bytes, "gbs": fp8_bytes / (ms / 1e3) / 1e9,
+                     "frac_hbm": fp8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+
+    def fp8_core():
+        rows = dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows)
+        pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
+
+    pipe._q = x["q"]
+    aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
+    # FP8 index rows: q_I and k_I quantised (HBM passes, bytes read + written),
+    # and the a3-a5 core with the indexer over them beside the same core over
+    # bf16 index rows, timed the same way
+    q8, k8 = dsa.dsa_indexer_fp8_rows(x["q_idx"]), dsa.dsa_indexer_fp8_rows(x["k_idx"])
+    idx8_bytes = x["q_idx"].numel() * 2 + q8.numel() + x["k_idx"].numel() * 2 + k8.numel()
+    ms = timed(lambda: (dsa.dsa_indexer_fp8_rows(x["q_idx"], q8), dsa.dsa_indexer_fp8_rows(x["k_idx"], k8)))
+    aux["index_fp8_quantize"] = {"ms": ms, "bytes": idx8_bytes, "gbs": idx8_bytes / (ms / 1e3) / 1e9,
+                                 "frac_hbm": idx8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    p8 = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
+                    view_streams=args.view_streams, fused=True, index_fp8=True)
+    p8.run(x["q"], x["kv"], q8, k8, x["w"], x["sink"])
+    aux["a3_a5_fp8index_ms"] = timed(lambda: p8.views(x["kv"], k8, x["sink"], torch.cuda.current_stream()), reps=3)
+    pipe._q = x["q"]
+    aux["a3_a5_bf16index_ms"] = timed(lambda: pipe.views(x["kv"], x["k_idx"], x["sink"],
+                                                         torch.cuda.current_stream()), reps=3)
+    del p8
+
+    def unfused_step():  # the whole step with the split of q and the rerange as passes of their own
+        pipe.fused = False
+        try:
+            step()
+        finally:
+            pipe.fused = True
+
+    aux["step_unfused_ms"] = timed(unfused_step, reps=3)
+    aux["note"] = ("a2a_heads: all views' [tpr][H][Dv] outputs -> [cp][T][H/cp][Dv] head-sharded; "
+                   "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
+                   "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
+                   "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
+                   "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own; "
+                   "a1_metadata_ms: every view's metadata (one launch per view); "
+                   "a3_a5_compressed_c*: metadata + core over compressed KV at ratio c (T / c entries); "
+                   "index_fp8_quantize: q_I and k_I to FP8 index rows; a3_a5_fp8index_ms / a3_a5_bf16index_ms: "
+                   "the core with the indexer over FP8 / bf16 index rows")
+    dsa.dsa_poll_device_error()
+    del pipe, x
+    torch.cuda.empty_cache()
+    return aux
+
+
 def run_ours(args, wl, mode, rank, world):
     import sparse_attention_prefill_cp_gb300 as dsa
-    from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill, HostStreamedPrefill
+    from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -282,7 +484,6 @@ def run_ours(args, wl, mode, rank, world):
     pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
                       view_streams=args.view_streams, fused=fused)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
 
     # attention launches timed live with events on the launching stream
     attn_events = []
@@ -340,199 +541,49 @@ def run_ours(args, wl, mode, rank, world):
     attn_flops = [per_view_flops[r] for (r, _, _) in attn_events]
     pk = peaks()
     achieved = (sum(attn_flops) / (sum(attn_ms) / 1e3)) / 1e12
-
-    e2e_stream_ms = e2e_serial = h2d = d2h = n_e2e = None
-    aux = None
-    if not args.core_only:  # the e2e and aux legs (need about 4x the workload's memory)
-        # end to end: pinned host inputs in, output out, through the same public
-        # calls.  Streamed: batches go through HostStreamedPrefill, whose copies of
-        # batch s+1's inputs (H2D) and batch s-1's output (D2H) overlap the compute
-        # of batch s; every batch's copies are inside the timed region.  Serial:
-        # one batch at a time, copy in, compute, copy out, on one stream.
-        host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
-        out_hosts = [torch.empty((wl.num_tokens, wl.H, wl.Dv), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-        d2h = out_hosts[0].numel() * out_hosts[0].element_size()
-        streamed = HostStreamedPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
-                                       dev, depth=2, view_streams=args.view_streams, fused=fused)
-        for s in range(2):  # warm-up of both buffer sets
-            streamed.submit(host, out_hosts[s % 2])
-        torch.cuda.synchronize()
-        n_e2e = max(2, args.e2e_steps)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e0.record(streamed.h2d)
-        for s in range(n_e2e):
-            last = streamed.submit(host, out_hosts[s % 2])
-        e1 = streamed.done_event(last)
-        torch.cuda.synchronize()
-        e2e_stream_ms = e0.elapsed_time(e1) / n_e2e
-        dsa.dsa_poll_device_error()
-        dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in host.items()}
-        e2e_serial = []
-        for s in range(3):
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            for k, v in host.items():
-                if v is not None:
-                    dev_in[k].copy_(v, non_blocking=True)
-            out = pipe.run(dev_in["q"], dev_in["kv"], dev_in["q_idx"], dev_in["k_idx"], dev_in["w"], dev_in["sink"])
-            out_hosts[0].copy_(out, non_blocking=True)
-            b.record()
-            torch.cuda.synchronize()
-            if s > 0:
-                e2e_serial.append(a.elapsed_time(b))
-        del streamed, dev_in
-        dsa.dsa_poll_device_error()
-
-        # data-movement steps and the head-sharded output, each timed on its own
-        # (cold L2, outside the timed step): a2 split, a6 rerange, the head/token
-        # all-to-all as a separate pass, and a3-a5 with the all-to-all fused into
-        # the attention's stores
-        def timed(fn, reps=5):
-            fn()
-            ts = []
-            for _ in range(reps):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                torch.cuda.synchronize()
-                ts.append(a.elapsed_time(b))
-            return statistics.median(ts)
-
-        def fused_core():
-            hs = pipe._head_sharded_buffer()
-            for r in range(wl.cp_size):
-                dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], x["k_idx"], pipe.w_split[r], pipe.topk,
-                                     pipe.max_kv_len, pipe.topk_idx[r], pipe.workspace)
-                dsa.dsa_sparse_attn_prefill_headsharded(pipe.md[r], pipe.q_split[r], x["kv"], pipe.topk_idx[r],
-                                                        pipe.scale, pipe.Dv, wl.cp_size, hs, x["sink"])
-
-        pipe.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
-        T, pad = wl.num_tokens, pipe.pad
-        split_bytes = (T + pad) * (wl.H * wl.D * 2 + wl.HI * wl.DI * 2 + wl.HI * 4)
-        out_bytes = 2 * T * wl.H * wl.Dv * 2
-        aux = {}
-
-        def split_all():  # a2 as its own pass, q included
-            for t, dst in ((x["q"], pipe.q_split), (x["q_idx"], pipe.qi_split), (x["w"], pipe.w_split)):
-                dsa.dsa_cp_split(t, wl.cp_size, mode, -1, dst)
-
-        for name, fn, nbytes in (("a2_split", split_all, split_bytes),
-                                 ("a6_rerange", lambda: dsa.dsa_cp_rerange(pipe.out_split, wl.num_tokens, wl.cp_size, mode,
-                                                                           pipe.out), out_bytes),
-                                 ("a2a_heads", pipe.all_to_all_heads, out_bytes)):
-            ms = timed(fn)
-            aux[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
-                         "frac_hbm": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
-        aux["a3_a5_headsharded_ms"] = timed(fused_core, reps=3)
-        aux["a1_metadata_ms"] = timed(pipe.metadata)  # every view's build_cp_local_metadata
-
-        # compressed KV: the same queries over floor(T / c) compressed entries
-        # (the first rows of kv and k_idx stand for them), the a3-a5 core timed
-        # with its metadata, against the roofline of its own work
-        for c in (4, 128):
-            rows = wl.num_tokens // c
-            pc = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
-                            view_streams=args.view_streams, fused=True, compress_ratio=c)
-            pc.run(x["q"], x["kv"][:rows], x["q_idx"], x["k_idx"][:rows], x["w"], x["sink"])
-
-            def core_c(pc=pc, rows=rows):
-                pc.metadata()
-                pc._q = x["q"]
-                pc.views(x["kv"][:rows], x["k_idx"][:rows], x["sink"], torch.cuda.current_stream())
-
-            ms = timed(core_c, reps=3)
-            fi, fa, by = algorithmic(wl, c)
-            roof_c = max((fi + fa) / (pk["bf16_tflops_sustained"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
-            aux[f"a3_a5_compressed_c{c}"] = {"ms": ms, "flops": fi + fa, "roofline_frac": roof_c / (ms / 1e3)}
-            del pc
-        # FP8 latent-KV cache: quantise / dequantise as HBM passes (bytes read +
-        # written), and the a3-a5 core over the cache (dequantisation + views)
-        cache = dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv)
-        kv_rows = torch.empty_like(x["kv"])
-        fp8_bytes = x["kv"].shape[0] * (wl.D * 2 + cache.shape[1])
-        for name, fn in (("kv_fp8_quantize", lambda: dsa.dsa_kv_fp8_quantize(x["kv"], wl.Dv, cache)),
-                         ("kv_fp8_dequantize", lambda: dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows))):
-            ms = timed(fn)
-            aux[name] = {"ms": ms, "bytes": fp8_bytes, "gbs": fp8_bytes / (ms / 1e3) / 1e9,
-                         "frac_hbm": fp8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
-
-        def fp8_core():
-            rows = dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows)
-            pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
-
-        aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
-        # FP8 index rows: q_I and k_I quantised (HBM passes, bytes read +
-        # written), and the a3-a5 core with the indexer over them beside the
-        # same core over bf16 index rows, timed the same way
-        q8, k8 = dsa.dsa_indexer_fp8_rows(x["q_idx"]), dsa.dsa_indexer_fp8_rows(x["k_idx"])
-        idx8_bytes = x["q_idx"].numel() * 2 + q8.numel() + x["k_idx"].numel() * 2 + k8.numel()
-        ms = timed(lambda: (dsa.dsa_indexer_fp8_rows(x["q_idx"], q8), dsa.dsa_indexer_fp8_rows(x["k_idx"], k8)))
-        aux["index_fp8_quantize"] = {"ms": ms, "bytes": idx8_bytes, "gbs": idx8_bytes / (ms / 1e3) / 1e9,
-                                     "frac_hbm": idx8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
-        p8 = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
-                        view_streams=args.view_streams, fused=True, index_fp8=True)
-        p8.run(x["q"], x["kv"], q8, k8, x["w"], x["sink"])
-        aux["a3_a5_fp8index_ms"] = timed(lambda: p8.views(x["kv"], k8, x["sink"], torch.cuda.current_stream()),
-                                         reps=3)
-        pipe._q = x["q"]
-        aux["a3_a5_bf16index_ms"] = timed(lambda: pipe.views(x["kv"], x["k_idx"], x["sink"],
-                                                             torch.cuda.current_stream()), reps=3)
-        del p8
-
-        def unfused_step():  # the whole step with the split of q and the rerange as passes of their own
-            pipe.fused = False
-            try:
-                step()
-            finally:
-                pipe.fused = fused
-
-        aux["step_unfused_ms"] = timed(unfused_step, reps=3)
-        aux["note"] = ("a2a_heads: all views' [tpr][H][Dv] outputs -> [cp][T][H/cp][Dv] head-sharded; "
-                       "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
-                       "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
-                       "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
-                       "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own; "
-                       "a1_metadata_ms: every view's metadata (one launch per view); "
-                       "a3_a5_compressed_c*: metadata + core over compressed KV at ratio c (T / c entries); "
-                       "index_fp8_quantize: q_I and k_I to FP8 index rows; a3_a5_fp8index_ms / a3_a5_bf16index_ms: "
-                       "the core with the indexer over FP8 / bf16 index rows")
-        dsa.dsa_poll_device_error()
-
     launches = pipe.launches_per_step() * args.steps
+    core_region_s = sum(core_ms_one_stream or core_ms) / 1e3
+
+    e2e = aux = None
+    if not args.core_only:
+        del pipe, flush
+        torch.cuda.empty_cache()
+        e2e = e2e_leg(args, wl, mode, dev, x, pk)
+        del x
+        torch.cuda.empty_cache()
+        wl_aux = W.ALL[args.aux_workload]
+        aux = aux_legs(args, wl_aux, default_mode(wl_aux), dev, pk)
+
     if rank != 0:
         return
     f_idx, f_att, bytes_core = algorithmic(wl)
     total_tokens = world * args.steps * wl.num_tokens
     value = total_tokens / t_rank
-    roof_s = max((f_idx + f_att) / (pk["bf16_tflops_sustained"] * 1e12), bytes_core / (pk["hbm_gbs"] * 1e9))
+    burst, sustained = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
+    roof_s = max((f_idx + f_att) / (burst * 1e12), bytes_core / (pk["hbm_gbs"] * 1e9))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_rank / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 inputs, shapes of the workload)",
         "config": dict(config_of(wl, mode), view_streams=args.view_streams, fused_split_rerange=fused),
         "roofline": {"bound": "tensor", "kernel": "sparse_attn_kernel", "achieved": achieved,
-                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
-                     "peak_source": f"{pk['source']} bf16 sustained", "traffic": profiled_traffic(),
+                     "peak": burst, "unit": "TFLOP/s", "frac": achieved / burst,
+                     "peak_source": f"{pk['source']} bf16 burst (cuBLAS, MEASURED_PEAKS.json bf16_tflops)",
+                     "frac_of_sustained_peak": achieved / sustained,
+                     "traffic": None,
+                     "traffic_note": "DRAM bytes per launch are taken by ncu on a smaller capture (profiles/)",
                      "launch_ms": statistics.mean(attn_ms), "flops_per_launch": statistics.mean(attn_flops),
+                     "launches": len(attn_ms), "timed_region_s": core_region_s,
                      "launches_timed": ("in the timed steps" if core_ms_one_stream is None else
                                         "in a second pass of the same steps with the views on one stream")},
         "core": {"what": "a3-a5 (indexer + top-k + sparse attention, all views)",
                  "ms_per_step": statistics.mean(core_ms), "value": wl.num_tokens / (statistics.mean(core_ms) / 1e3),
                  "roofline_frac": roof_s / (statistics.mean(core_ms) / 1e3),
-                 "roofline_ms": roof_s * 1e3, "flops": f_idx + f_att,
-                 "view_streams": pipe.view_streams,
+                 "roofline_ms": roof_s * 1e3, "flops": f_idx + f_att, "flops_indexer": f_idx, "flops_attention": f_att,
+                 "peak": "bf16 burst",
+                 "view_streams": args.view_streams,
                  "ms_per_step_one_stream": (statistics.mean(core_ms_one_stream) if core_ms_one_stream else None)},
-        "e2e": None if args.core_only else {
-            "value": wl.num_tokens / (e2e_stream_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_stream_ms, "batches": n_e2e,
-            "how": "pinned host inputs -> device -> output back to pinned host, every batch; copies of the "
-                   "neighbouring batches overlap each batch's compute (HostStreamedPrefill, 2 buffer sets)",
-            "serial_ms_per_step": statistics.mean(e2e_serial),
-            "serial_value": wl.num_tokens / (statistics.mean(e2e_serial) / 1e3)},
+        "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": launches,
         "aux": aux,
@@ -551,8 +602,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     wl = W.ALL[args.workload]
-    mode = wl.modes[0] if args.mode is None else {"in-seq": W.IN_SEQ_SPLIT, "round-robin": W.ROUND_ROBIN,
-                                                   "head-tail": W.HEAD_TAIL}[args.mode]
+    mode = default_mode(wl) if args.mode is None else {"in-seq": W.IN_SEQ_SPLIT, "round-robin": W.ROUND_ROBIN,
+                                                        "head-tail": W.HEAD_TAIL}[args.mode]
     if world > 1:
         backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
         torch.distributed.init_process_group(backend=backend)

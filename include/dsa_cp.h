@@ -26,6 +26,12 @@
  *     one second) sets a device error word and the kernel returns early;
  *     dsa_poll_device_error reports it.
  *   - bf16 tensors are row-major, contiguous, 16-byte aligned.
+ *   - The library looks up the device addresses of its own static device
+ *     arrays (the error record, the no-allocation scratch) once per device
+ *     and keeps them for the life of the process.  They belong to the
+ *     device's primary context: after a cudaDeviceReset of that device the
+ *     kept addresses are stale, so do not use the library on that device
+ *     again in the same process.
  *   - Supported dimension sets (others return DSA_ERR_UNSUPPORTED):
  *       DeepSeek-V3.2 shapes: H=128, D=576, Dv=512, HI=64, DI=128, topk=2048
  *       tiny shapes:          H=8,   D=64,  Dv=48,  HI=4,  DI=32,  topk=64
@@ -40,7 +46,7 @@
 extern "C" {
 #endif
 
-#define DSA_CP_ABI_VERSION 5
+#define DSA_CP_ABI_VERSION 6
 
 typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 
@@ -202,6 +208,33 @@ dsa_status dsa_cp_split(const void *src, int64_t row_bytes, int32_t num_tokens, 
  */
 dsa_status dsa_cp_rerange(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
                           dsa_cp_mode mode, void *dst, dsa_stream_t stream);
+
+/*
+ * The split and the rerange of ONE rank's rows between HOST memory and the
+ * device, done by the copy engines (cudaMemcpy2DAsync: no kernel, no
+ * allocation), for inputs and outputs that live on the host ([blog]
+ * "第三部分": a rank receives its own rows of the token stream and its
+ * outputs go back to logical token order).
+ *   dsa_cp_split_from_host:  host_src [num_tokens][row_bytes] (host) ->
+ *       dst [tpr][row_bytes] (device): the rows of rank cp_rank, slot order
+ *       as in dsa_cp_split with that cp_rank.
+ *   dsa_cp_rerange_to_host:  src [tpr][row_bytes] (device, rank cp_rank's
+ *       slots) -> host_dst [num_tokens][row_bytes] (host): each real slot's
+ *       row to its flat token row; other rows of host_dst are not written.
+ * Pad slots are neither read nor written (the device buffer's pad rows keep
+ * what they held).  A rank's rows are at most two runs of evenly spaced flat
+ * rows (in-seq: one contiguous run; round-robin: stride cp_size rows;
+ * head-tail: a head run and a tail run), so a call issues at most two 2D
+ * copies on `stream`.  The host buffer should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copy to be asynchronous;
+ * pageable memory works but the copy then blocks the calling thread.
+ * 0 <= cp_rank < cp_size.  Byte copies: bit-exact.  A failing copy returns
+ * DSA_ERR_CUDA.
+ */
+dsa_status dsa_cp_split_from_host(const void *host_src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
+                                  dsa_cp_mode mode, int32_t cp_rank, void *dst, dsa_stream_t stream);
+dsa_status dsa_cp_rerange_to_host(const void *src, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
+                                  dsa_cp_mode mode, int32_t cp_rank, void *host_dst, dsa_stream_t stream);
 
 /*
  * Head/token all-to-all of the attention outputs ([xLLM] 单层前向数据流 (6)

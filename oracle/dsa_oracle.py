@@ -32,41 +32,40 @@ Readings taken where the pages are silent or ambiguous (each listed in the
 design notes):
   R1  split granularity is the flat token stream, not per request ([xLLM] 2).
   R2  in-seq-split is contiguous ([blog] 4 第一部分); padding sits at the end.
-  R3  round-robin indexes the global flat token ([blog] 2.B).
-  R4  local_seq_lens is the KV extent visible to the rank's queries of that
-      request, i.e. last local in-request position + 1 ([xLLM] 单层前向数据流
-      "右对齐"); local_kv_start_loc is its exclusive cumsum.
-  R5  requests with no local row are dropped from the local batch.
-  R6  top-k ties go to the lower index; -0.0 equals +0.0; rows with p+1 <= k
-      select every s <= p and pad with -1; the result is a set (returned in
-      ascending order).
-  R7  the sink is a logit already in scaled units that adds exp(sink - m) to
-      the softmax denominator only; absent means no term.
-  R8  KV rows stay in full flat order; request b's key s is flat row qs_b + s.
-  R9  chunked prefill ([xLLM] 测试与验证 lists it; 单层前向数据流 (4) gives the
-      attention separate KV geometry: cu_seqlens_ori_kv, seqused_kv): request
-      b's queries are the last q_len_b positions of its sequence of
-      seq_lens[b] >= q_len_b tokens, after a prefix of seq_lens[b] - q_len_b
-      positions whose KV is already there.  KV and index keys hold every
-      request's whole sequence, requests in order: position s of request b is
-      KV row kv_start_b + s, kv_start_b = sum of seq_lens before b.  With no
-      prefix kv_start_b = qs_b and this is R8.
-  R11 head-tail in-seq-split (only named by [xLLM] 7, as a worker-side split):
+  R2  head-tail in-seq-split (only named by [xLLM] 7, as a worker-side split):
       the zigzag split.  tokens_per_rank is as for the other modes; the first
       cp*ceil(tpr/2) padded rows are cut into head chunks of ceil(tpr/2) rows
       (rank r: chunk r), the rest into tail chunks of floor(tpr/2) rows given
       out in reverse rank order (rank r: chunk cp-1-r), so a rank pairs an early
       (short-context) chunk with a late one; a rank's slots are its head rows
       then its tail rows, i.e. ascending flat order.
-  R10 the head/token all-to-all after the attention ([xLLM] 单层前向数据流 (6))
+  R3  round-robin indexes the global flat token ([blog] 2.B).
+  R4  local_seq_lens is the KV extent visible to the rank's queries of that
+      request, i.e. last local in-request position + 1 ([xLLM] 单层前向数据流
+      "右对齐"); local_kv_start_loc is its exclusive cumsum.
+  R5  requests with no local row are dropped from the local batch.
+  R7  KV rows stay in full flat order; request b's key s is flat row qs_b + s.
+  R9  top-k ties go to the lower index; -0.0 equals +0.0; rows with p+1 <= k
+      select every s <= p and pad with -1; the result is a set (returned in
+      ascending order).
+  R10 the sink is a logit already in scaled units that adds exp(sink - m) to
+      the softmax denominator only; absent means no term.
+  R12 chunked prefill ([xLLM] 测试与验证 lists it; 单层前向数据流 (4) gives the
+      attention separate KV geometry: cu_seqlens_ori_kv, seqused_kv): request
+      b's queries are the last q_len_b positions of its sequence of
+      seq_lens[b] >= q_len_b tokens, after a prefix of seq_lens[b] - q_len_b
+      positions whose KV is already there.  KV and index keys hold every
+      request's whole sequence, requests in order: position s of request b is
+      KV row kv_start_b + s, kv_start_b = sum of seq_lens before b.  With no
+      prefix kv_start_b = qs_b and this is R7.
+  R16 the head/token all-to-all after the attention ([xLLM] 单层前向数据流 (6))
       leaves rank r' with heads r'*H/cp .. (r'+1)*H/cp - 1 of every real token,
       tokens in flat order for both split modes (for in-seq-split the
       rank-major order already is the flat order; for round-robin the rows are
       put back in flat order as by rerange); H must divide by cp.
-
-  R12 the FP8 latent-KV cache ([blog] 1, named only): the OCP E4M3 row layout
+  R17 the FP8 latent-KV cache ([blog] 1, named only): the OCP E4M3 row layout
       of the FP8 section at the end of this file.
-  R13 compressed KV ([xLLM] 背景: compress_ratio in {1, 4, 128}; 5: the sparse
+  R18 compressed KV ([xLLM] 背景: compress_ratio in {1, 4, 128}; 5: the sparse
       metadata is built per ratio with the local geometry).  At ratio c a
       request of seq_len tokens has floor(seq_len / c) compressed entries
       (latent rows and index keys, given as inputs: the compressor is out of
@@ -76,7 +75,14 @@ design notes):
       entries.  Entries of all requests are stored in request order.  A query
       that sees no entry selects nothing and its output is zero.  c = 1 is
       the uncompressed path.
-  R15 sliding window (SWA; [xLLM] 背景 names it beside the compressed KV, and
+  R19 FP8 indexer operands (the FP8 path of [blog] 1 applied to the index
+      query and keys; the pages fix no format): each DI-wide index row (a key
+      k_I[s], or one head q_I[t, j]) is stored like an R17 cache row with
+      D = Dv = DI (codes, one fp32 scale per 128 columns, zero padding), and
+      stands for the real values decode(code) * scale, taken exactly (no
+      rounding to bf16).  The FP8 indexer score is the indexer score of those
+      values.
+  R20 sliding window (SWA; [xLLM] 背景 names it beside the compressed KV, and
       单层前向数据流 (4) gives the attention the original KV's geometry,
       cu_seqlens_ori_kv / seqused_kv, besides the sparse selection; nothing
       says how the two combine).  Reading taken: a query at position p also
@@ -85,14 +91,7 @@ design notes):
       entries and those window rows together; at c = 1 the entries are the
       original rows and a row both selected and in the window counts once.
       The original rows are every request's whole sequence in request order
-      (R9).  W = 0 is the plain sparse path.
-  R14 FP8 indexer operands (the FP8 path of [blog] 1 applied to the index
-      query and keys; the pages fix no format): each DI-wide index row (a key
-      k_I[s], or one head q_I[t, j]) is stored like an R12 cache row with
-      D = Dv = DI (codes, one fp32 scale per 128 columns, zero padding), and
-      stands for the real values decode(code) * scale, taken exactly (no
-      rounding to bf16).  The FP8 indexer score is the indexer score of those
-      values.
+      (R12).  W = 0 is the plain sparse path.
 
 parity pins: every function here is pinned by tests/test_oracle_pins.py
 against worked examples from the pages (tests/golden/), closed forms,
@@ -132,12 +131,12 @@ def local_rows(num_tokens: int, cp_size: int, cp_rank: int, mode: int) -> np.nda
       the flattened stream is cut evenly, padding at the end (R1, R2).
     round-robin: [blog] 2.B -- rank r holds arange(r, tokens, cp_size), i.e.
       token g goes to rank g % cp_size, slot g // cp_size (R3).
-    head-tail: the zigzag split of R11 ([xLLM] 7 names it only).
+    head-tail: the zigzag split of R2 ([xLLM] 7 names it only).
     """
     if not 0 <= cp_rank < cp_size:
         raise ValueError("cp_rank out of range")
     _, tpr = padded_geometry(num_tokens, cp_size)
-    head, tail = (tpr + 1) // 2, tpr // 2  # R11: head and tail chunk lengths
+    head, tail = (tpr + 1) // 2, tpr // 2  # R2: head and tail chunk lengths
     rows = np.full(tpr, -1, dtype=np.int64)
     for i in range(tpr):
         if mode == IN_SEQ_SPLIT:
@@ -174,14 +173,14 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
     ends at their last position (right-aligned) (R4).
     [xLLM] 5: batch_size / max_seqlen_q are replaced by the local geometry.
 
-    Extras (R8, R9): local_req_id (global request index), local_req_kv_base
+    Extras (R7, R12): local_req_id (global request index), local_req_kv_base
     (KV row of the request's position 0), local_req_pos_base (a local slot of
     flat query row g is at in-request position g - local_req_pos_base, i.e.
     qs_b minus the request's prefix) and local_token_pos (flat query row of
     every local slot, -1 for pad); num_tokens = T and num_kv_rows = the KV rows
     of the batch (the sum of seq_lens).
 
-    Compressed KV (R13) at ratio c: KV extents, KV bases and the KV row count
+    Compressed KV (R18) at ratio c: KV extents, KV bases and the KV row count
     count compressed entries: local_seq_lens = floor(extent / c) of the token
     extent above, request b's entries start at the sum of floor(seq_lens / c)
     before it; query positions stay in tokens.
@@ -198,7 +197,7 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
     for b in range(B):
         q_len = qsl[b + 1] - qsl[b]
         if q_len < 0 or sl[b] < q_len:
-            raise ValueError("seq_lens[b] must be at least the query length of request b (R9)")
+            raise ValueError("seq_lens[b] must be at least the query length of request b (R12)")
         prefix.append(sl[b] - q_len)
         kv_start.append(kv_start[-1] + sl[b] // c)
     T = qsl[B]
@@ -209,7 +208,7 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
         local_start = min(cp_rank * tpr, T)
         local_end = min((cp_rank + 1) * tpr, T)
     elif mode == HEAD_TAIL:
-        # the span from the head chunk's start to the tail chunk's end (R11)
+        # the span from the head chunk's start to the tail chunk's end (R2)
         head, tail = (tpr + 1) // 2, tpr // 2
         local_start = min(cp_rank * head, T)
         local_end = max(local_start, min(cp_size * head + (cp_size - cp_rank) * tail, T))
@@ -224,9 +223,9 @@ def build_local_metadata(query_start_loc, seq_lens, cp_size: int, cp_rank: int, 
         if not mine:
             continue  # R5
         q_lens.append(len(mine))
-        kv_lens.append((prefix[b] + max(mine) - qsl[b] + 1) // c)  # R4: last local position + 1 (R13: entries)
+        kv_lens.append((prefix[b] + max(mine) - qsl[b] + 1) // c)  # R4: last local position + 1 (R18: entries)
         req_id.append(b)
-        kv_base.append(kv_start[b])         # R9: KV row of position 0
+        kv_base.append(kv_start[b])         # R12: KV row of position 0
         pos_base.append(qsl[b] - prefix[b])  # position of flat row g = g - pos_base
 
     lqs = [0]
@@ -296,7 +295,7 @@ def rerange(y: np.ndarray, num_tokens: int, cp_size: int, mode: int) -> np.ndarr
 
 
 def all_to_all_heads(y: np.ndarray, num_tokens: int, cp_size: int, mode: int) -> np.ndarray:
-    """Head/token transpose of the views' attention outputs (R10).
+    """Head/token transpose of the views' attention outputs (R16).
 
     [xLLM] 单层前向数据流 (6) and "3. DSAttention 前向": each rank holds its
     attention output [T_local padded to tokens_per_rank, num_heads_full,
@@ -340,7 +339,7 @@ def indexer_scores(q_idx_row: np.ndarray, w_row: np.ndarray, k_idx_keys: np.ndar
 def topk_positions(scores: np.ndarray, k: int) -> np.ndarray:
     """The k positions with the largest scores, ties to the lower position.
 
-    R6: a row with n <= k keys selects all of them (never collapses to
+    R9: a row with n <= k keys selects all of them (never collapses to
     position 0, cf. [xLLM] 5 "top-k 塌缩到 position 0").  Otherwise the k-th
     largest value is the threshold; every position above it is selected and
     the remaining places go to the lowest positions equal to it.  numpy's
@@ -367,7 +366,7 @@ def sparse_attention(q_row: np.ndarray, kv_sel: np.ndarray, scale: float, Dv: in
       l[h, j] = scale * q[h] . kv[j]
       m[h]    = max(max_j l[h, j], sink[h])
       o[h]    = sum_j exp(l[h, j] - m[h]) kv[j, :Dv] / (sum_j exp(l[h, j] - m[h]) + exp(sink[h] - m[h]))
-    with the sink terms present only when a sink is given (R7).
+    with the sink terms present only when a sink is given (R10).
     """
     q = np.asarray(q_row, dtype=np.float64)
     kv = np.asarray(kv_sel, dtype=np.float64)
@@ -401,7 +400,7 @@ def view_row(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int,
     The local query of flat row g in request b, at in-request position
     p = g - local_req_pos_base (= g - qs_b without a prefix), sees the keys at
     positions 0 .. p of its own request, KV rows kv_base .. kv_base + p
-    (causal, same request; R8, R9).  At compress ratio c (R13) it sees the
+    (causal, same request; R7, R12).  At compress ratio c (R18) it sees the
     entries 0 .. floor((p + 1) / c) - 1 instead; with none, nothing is selected
     and the output is zero.
     """
@@ -444,7 +443,7 @@ def prefill(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mod
     """The whole prefill through cp_size views: split the local tensors, run
     every view with full KV and index keys, rerange the outputs to flat order
     ([xLLM] 单层前向数据流: q local, KV full).  q, q_idx, w hold the T query
-    tokens; kv and k_idx the KV rows of every request's whole sequence (R9;
+    tokens; kv and k_idx the KV rows of every request's whole sequence (R12;
     the same T rows when seq_lens equal the query lengths).  Returns
     out [T, H, Dv] fp64."""
     q = np.asarray(q, dtype=np.float64)
@@ -461,10 +460,10 @@ def prefill(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mod
 
 
 # --------------------------------------------------------------------------
-# FP8 latent-KV cache (R12)
+# FP8 latent-KV cache (R17)
 # --------------------------------------------------------------------------
 #
-# R12 "FP8 KV Cache" ([blog] 1 核心改动总结: round-robin-split lifts the old
+# R17 "FP8 KV Cache" ([blog] 1 核心改动总结: round-robin-split lifts the old
 #     restriction that NSA prefill CP could not use an FP8 KV cache) is named
 #     without a format.  Reading taken: the published DeepSeek-V3.2 layout of
 #     one latent row -- the Dv value ("nope") columns as OCP FP8 E4M3 codes with
@@ -566,7 +565,7 @@ def kv_fp8_dequantize(cache, D: int, Dv: int) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# FP8 indexer operands (R14)
+# FP8 indexer operands (R19)
 # --------------------------------------------------------------------------
 
 def index_fp8_values(rows, DI: int) -> np.ndarray:
@@ -592,7 +591,7 @@ def indexer_scores_fp8(q_idx_row8, w_row, k_idx_keys8, DI: int) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# Sliding window over the original KV (R15)
+# Sliding window over the original KV (R20)
 # --------------------------------------------------------------------------
 
 def window_rows(p: int, ori_start: int, window: int) -> np.ndarray:
@@ -605,7 +604,7 @@ def window_rows(p: int, ori_start: int, window: int) -> np.ndarray:
 
 def view_row_swa(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: int, scale: float, Dv: int,
                  window: int, kv_ori, ori_starts, sink=None):
-    """One local slot with the sliding window (R15): the selection of view_row
+    """One local slot with the sliding window (R20): the selection of view_row
     over the (compressed) rows ``kv``, plus the window rows of ``kv_ori``
     (the original rows; request b starts at ori_starts[b]), one softmax over
     both.  Returns (selected rows, window rows, output fp64 [H, Dv]); (None,
@@ -628,7 +627,7 @@ def view_row_swa(md: dict, slot: int, q_loc, q_idx_loc, w_loc, kv, k_idx, topk: 
 
 def prefill_swa(q, kv, q_idx, k_idx, w, query_start_loc, seq_lens, cp_size: int, mode: int, topk: int,
                 scale: float, Dv: int, window: int, kv_ori=None, sink=None, compress_ratio: int = 1):
-    """prefill with the sliding window (R15): ``kv`` / ``k_idx`` are the rows
+    """prefill with the sliding window (R20): ``kv`` / ``k_idx`` are the rows
     the indexer selects from (compressed entries at compress_ratio > 1),
     ``kv_ori`` the original rows of every request's whole sequence (``kv``
     itself when omitted, as at c = 1).  Returns out [T, H, Dv] fp64."""

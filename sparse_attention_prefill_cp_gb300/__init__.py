@@ -22,7 +22,7 @@ HEAD_TAIL = 2
 __all__ = [
     "IN_SEQ_SPLIT", "ROUND_ROBIN", "HEAD_TAIL", "DSAError", "CPLocalMetadata", "load",
     "dsa_cp_geometry", "dsa_cp_metadata_sizes", "dsa_cp_build_local_metadata", "dsa_cp_split",
-    "dsa_cp_rerange", "dsa_cp_all_to_all_heads", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk",
+    "dsa_cp_rerange", "dsa_cp_split_from_host", "dsa_cp_rerange_to_host", "dsa_cp_all_to_all_heads", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk",
     "dsa_indexer_scores", "dsa_indexer_fp8_rows", "dsa_indexer_topk_fp8", "dsa_indexer_scores_fp8",
     "dsa_sparse_attn_prefill", "dsa_sparse_attn_prefill_headsharded", "dsa_poll_device_error",
 ]
@@ -154,6 +154,43 @@ def dsa_cp_rerange(src: torch.Tensor, num_tokens: int, cp_size: int, mode: int, 
     check(load().dsa_cp_rerange(_ptr(src), row, num_tokens, cp_size, mode, _ptr(out), _stream(stream)),
           "dsa_cp_rerange")
     return out
+
+
+def _host_rows(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host (CPU) tensor, page-locked for asynchronous copies")
+    return t
+
+
+def dsa_cp_split_from_host(host_src: torch.Tensor, cp_size: int, mode: int, cp_rank: int, out: torch.Tensor,
+                           stream=None) -> torch.Tensor:
+    """Rows of rank ``cp_rank`` of host_src [T, ...] (host memory) -> out
+    [tpr, ...] (device) by the copy engines; pad rows of ``out`` untouched."""
+    _host_rows(host_src, "host_src")
+    T = host_src.shape[0]
+    _, tpr = dsa_cp_geometry(T, cp_size)
+    shape = (tpr,) + tuple(host_src.shape[1:])
+    if not out.is_cuda or tuple(out.shape) != shape or out.dtype != host_src.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous CUDA {host_src.dtype} tensor of shape {shape}")
+    check(load().dsa_cp_split_from_host(_ptr(host_src), _row_bytes(host_src), T, cp_size, mode, cp_rank, _ptr(out),
+                                        _stream(stream)), "dsa_cp_split_from_host")
+    return out
+
+
+def dsa_cp_rerange_to_host(src: torch.Tensor, num_tokens: int, cp_size: int, mode: int, cp_rank: int,
+                           host_out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Rank ``cp_rank``'s rows src [tpr, ...] (device) -> their token rows of
+    host_out [num_tokens, ...] (host memory) by the copy engines."""
+    _host_rows(host_out, "host_out")
+    if not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    _, tpr = dsa_cp_geometry(num_tokens, cp_size)
+    if src.shape[0] != tpr or tuple(host_out.shape) != (num_tokens,) + tuple(src.shape[1:]) or \
+            host_out.dtype != src.dtype:
+        raise ValueError("src must be [tpr, ...] and host_out [num_tokens, ...] of the same row shape and dtype")
+    check(load().dsa_cp_rerange_to_host(_ptr(src), _row_bytes(src), num_tokens, cp_size, mode, cp_rank,
+                                        _ptr(host_out), _stream(stream)), "dsa_cp_rerange_to_host")
+    return host_out
 
 
 def dsa_cp_all_to_all_heads(src: torch.Tensor, num_tokens: int, cp_size: int, mode: int,

@@ -38,6 +38,10 @@ SIGNATURES = {
     "dsa_cp_split": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_int32, C.c_void_p,
                                c_stream]),
     "dsa_cp_rerange": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_void_p, c_stream]),
+    "dsa_cp_split_from_host": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_int32,
+                                         C.c_void_p, c_stream]),
+    "dsa_cp_rerange_to_host": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int, C.c_int32,
+                                         C.c_void_p, c_stream]),
     "dsa_cp_all_to_all_heads": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int,
                                           C.c_void_p, c_stream]),
     "dsa_indexer_topk_workspace_size": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_size_t)]),

@@ -168,3 +168,81 @@ extern "C" dsa_status dsa_cp_all_to_all_heads(const void *src, int32_t num_heads
   return launch_copy(src, dst, slice_bytes, static_cast<int64_t>(cp_size) * num_tokens, map,
                      reinterpret_cast<cudaStream_t>(stream));
 }
+
+// ------------------------------------------------------------------ one rank's rows to / from host memory
+// A rank's slots are at most two runs of consecutive slots whose flat rows are
+// evenly spaced (in-seq: one contiguous run; round-robin: one run of stride
+// cp; head-tail: the head run and the tail run).  Each run is one 2D copy of
+// the copy engines: rows of row_bytes, the flat side pitched by stride rows.
+namespace dsa {
+namespace {
+
+struct RowRun {
+  int64_t slot0, row0, n, stride;  // slots [slot0, slot0 + n) <-> flat rows row0 + k * stride
+};
+
+int rank_runs(int64_t T, int64_t tpr, int64_t cp, int64_t r, int mode, RowRun runs[2]) {
+  auto clamp_n = [](int64_t v, int64_t hi) { return v < 0 ? int64_t{0} : (v > hi ? hi : v); };
+  if (mode == DSA_CP_IN_SEQ_SPLIT) {
+    runs[0] = {0, r * tpr, clamp_n(T - r * tpr, tpr), 1};
+    return 1;
+  }
+  if (mode == DSA_CP_ROUND_ROBIN) {
+    runs[0] = {0, r, r < T ? clamp_n((T - r + cp - 1) / cp, tpr) : 0, cp};
+    return 1;
+  }
+  const int64_t h = (tpr + 1) / 2, t = tpr / 2;
+  runs[0] = {0, r * h, clamp_n(T - r * h, h), 1};
+  const int64_t tail0 = cp * h + (cp - 1 - r) * t;
+  runs[1] = {h, tail0, clamp_n(T - tail0, t), 1};
+  return 2;
+}
+
+dsa_status host_rows_copy(const void *src, void *dst, int64_t row_bytes, int32_t num_tokens, int32_t cp_size,
+                          dsa_cp_mode mode, int32_t cp_rank, bool to_device, cudaStream_t stream) {
+  if (!src || !dst) return DSA_ERR_INVALID_ARG;
+  if (mode != DSA_CP_IN_SEQ_SPLIT && mode != DSA_CP_ROUND_ROBIN && mode != DSA_CP_HEAD_TAIL)
+    return DSA_ERR_INVALID_ARG;
+  if (cp_size < 1 || cp_rank < 0 || cp_rank >= cp_size) return DSA_ERR_INVALID_ARG;
+  if (row_bytes <= 0 || num_tokens < 0) return DSA_ERR_SHAPE;
+  int32_t pad = 0, tpr = 0;
+  dsa_status st = dsa_cp_geometry(num_tokens, cp_size, &pad, &tpr);
+  if (st != DSA_OK) return st;
+  if (row_bytes > (int64_t{1} << 40) / (static_cast<int64_t>(cp_size) * (static_cast<int64_t>(pad) + 1)))
+    return DSA_ERR_SHAPE;
+  RowRun runs[2];
+  const int nr = rank_runs(num_tokens, tpr, cp_size, cp_rank, static_cast<int>(mode), runs);
+  for (int k = 0; k < nr; ++k) {
+    const RowRun &u = runs[k];
+    if (u.n == 0) continue;
+    const size_t w = static_cast<size_t>(row_bytes), flat_pitch = static_cast<size_t>(u.stride * row_bytes);
+    const char *s = static_cast<const char *>(src);
+    char *d = static_cast<char *>(dst);
+    cudaError_t e;
+    if (to_device)
+      e = cudaMemcpy2DAsync(d + u.slot0 * row_bytes, w, s + u.row0 * row_bytes, flat_pitch, w,
+                            static_cast<size_t>(u.n), cudaMemcpyHostToDevice, stream);
+    else
+      e = cudaMemcpy2DAsync(d + u.row0 * row_bytes, flat_pitch, s + u.slot0 * row_bytes, w, w,
+                            static_cast<size_t>(u.n), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_cp_split_from_host(const void *host_src, int64_t row_bytes, int32_t num_tokens,
+                                             int32_t cp_size, dsa_cp_mode mode, int32_t cp_rank, void *dst,
+                                             dsa_stream_t stream) {
+  return host_rows_copy(host_src, dst, row_bytes, num_tokens, cp_size, mode, cp_rank, true,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsa_status dsa_cp_rerange_to_host(const void *src, int64_t row_bytes, int32_t num_tokens,
+                                             int32_t cp_size, dsa_cp_mode mode, int32_t cp_rank, void *host_dst,
+                                             dsa_stream_t stream) {
+  return host_rows_copy(src, host_dst, row_bytes, num_tokens, cp_size, mode, cp_rank, false,
+                        reinterpret_cast<cudaStream_t>(stream));
+}

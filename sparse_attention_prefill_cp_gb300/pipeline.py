@@ -21,7 +21,8 @@ from __future__ import annotations
 import torch
 
 from . import (CPLocalMetadata, dsa_cp_all_to_all_heads, dsa_cp_build_local_metadata, dsa_cp_geometry,
-               dsa_cp_rerange, dsa_cp_split, dsa_indexer_topk, dsa_indexer_topk_fp8,
+               dsa_cp_rerange, dsa_cp_rerange_to_host, dsa_cp_split, dsa_cp_split_from_host, dsa_indexer_topk,
+               dsa_indexer_topk_fp8,
                dsa_indexer_topk_workspace_size, dsa_kv_fp8_dequantize, dsa_kv_fp8_row_bytes, dsa_sparse_attn_prefill, dsa_sparse_attn_prefill_flat,
                dsa_sparse_attn_prefill_headsharded)
 
@@ -249,78 +250,131 @@ class DSAPrefill:
 
 
 class HostStreamedPrefill:
-    """Prefill batches that live in pinned host memory, with the copies
-    overlapped: while batch s computes, the inputs of batch s + 1 go up on one
-    copy stream and the output of batch s - 1 comes down on another.
+    """Prefill batches whose inputs and output live in page-locked host memory,
+    streamed one CP view at a time so that copies and compute overlap.
 
-    ``depth`` sets of device buffers (one ``DSAPrefill`` each, inputs and
-    outputs) rotate, so a set is reused only after its last batch's output has
-    been read back.  ``submit`` only enqueues work; the caller synchronises (or
-    waits on ``done_event(s)``) before reading the host output of batch s.
-    Every compute step is the same sequence of library calls as
-    ``DSAPrefill.run``.
+    Per batch: the full-token inputs every view reads (kv, k_idx, w and the
+    sink) go up first and w is split on the device; then, for each view r, the
+    copy engines take r's rows of q and q_idx straight from the host tensors
+    into a view buffer (dsa_cp_split_from_host: the split done by the copy
+    itself), the view's indexer + top-k and attention run into a view output
+    buffer, and its rows go back to their token rows of the host output
+    (dsa_cp_rerange_to_host: the rerange done by the copy).  ``depth`` view
+    buffer sets rotate, so while view r computes, the rows of the next views
+    go up and the output of the previous one comes down; consecutive batches
+    chain the same way (the full-token buffers alternate between two sets).
+    Streams: one for uploads, one for compute, one for read-back.
+
+    ``submit`` only enqueues work; wait on ``done_event(s)`` (or synchronise)
+    before reading batch s's host output.  The kernels and their arguments are
+    those of ``DSAPrefill.run`` with the view layout, so the output is the
+    same bit for bit.
     """
 
     INPUTS = ("q", "kv", "q_idx", "k_idx", "w", "sink")
 
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
-                 softmax_scale: float, device=None, depth: int = 2, view_streams: int = 1, prefix_lens=None,
-                 fused: bool = False):
+                 softmax_scale: float, device=None, depth: int = 3, prefix_lens=None):
         if depth < 1:
             raise ValueError("depth must be at least 1")
-        self.pipes = [DSAPrefill(lengths, cp_size, mode, H, D, Dv, HI, DI, topk, softmax_scale, device,
-                                 view_streams=view_streams, prefix_lens=prefix_lens, fused=fused)
-                      for _ in range(depth)]
-        self.device = self.pipes[0].device
+        self.device = torch.device(device or "cuda")
+        dev = self.device
+        self.lengths = [int(x) for x in lengths]
+        self.prefix_lens = [0] * len(self.lengths) if prefix_lens is None else [int(x) for x in prefix_lens]
+        self.cp_size, self.mode = int(cp_size), int(mode)
+        self.H, self.D, self.Dv, self.HI, self.DI, self.topk = H, D, Dv, HI, DI, topk
+        self.scale = float(softmax_scale)
+        self.T, self.B = sum(self.lengths), len(self.lengths)
+        kv_lens = [n + p for n, p in zip(self.lengths, self.prefix_lens)]
+        self.num_kv_rows, self.max_kv_len = sum(kv_lens), max(1, max(kv_lens))
+        self.pad, self.tpr = dsa_cp_geometry(self.T, cp_size)
+        qsl = [0]
+        for n in self.lengths:
+            qsl.append(qsl[-1] + n)
+        self.query_start_loc = torch.tensor(qsl, dtype=torch.int32, device=dev)
+        self.seq_lens = torch.tensor(kv_lens, dtype=torch.int32, device=dev)
+        self.md = [CPLocalMetadata(self.B, self.T, cp_size, dev) for _ in range(cp_size)]
+        tpr = self.tpr
         self.depth = depth
-        self.dev_in = [None] * depth
-        self.h2d = torch.cuda.Stream(self.device)
-        self.d2h = torch.cuda.Stream(self.device)
+        # view buffer sets; pad rows stay zero (the host copies never write them)
+        self.q_v = [torch.zeros((tpr, H, D), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.qi_v = [torch.zeros((tpr, HI, DI), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.out_v = [torch.empty((tpr, H, Dv), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.topk_idx = torch.empty((tpr, topk), dtype=torch.int32, device=dev)
+        self.workspace = torch.empty(dsa_indexer_topk_workspace_size(tpr, self.max_kv_len, topk), dtype=torch.uint8,
+                                     device=dev)
+        self.full = [None, None]      # full-token device inputs, by batch parity
+        self.w_split = [torch.empty((cp_size, tpr, HI), dtype=torch.float32, device=dev) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(dev)
+        self.compute = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.full_ready = [torch.cuda.Event() for _ in range(2)]
+        self.full_free = [torch.cuda.Event() for _ in range(2)]
+        self.in_ready = [torch.cuda.Event() for _ in range(depth)]
         self.computed = [torch.cuda.Event() for _ in range(depth)]
         self.read_back = [torch.cuda.Event() for _ in range(depth)]
-        self.in_ready = [torch.cuda.Event() for _ in range(depth)]
         self._done = {}
         self._submitted = 0
+        self._views = 0  # views enqueued so far (the buffer set of view v is v % depth)
 
-    def _inputs(self, k, host):
-        if self.dev_in[k] is None:
-            self.dev_in[k] = {n: (torch.empty(host[n].shape, dtype=host[n].dtype, device=self.device)
-                                  if host.get(n) is not None else None) for n in self.INPUTS}
-        return self.dev_in[k]
+    def _full_inputs(self, b, host):
+        if self.full[b] is None:
+            self.full[b] = {n: (torch.empty(host[n].shape, dtype=host[n].dtype, device=self.device)
+                                if host.get(n) is not None else None) for n in ("kv", "k_idx", "w", "sink")}
+        return self.full[b]
 
     def submit(self, host: dict, out_host: torch.Tensor, stream=None) -> int:
         """Enqueue one batch: ``host`` maps q, kv, q_idx, k_idx, w (and sink or
-        None) to pinned CPU tensors; ``out_host`` is a pinned CPU tensor
-        [T, H, Dv] bf16 that receives the output.  Returns the batch number."""
-        s = self._submitted
-        k = s % self.depth
-        pipe = self.pipes[k]
+        None) to page-locked CPU tensors; ``out_host`` is a page-locked CPU
+        tensor [T, H, Dv] bf16 that receives the output.  ``stream``: the
+        stream whose prior work the batch waits for (default: the current
+        stream).  Returns the batch number."""
         for n in self.INPUTS:
             t = host.get(n)
             if t is not None and (t.device.type != "cpu" or not t.is_pinned()):
-                raise ValueError(f"{n}: pinned host memory expected")
+                raise ValueError(f"{n}: page-locked host memory expected")
         if out_host.device.type != "cpu" or not out_host.is_pinned():
-            raise ValueError("out_host: pinned host memory expected")
-        compute = stream or torch.cuda.current_stream(self.device)
-        dev = self._inputs(k, host)
-        first_use = s < self.depth
-        # inputs of set k: free once the batch that used them has computed
-        if not first_use:
-            self.h2d.wait_event(self.computed[k])
+            raise ValueError("out_host: page-locked host memory expected")
+        s = self._submitted
+        b = s % 2
+        cp, mode, T = self.cp_size, self.mode, self.T
+        caller = stream or torch.cuda.current_stream(self.device)
+        full = self._full_inputs(b, host)
+        # the full-token inputs of batch parity b are free once batch s - 2's views have run
+        self.h2d.wait_stream(caller)
+        if s >= 2:
+            self.h2d.wait_event(self.full_free[b])
         with torch.cuda.stream(self.h2d):
-            for n in self.INPUTS:
-                if dev[n] is not None:
-                    dev[n].copy_(host[n], non_blocking=True)
-        self.in_ready[k].record(self.h2d)
-        compute.wait_event(self.in_ready[k])
-        if not first_use:
-            compute.wait_event(self.read_back[k])  # the output buffer of set k has been read back
-        out = pipe.run(dev["q"], dev["kv"], dev["q_idx"], dev["k_idx"], dev["w"], dev["sink"], stream=compute)
-        self.computed[k].record(compute)
-        self.d2h.wait_event(self.computed[k])
-        with torch.cuda.stream(self.d2h):
-            out_host.copy_(out, non_blocking=True)
-        self.read_back[k].record(self.d2h)
+            for n, t in full.items():
+                if t is not None:
+                    t.copy_(host[n], non_blocking=True)
+        self.full_ready[b].record(self.h2d)
+        comp = self.compute
+        comp.wait_event(self.full_ready[b])
+        for r in range(cp):                                                            # a1
+            dsa_cp_build_local_metadata(self.query_start_loc, self.seq_lens, T, cp, r, mode, self.md[r], comp)
+        dsa_cp_split(full["w"], cp, mode, -1, self.w_split[b], comp)                   # a2 (w)
+        for r in range(cp):
+            v = self._views
+            k = v % self.depth
+            if v >= self.depth:  # view v - depth has read set k's inputs
+                self.h2d.wait_event(self.computed[k])
+            dsa_cp_split_from_host(host["q"], cp, mode, r, self.q_v[k], self.h2d)      # a2 (q, q_idx)
+            dsa_cp_split_from_host(host["q_idx"], cp, mode, r, self.qi_v[k], self.h2d)
+            self.in_ready[k].record(self.h2d)
+            comp.wait_event(self.in_ready[k])
+            if v >= self.depth:  # view v - depth's output has been read back
+                comp.wait_event(self.read_back[k])
+            dsa_indexer_topk(self.md[r], self.qi_v[k], full["k_idx"], self.w_split[b][r], self.topk,  # a3 + a4
+                             self.max_kv_len, self.topk_idx, self.workspace, comp)
+            dsa_sparse_attn_prefill(self.md[r], self.q_v[k], full["kv"], self.topk_idx, self.scale, self.Dv,  # a5
+                                    full["sink"], self.out_v[k], comp)
+            self.computed[k].record(comp)
+            self.d2h.wait_event(self.computed[k])
+            dsa_cp_rerange_to_host(self.out_v[k], T, cp, mode, r, out_host, self.d2h)  # a6
+            self.read_back[k].record(self.d2h)
+            self._views += 1
+        self.full_free[b].record(comp)
         done = torch.cuda.Event(enable_timing=True)
         done.record(self.d2h)
         self._done[s] = done
@@ -328,5 +382,5 @@ class HostStreamedPrefill:
         return s
 
     def done_event(self, s: int) -> torch.cuda.Event:
-        """Recorded on the copy-out stream once batch s's output is on the host."""
+        """Recorded on the read-back stream once batch s's output is on the host."""
         return self._done[s]

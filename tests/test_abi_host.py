@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 5
+    assert lib.dsa_abi_version() == 6
     for code, name in _lib.STATUS.items():
         assert lib.dsa_status_string(code).decode().startswith(name)
 
@@ -155,3 +155,20 @@ def test_fp8_indexer_validation(lib):
     n = C.c_size_t()
     assert lib.dsa_kv_fp8_row_bytes(128, 128, C.byref(n)) == 0 and n.value == 144 == O.kv_fp8_row_bytes(128, 128)
 
+
+
+def test_host_row_copies_validation(lib):
+    # one rank's rows between host memory and the device: null pointers, bad
+    # mode or rank (-1 = all ranks is not a host-copy rank), bad sizes; all
+    # answered on the host before any copy is issued
+    p = C.c_void_p(0x10000)
+    for fn in (lib.dsa_cp_split_from_host, lib.dsa_cp_rerange_to_host):
+        assert fn(None, 16, 10, 2, 0, 0, p, None) == 1
+        assert fn(p, 16, 10, 2, 0, 0, None, None) == 1
+        assert fn(p, 16, 10, 2, 9, 0, p, None) == 1
+        assert fn(p, 16, 10, 2, 0, -1, p, None) == 1
+        assert fn(p, 16, 10, 2, 0, 2, p, None) == 1
+        assert fn(p, 16, 10, 0, 0, 0, p, None) == 1
+        assert fn(p, 0, 10, 2, 0, 0, p, None) == 2
+        assert fn(p, 16, -3, 2, 0, 0, p, None) == 2
+        assert fn(p, 1 << 40, 10, 2, 1, 0, p, None) == 2

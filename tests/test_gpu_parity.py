@@ -128,6 +128,44 @@ def test_split_rerange_bit_exact(T, cp, row_shape, dtype, mode):
 
 # ------------------------------------------------------------------ head/token all-to-all
 
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T,cp,row_shape,dtype", [
+    (11805, 4, (64,), torch.float32),          # w-like 256-byte rows
+    (257, 2, (64, 128), torch.bfloat16),       # q_idx-like 16 KB rows
+    (37, 16, (128, 576), torch.bfloat16),      # attention-q rows (147,456 B), empty and ragged views
+    (13, 4, (3,), torch.uint8),                # odd byte rows
+    (1, 8, (5,), torch.int32),                 # one token, seven empty views
+])
+def test_split_from_host_and_rerange_to_host_bit_exact(T, cp, row_shape, dtype, mode):
+    # the copy-engine split / rerange of one rank's rows between host memory
+    # and the device: every real slot equals the oracle's split, pad slots are
+    # not written, and the read-back puts every row at its token
+    g = torch.Generator().manual_seed(T * 11 + cp)
+    if dtype.is_floating_point:
+        x = torch.randn((T,) + row_shape, generator=g).to(dtype)
+    else:
+        x = torch.randint(0, 100, (T,) + row_shape, generator=g).to(dtype)
+    host = x.pin_memory()
+    ref = O.split(x.view(torch.uint8).numpy() if dtype == torch.bfloat16 else x.numpy(), cp, mode)
+    _, tpr = O.padded_geometry(T, cp)
+    back = torch.zeros_like(x).pin_memory()
+    for r in range(cp):
+        dst = torch.full((tpr,) + row_shape, 0, dtype=dtype, device="cuda")
+        dst.view(torch.uint8).fill_(7)
+        dsa.dsa_cp_split_from_host(host, cp, mode, r, dst)
+        got = dst.cpu()
+        rows = O.local_rows(T, cp, r, mode)
+        for i, gr in enumerate(rows):
+            gb = got[i].view(torch.uint8) if dtype == torch.bfloat16 else got[i]
+            if gr >= 0:
+                assert np.array_equal(gb.numpy(), ref[r, i]), (r, i)
+            else:
+                assert torch.all(got[i].reshape(-1).view(torch.uint8) == 7), (r, i)  # pad slot untouched
+        dsa.dsa_cp_rerange_to_host(dst, T, cp, mode, r, back)
+    torch.cuda.synchronize()
+    assert torch.equal(back, x)
+
+
 def _a2a_reference(y, T, cp, mode):
     """[cp, tpr, H, Dv] -> [cp, T, H / cp, Dv] with torch's index_select on the
     oracle's slot of every token (used where the full oracle is too large)."""
@@ -325,7 +363,7 @@ def test_views_reproduce_single_view_bitwise(wl, mode):
     assert torch.equal(out_views, out_single)
 
 
-@pytest.mark.parametrize("mode", (IN_SEQ_SPLIT, ROUND_ROBIN))
+@pytest.mark.parametrize("mode", MODES)
 def test_view_streams_and_host_streaming_are_bit_identical(mode):
     # the same library calls on other streams: views spread over two streams,
     # and batches streamed from pinned host memory with overlapped copies,
@@ -341,7 +379,7 @@ def test_view_streams_and_host_streaming_are_bit_identical(mode):
     for x, ref in zip(xs, refs):
         assert torch.equal(pipe2.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"]), ref)
     hs = HostStreamedPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
-                             depth=2, view_streams=2)
+                             depth=2)
     hosts = [{k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()} for x in xs]
     outs = [torch.empty((wl.num_tokens, wl.H, wl.Dv), dtype=torch.bfloat16).pin_memory() for _ in range(5)]
     ids = [hs.submit(hosts[b % 3], outs[b]) for b in range(5)]

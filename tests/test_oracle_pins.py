@@ -445,7 +445,7 @@ def test_short_rows_select_everything():
     assert np.all(idx[200] >= 0) and np.all(np.diff(idx[200]) > 0) and idx[200].max() <= 200
 
 
-# ---------------------------------------------------------------- FP8 latent-KV cache (R12)
+# ---------------------------------------------------------------- FP8 latent-KV cache (R17)
 # The pages name an FP8 KV cache without a format; the reading is the OCP E4M3
 # code with per-128-column fp32 scales and bf16 rope columns.  Pins: values the
 # E4M3 format fixes, torch's own float8_e4m3fn conversion (a library routine),
@@ -520,7 +520,7 @@ def test_kv_fp8_cache_layout_and_error_bound(D, Dv):
     assert np.all(c[7, :Dv] == 0) and np.all(d[7] == 0)
 
 
-# ---------------------------------------------------------------- FP8 indexer operands (R14)
+# ---------------------------------------------------------------- FP8 indexer operands (R19)
 # Index rows in the FP8 cache row format with D = Dv = DI; the score is the
 # indexer score of decode(code) * scale.  Pins: the hand example with its
 # operands as hand-encoded bytes, a closed form with distinct per-row scales,
@@ -592,7 +592,7 @@ def test_indexer_fp8_exact_where_quantisation_is_exact():
     assert np.all(np.abs(s8 - s) <= bound) and not np.array_equal(s8, s)
 
 
-# ---------------------------------------------------------------- compressed KV (R13)
+# ---------------------------------------------------------------- compressed KV (R18)
 
 _COMPRESSED_CASES = {"C": ([9, 6], [9, 6], 2, 4), "D": ([5, 3], [135, 3], 2, 128)}  # q_lens, seq_lens, cp, c
 
@@ -677,7 +677,7 @@ def test_compressed_metadata_extents(mode):
     assert widest == [n // c for n in seq_lens]
 
 
-# ---------------------------------------------------------------- sliding window (R15)
+# ---------------------------------------------------------------- sliding window (R20)
 # A query at position p also attends to the original rows of positions
 # max(0, p - W + 1) .. p; one softmax over the selected entries and the window
 # rows (a row both selected and in the window counts once at c = 1).

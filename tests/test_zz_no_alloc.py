@@ -11,13 +11,16 @@ import torch
 
 import sparse_attention_prefill_cp_gb300 as dsa
 from sparse_attention_prefill_cp_gb300.pipeline import DSAPrefill
-from workloads import IN_SEQ_SPLIT, ROUND_ROBIN, LONG_8K, TINY, draw_inputs
+from workloads import IN_SEQ_SPLIT, ROUND_ROBIN, LONG_8K, TINY, draw_index_inputs, draw_inputs
 
 pytestmark = pytest.mark.gpu
 
 CASES = [
     (TINY, IN_SEQ_SPLIT),
     (LONG_8K.with_(name="noalloc-full-2x", lengths=(2500, 700), cp_size=2, seed=21), ROUND_ROBIN),
+    # 4096 query rows of 8192-key scores (128 MiB) per view: four passes over
+    # the 32 MiB array within one call
+    (LONG_8K.with_(name="noalloc-multipass", cp_size=2, seed=22), IN_SEQ_SPLIT),
 ]
 
 
@@ -31,10 +34,11 @@ def _gpu():
 @pytest.mark.parametrize("wl,mode", CASES, ids=lambda v: getattr(v, "name", str(v)))
 def test_noalloc_matches_workspace_entry_point_twice(wl, mode):
     for call in range(2):
-        x = {k: (v.cuda() if v is not None else None) for k, v in draw_inputs(wl, seed_offset=call).items()}
-        pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale)
+        x = draw_index_inputs(wl, device="cuda", seed_offset=call)
+        pipe = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                          fused=True)
         pipe.metadata()
-        pipe.split(x["q"], x["q_idx"], x["w"])
+        pipe.split(None, x["q_idx"], x["w"])
         for r in range(wl.cp_size):
             ref = dsa.dsa_indexer_topk(pipe.md[r], pipe.qi_split[r], x["k_idx"], pipe.w_split[r], wl.topk,
                                        pipe.max_kv_len)
