@@ -297,25 +297,28 @@ def e2e_leg(args, wl, mode, dev, x, pk):
     e2e_ms = e0.elapsed_time(e1) / n
     dsa.dsa_poll_device_error()
 
-    # the same bytes through the copy engines alone: full-token inputs, then
-    # per view its q and q_idx rows up and its output rows down, on the same
-    # two copy streams (view v's read-back after view v's upload)
-    cp = wl.cp_size
-    full = {k: torch.empty_like(x[k]) for k in ("kv", "k_idx", "w")}
-    qv, qiv, ov = streamed.q_v[0], streamed.qi_v[0], streamed.out_v[0]
+    # the same bytes through the copy engines alone, on the same two copy
+    # streams: full-token inputs, then per chunk its q, q_idx and w rows up
+    # and its output rows down (a chunk's read-back after its upload)
+    full = {k: torch.empty_like(x[k]) for k in ("kv", "k_idx")}
+    qc, qic, wc, oc = streamed.q_c[0], streamed.qi_c[0], streamed.w_c[0], streamed.out_c[0]
     up, down = streamed.h2d, streamed.d2h
 
     def copies():
         with torch.cuda.stream(up):
             for k, t in full.items():
                 t.copy_(host[k], non_blocking=True)
-        for r in range(cp):
-            dsa.dsa_cp_split_from_host(host["q"], cp, mode, r, qv, up)
-            dsa.dsa_cp_split_from_host(host["q_idx"], cp, mode, r, qiv, up)
+        for (t0, t1) in streamed.chunks:
+            n = t1 - t0
+            with torch.cuda.stream(up):
+                qc[:n].copy_(host["q"][t0:t1], non_blocking=True)
+                qic[:n].copy_(host["q_idx"][t0:t1], non_blocking=True)
+                wc[:n].copy_(host["w"][t0:t1], non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(up)
             down.wait_event(ev)
-            dsa.dsa_cp_rerange_to_host(ov, wl.num_tokens, cp, mode, r, out_host, down)
+            with torch.cuda.stream(down):
+                out_host[t0:t1].copy_(oc[:n], non_blocking=True)
 
     copies()
     torch.cuda.synchronize()
@@ -327,15 +330,18 @@ def e2e_leg(args, wl, mode, dev, x, pk):
     c1.record(down)
     torch.cuda.synchronize()
     copy_ms = c0.elapsed_time(c1) / n
+    chunk_tokens, n_chunks = streamed.chunk_tokens, len(streamed.chunks)
     del streamed, full, host, out_host
     torch.cuda.empty_cache()
     return {
         "value": wl.num_tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
         "ms_per_step": e2e_ms, "batches": n,
         "how": "page-locked host inputs -> device -> output back to page-locked host, every batch: full-token inputs "
-               "(kv, k_idx, w, sink) up first, then per CP view its q and q_idx rows taken up by the copy engines "
-               "(dsa_cp_split_from_host) while earlier views compute, and its output rows copied back into token "
-               "order (dsa_cp_rerange_to_host); HostStreamedPrefill, 3 view buffer sets",
+               "(kv, k_idx, sink) up first, then the token stream in chunks of contiguous rows: a chunk's q, q_idx "
+               "and w go up while earlier chunks compute (every view's slots in the chunk: dsa_indexer_topk_rows, "
+               "dsa_sparse_attn_prefill_rows) and its output rows come back; HostStreamedPrefill, 3 chunk buffer "
+               "sets, views over 2 compute streams",
+        "chunk_tokens": chunk_tokens, "chunks_per_batch": n_chunks,
         "copies_only_ms_per_step": copy_ms,
         "copies_gbs": (h2d + d2h) / (copy_ms / 1e3) / 1e9,
     }

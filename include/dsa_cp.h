@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define DSA_CP_ABI_VERSION 6
+#define DSA_CP_ABI_VERSION 8
 
 typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 
@@ -289,6 +289,20 @@ dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t batch, int3
                             void *workspace, size_t ws_bytes, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_topk over a range of the view's slots, [slot_begin,
+ * slot_begin + slot_count): q_idx_rows bf16 [slot_count][HI][DI] and w_rows
+ * fp32 [slot_count][HI] hold those slots' rows, topk_rows int32
+ * [slot_count][topk] receives theirs; the metadata, keys and results are
+ * those of dsa_indexer_topk (the same rows of its output).  For inputs that
+ * arrive in pieces (a chunk of the token stream at a time).  0 <= slot_begin,
+ * slot_begin + slot_count <= tpr.
+ */
+dsa_status dsa_indexer_topk_rows(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr, int32_t max_kv_len,
+                                 int32_t slot_begin, int32_t slot_count, const void *q_idx_rows, const void *k_idx,
+                                 const float *w_rows, int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t topk,
+                                 int32_t *topk_rows, void *workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
  * dsa_indexer_topk without a workspace argument, for callers that cannot
  * allocate device memory where they call it (inside an allocator or memory
  * pool callback, in a runtime whose memory is all owned by a pool, or from
@@ -418,6 +432,72 @@ dsa_status dsa_sparse_attn_prefill_flat(const dsa_cp_local_metadata *md, int32_t
                                         const int32_t *topk_idx, int32_t topk, const float *attn_sink,
                                         float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
                                         dsa_stream_t stream);
+
+/*
+ * dsa_sparse_attn_prefill_flat over a range of the view's slots and a window
+ * of the token stream: the slots [slot_begin, slot_begin + slot_count) with
+ * their index rows topk_rows [slot_count][topk]; q_rows bf16
+ * [num_q_rows][H][D] and out_rows bf16 [num_q_rows][H][Dv] hold the tokens
+ * q_row0 .. q_row0 + num_q_rows - 1 in flat order, and a slot reads and
+ * writes the row of its token (local_token_pos) there.  Every slot's token
+ * must lie in that window (otherwise DSA_ERR_DEVICE_BOUNDS and nothing is
+ * written for it); pad slots write nothing.  Same arithmetic and results as
+ * the whole-view calls.  For inputs and outputs streamed a chunk of tokens
+ * at a time.
+ */
+dsa_status dsa_sparse_attn_prefill_rows(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                        int32_t slot_begin, int32_t slot_count, const void *q_rows, int32_t q_row0,
+                                        int32_t num_q_rows, const void *kv, int32_t num_kv_rows,
+                                        const int32_t *topk_rows, int32_t topk, const float *attn_sink,
+                                        float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out_rows,
+                                        dsa_stream_t stream);
+
+/*
+ * Sliding window (SWA; [xLLM] "背景" names it beside the compressed KV, and
+ * "单层前向数据流" (4) hands the attention the original KV's geometry besides
+ * the sparse selection; the page does not say how the two combine).  Reading
+ * taken: a query at in-request position p (tokens) also attends to the
+ * ORIGINAL latent rows of its own request at positions max(0, p - W + 1) ..
+ * p, under one softmax with its selected entries (and the sink, if any); at
+ * compress ratio 1 the entries are those same rows and a row both selected
+ * and in the window counts once.  Two calls:
+ *
+ * dsa_swa_index: for every local slot, the extended index row
+ *   ext_idx [tpr][ext_stride] int32 = the slot's top-k row as dsa_indexer_topk
+ *   wrote it (its valid entries, ascending), then its window rows, then -1;
+ *   counts [tpr] int32 = the number of valid entries.  Window rows are KV row
+ *   numbers: at ratio 1 (from md) local_req_kv_base[j] + position, only those
+ *   the selection does not hold; at ratio c > 1, num_kv_rows +
+ *   ori_req_kv_base[j] + position (rows of the original KV, numbered after
+ *   the num_kv_rows compressed rows).
+ *     md               the view's metadata (ratio c) that the top-k used
+ *     ori_req_kv_base  [local batch] original KV row of each local request's
+ *                      position 0: local_req_kv_base of the same view's
+ *                      metadata built with ratio 1 (md's own at ratio 1)
+ *     topk_idx         [tpr][topk] from dsa_indexer_topk
+ *     window           W >= 1;  ext_stride >= topk + W (a multiple of 4 keeps
+ *                      every row 16-byte aligned, which the attention needs)
+ *   Integer work, exact.  Pad slots get count 0 and a row of -1.
+ *
+ * dsa_sparse_attn_prefill_swa: dsa_sparse_attn_prefill over the extended
+ *   rows: entry e < num_kv_rows reads kv row e, entry e >= num_kv_rows reads
+ *   kv_ori row e - num_kv_rows (kv_ori [num_ori_rows][D] bf16, every
+ *   request's whole sequence in request order; NULL with num_ori_rows = 0 at
+ *   ratio 1, where every entry is a kv row).  A slot's count replaces the
+ *   causal key count (a query with no visible entry still attends to its
+ *   window).  Output, layout, sink and precision as dsa_sparse_attn_prefill;
+ *   an entry outside both sources is a DSA_ERR_DEVICE_BOUNDS (zero row used).
+ */
+dsa_status dsa_swa_index(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                         const int32_t *ori_req_kv_base, int32_t num_kv_rows, const int32_t *topk_idx,
+                         int32_t topk, int32_t window, int32_t ext_stride, int32_t *ext_idx, int32_t *counts,
+                         dsa_stream_t stream);
+dsa_status dsa_sparse_attn_prefill_swa(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                       const void *q, const void *kv, int32_t num_kv_rows, const void *kv_ori,
+                                       int32_t num_ori_rows, const int32_t *ext_idx, int32_t ext_stride,
+                                       const int32_t *counts, int32_t topk, const float *attn_sink,
+                                       float softmax_scale, int32_t H, int32_t D, int32_t Dv, void *out,
+                                       dsa_stream_t stream);
 
 /*
  * FP8 latent-KV cache ([blog] "1 核心改动总结": round-robin-split lifts the

@@ -23,8 +23,10 @@ __all__ = [
     "IN_SEQ_SPLIT", "ROUND_ROBIN", "HEAD_TAIL", "DSAError", "CPLocalMetadata", "load",
     "dsa_cp_geometry", "dsa_cp_metadata_sizes", "dsa_cp_build_local_metadata", "dsa_cp_split",
     "dsa_cp_rerange", "dsa_cp_split_from_host", "dsa_cp_rerange_to_host", "dsa_cp_all_to_all_heads", "dsa_indexer_topk_workspace_size", "dsa_indexer_topk",
-    "dsa_indexer_scores", "dsa_indexer_fp8_rows", "dsa_indexer_topk_fp8", "dsa_indexer_scores_fp8",
-    "dsa_sparse_attn_prefill", "dsa_sparse_attn_prefill_headsharded", "dsa_poll_device_error",
+    "dsa_indexer_topk_rows", "dsa_indexer_scores", "dsa_indexer_fp8_rows", "dsa_indexer_topk_fp8", "dsa_indexer_scores_fp8",
+    "dsa_sparse_attn_prefill", "dsa_sparse_attn_prefill_headsharded", "dsa_sparse_attn_prefill_rows",
+    "dsa_swa_index",
+    "dsa_sparse_attn_prefill_swa", "dsa_poll_device_error",
 ]
 
 
@@ -243,6 +245,30 @@ def dsa_indexer_topk(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Tens
     return out
 
 
+def dsa_indexer_topk_rows(md: CPLocalMetadata, slot_begin: int, q_idx_rows: torch.Tensor, k_idx: torch.Tensor,
+                          w_rows: torch.Tensor, topk: int, max_kv_len: int, out: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dsa_indexer_topk for the slots [slot_begin, slot_begin + n): q_idx_rows
+    bf16 [n, HI, DI], w_rows fp32 [n, HI] -> int32 [n, topk]."""
+    _need(q_idx_rows, torch.bfloat16, "q_idx_rows")
+    _need(k_idx, torch.bfloat16, "k_idx")
+    _need(w_rows, torch.float32, "w_rows")
+    n, HI, DI = q_idx_rows.shape
+    if tuple(w_rows.shape) != (n, HI) or k_idx.shape[1] != DI:
+        raise ValueError("q_idx_rows / w_rows / k_idx shapes do not match")
+    if out is None:
+        out = torch.empty((n, topk), dtype=torch.int32, device=q_idx_rows.device)
+    _need(out, torch.int32, "out")
+    if workspace is None:
+        workspace = torch.empty(dsa_indexer_topk_workspace_size(max(n, 1), max_kv_len, topk), dtype=torch.uint8,
+                                device=q_idx_rows.device)
+    check(load().dsa_indexer_topk_rows(C.byref(md.struct), md.batch, md.tokens_per_rank, max_kv_len, int(slot_begin),
+                                       n, _ptr(q_idx_rows), _ptr(k_idx), _ptr(w_rows), k_idx.shape[0], HI, DI, topk,
+                                       _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "dsa_indexer_topk_rows")
+    return out
+
+
 def dsa_indexer_topk_noalloc(md: CPLocalMetadata, q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor,
                              topk: int, max_kv_len: int, out: torch.Tensor | None = None,
                              stream=None) -> torch.Tensor:
@@ -422,6 +448,85 @@ def dsa_sparse_attn_prefill_flat(md: CPLocalMetadata, q: torch.Tensor, kv: torch
                                               _ptr(topk_idx), topk_idx.shape[1], _ptr(attn_sink),
                                               float(softmax_scale), H, D, Dv, _ptr(out), _stream(stream)),
           "dsa_sparse_attn_prefill_flat")
+    return out
+
+
+def dsa_sparse_attn_prefill_rows(md: CPLocalMetadata, slot_begin: int, slot_count: int, q_rows: torch.Tensor,
+                                 q_row0: int, kv: torch.Tensor, topk_rows: torch.Tensor, softmax_scale: float,
+                                 Dv: int, out_rows: torch.Tensor, attn_sink: torch.Tensor | None = None,
+                                 stream=None) -> torch.Tensor:
+    """The attention of the slots [slot_begin, slot_begin + slot_count) whose
+    tokens lie in q_rows bf16 [n, H, D] (tokens q_row0 .. q_row0 + n - 1,
+    flat order); their rows of out_rows bf16 [n, H, Dv] are written."""
+    _need(q_rows, torch.bfloat16, "q_rows")
+    _need(kv, torch.bfloat16, "kv")
+    _need(topk_rows, torch.int32, "topk_rows")
+    _need(out_rows, torch.bfloat16, "out_rows")
+    if attn_sink is not None:
+        _need(attn_sink, torch.float32, "attn_sink")
+    n, H, D = q_rows.shape
+    if kv.shape[1] != D or topk_rows.shape[0] < slot_count or tuple(out_rows.shape) != (n, H, Dv):
+        raise ValueError("q_rows / kv / topk_rows / out_rows shapes do not match")
+    check(load().dsa_sparse_attn_prefill_rows(C.byref(md.struct), md.batch, md.tokens_per_rank, int(slot_begin),
+                                              int(slot_count), _ptr(q_rows), int(q_row0), n, _ptr(kv), kv.shape[0],
+                                              _ptr(topk_rows), topk_rows.shape[1], _ptr(attn_sink),
+                                              float(softmax_scale), H, D, Dv, _ptr(out_rows), _stream(stream)),
+          "dsa_sparse_attn_prefill_rows")
+    return out_rows
+
+
+def dsa_swa_index(md: CPLocalMetadata, ori_md: CPLocalMetadata, topk_idx: torch.Tensor, window: int,
+                  num_kv_rows: int, ext_idx: torch.Tensor | None = None, counts: torch.Tensor | None = None,
+                  stream=None) -> tuple:
+    """Extended index rows for the sliding window: (ext_idx int32 [tpr,
+    stride], counts int32 [tpr]), stride = topk + window rounded up to a
+    multiple of 4 (16-byte aligned rows) unless ``ext_idx`` is given.  ``ori_md``: the same view's
+    metadata built with compress ratio 1 (``md`` itself at ratio 1), whose
+    local_req_kv_base gives the original KV row of each local request."""
+    _need(topk_idx, torch.int32, "topk_idx")
+    tpr, topk = topk_idx.shape
+    if tpr != md.tokens_per_rank or ori_md.tokens_per_rank != tpr or ori_md.batch != md.batch:
+        raise ValueError("topk_idx / ori_md do not match the view")
+    stride = (topk + int(window) + 3) // 4 * 4
+    if ext_idx is None:
+        ext_idx = torch.empty((tpr, stride), dtype=torch.int32, device=topk_idx.device)
+    if counts is None:
+        counts = torch.empty(tpr, dtype=torch.int32, device=topk_idx.device)
+    _need(ext_idx, torch.int32, "ext_idx")
+    _need(counts, torch.int32, "counts")
+    if ext_idx.shape[0] != tpr or ext_idx.shape[1] < topk + int(window) or counts.numel() != tpr:
+        raise ValueError("ext_idx must be [tpr, >= topk + window] and counts [tpr]")
+    check(load().dsa_swa_index(C.byref(md.struct), md.batch, tpr, C.c_void_p(ori_md.struct.local_req_kv_base),
+                               int(num_kv_rows), _ptr(topk_idx), topk, int(window), ext_idx.shape[1], _ptr(ext_idx),
+                               _ptr(counts), _stream(stream)), "dsa_swa_index")
+    return ext_idx, counts
+
+
+def dsa_sparse_attn_prefill_swa(md: CPLocalMetadata, q: torch.Tensor, kv: torch.Tensor, kv_ori: torch.Tensor | None,
+                                ext_idx: torch.Tensor, counts: torch.Tensor, topk: int, softmax_scale: float, Dv: int,
+                                attn_sink: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                                stream=None) -> torch.Tensor:
+    """One view's attention over its extended index rows (selected entries
+    of ``kv`` plus window rows, of ``kv_ori`` when given): bf16 [tpr, H, Dv]."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv, torch.bfloat16, "kv")
+    _need(ext_idx, torch.int32, "ext_idx")
+    _need(counts, torch.int32, "counts")
+    if kv_ori is not None:
+        _need(kv_ori, torch.bfloat16, "kv_ori")
+    if attn_sink is not None:
+        _need(attn_sink, torch.float32, "attn_sink")
+    tpr, H, D = q.shape
+    if tpr != md.tokens_per_rank or kv.shape[1] != D or ext_idx.shape[0] != tpr or counts.numel() != tpr:
+        raise ValueError("q / kv / ext_idx / counts shapes do not match the view")
+    if out is None:
+        out = torch.empty((tpr, H, Dv), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    n_ori = 0 if kv_ori is None else kv_ori.shape[0]
+    check(load().dsa_sparse_attn_prefill_swa(C.byref(md.struct), md.batch, tpr, _ptr(q), _ptr(kv), kv.shape[0],
+                                             _ptr(kv_ori), n_ori, _ptr(ext_idx), ext_idx.shape[1], _ptr(counts),
+                                             int(topk), _ptr(attn_sink), float(softmax_scale), H, D, Dv, _ptr(out),
+                                             _stream(stream)), "dsa_sparse_attn_prefill_swa")
     return out
 
 

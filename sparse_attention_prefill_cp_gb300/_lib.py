@@ -48,6 +48,9 @@ SIGNATURES = {
     "dsa_indexer_topk": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                    C.c_void_p, C.c_size_t, c_stream]),
+    "dsa_indexer_topk_rows": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                        C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                                        C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t, c_stream]),
     "dsa_indexer_topk_noalloc": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                            C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                            C.c_void_p, c_stream]),
@@ -70,6 +73,16 @@ SIGNATURES = {
     "dsa_sparse_attn_prefill_flat": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_void_p, C.c_int32,
                                                C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_float,
                                                C.c_int32, C.c_int32, C.c_int32, C.c_void_p, c_stream]),
+    "dsa_sparse_attn_prefill_rows": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                               C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
+                                               C.c_int32, C.c_void_p, C.c_float, C.c_int32, C.c_int32, C.c_int32,
+                                               C.c_void_p, c_stream]),
+    "dsa_swa_index": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
+                                C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, c_stream]),
+    "dsa_sparse_attn_prefill_swa": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                              C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
+                                              C.c_int32, C.c_void_p, C.c_float, C.c_int32, C.c_int32, C.c_int32,
+                                              C.c_void_p, c_stream]),
     "dsa_kv_fp8_row_bytes": (C.c_int, [C.c_int32, C.c_int32, C.POINTER(C.c_size_t)]),
     "dsa_kv_fp8_quantize": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, c_stream]),
     "dsa_kv_fp8_dequantize": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, c_stream]),

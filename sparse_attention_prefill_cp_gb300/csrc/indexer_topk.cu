@@ -91,6 +91,7 @@ struct IdxParams {
   float *scores;       // [rows][ld]
   int64_t ld;          // score row stride (floats)
   int32_t tpr, row_begin, row_end, max_kv_len, num_kv_rows;
+  int32_t op_slot0;    // the slot of operand row 0 (q_I, w; 0 when they hold every slot of the view)
   int32_t key_chunk;   // keys per chunk: a multiple of kKeyChunk, set at launch
   int32_t min_keys;    // slots that see at most this many keys are not scored (the top-k takes them all)
   int *err;
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int slot = slot0 + i / C::HI;
     float wv = 0.f;
     if (slot < P.row_end) {
-      const int64_t r = static_cast<int64_t>(slot) * C::HI + (i % C::HI);
+      const int64_t r = static_cast<int64_t>(slot - P.op_slot0) * C::HI + (i % C::HI);
       wv = P.w[r];
       if constexpr (C::FP8) wv *= *reinterpret_cast<const float *>(P.q8 + r * C::kRowBytes + C::DI);
     }
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int c = 0; c < C::kNCh; ++c)
         for (int h = 0; h < C::kRowsQ / 256; ++h)
           tma_load_2d(smem + C::kOffQ + (c * C::kRowsQ + h * 256) * C::kCWB, &qmap, c * C::kCW,
-                      slot0 * C::HI + h * 256, q_full);
+                      (slot0 - P.op_slot0) * C::HI + h * 256, q_full);
       int issued = 0;
       BlockCursor cur;
       cursor_begin(cur);
@@ -426,7 +427,7 @@ template <int TOPK>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_metadata md, int32_t row_begin,
                                                             int32_t max_kv_len, const float *__restrict__ scores,
                                                             int64_t ld, int32_t *__restrict__ topk_idx,
-                                                            int32_t cache_words, int *err) {
+                                                            int32_t out_slot0, int32_t cache_words, int *err) {
   extern __shared__ uint32_t dyn_smem[];
   uint32_t *hist = dyn_smem;               // [kBins]
   uint32_t *cand = dyn_smem + kBins;       // [kCandMax]
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
   __shared__ int s_base, s_p, s_digit, s_krem, s_cnt, s_ncand;
   const int tid = threadIdx.x;
   const int slot = row_begin + blockIdx.x;
-  int32_t *out = topk_idx + static_cast<int64_t>(slot) * TOPK;
+  int32_t *out = topk_idx + static_cast<int64_t>(slot - out_slot0) * TOPK;
   if (tid == 0) {
     int base = 0, p = -1;
     const int g = md.local_token_pos[slot];
@@ -669,6 +670,10 @@ struct Args {
   int32_t batch, tpr, max_kv_len, num_kv_rows, HI, DI;
   const void *q_idx, *k_idx;
   const float *w;
+  // the slots [slot0, slot0 + nslots) that q_idx, w and the top-k rows hold
+  // (nslots < 0: every slot of the view, from slot 0)
+  int32_t slot0 = 0, nslots = -1;
+  int32_t count() const { return nslots < 0 ? tpr : nslots; }
 };
 
 dsa_status validate(const Args &a) {
@@ -679,6 +684,7 @@ dsa_status validate(const Args &a) {
   if (!aligned16(a.q_idx) || !aligned16(a.k_idx)) return DSA_ERR_INVALID_ARG;
   if (a.batch < 0 || a.tpr < 0 || a.max_kv_len < 1 || a.num_kv_rows < 1) return DSA_ERR_SHAPE;
   if (static_cast<int64_t>(a.tpr) * a.HI > INT32_MAX) return DSA_ERR_SHAPE;
+  if (a.nslots >= 0 && (a.slot0 < 0 || static_cast<int64_t>(a.slot0) + a.nslots > a.tpr)) return DSA_ERR_SHAPE;
   return DSA_OK;
 }
 
@@ -690,12 +696,12 @@ template <class C>
 dsa_status run_scores(const Args &a, int32_t row_begin, int32_t row_end, float *out, int64_t ld,
                       cudaStream_t stream) {
   CUtensorMap qmap, kmap;
-  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_kv_rows, &qmap, &kmap);
+  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.count(), a.num_kv_rows, &qmap, &kmap);
   if (st != DSA_OK) return st;
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
   IdxParams P{*a.md, a.w, static_cast<const uint8_t *>(a.q_idx), static_cast<const uint8_t *>(a.k_idx), out, ld,
-              a.tpr, row_begin, row_end, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, 0, err};
+              a.tpr, row_begin, row_end, a.max_kv_len, a.num_kv_rows, a.slot0, C::kKeyChunk, 0, err};
   return launch_indexer<C>(qmap, kmap, P, stream);
 }
 
@@ -707,14 +713,15 @@ constexpr int64_t kTopkSmemMax = 110 * 1024;
 
 template <int TOPK>
 dsa_status launch_topk(const dsa_cp_local_metadata &md, int32_t row_begin, int32_t rows, int32_t max_kv_len,
-                       const float *scores, int64_t ld, int32_t *topk_idx, int *err, cudaStream_t stream) {
+                       const float *scores, int64_t ld, int32_t *topk_idx, int32_t out_slot0, int *err,
+                       cudaStream_t stream) {
   const int64_t cap = kTopkSmemMax / 4 - kTopkFixedWords;
   const int32_t cache_words = static_cast<int32_t>(ld < cap ? ld : cap);
   const int smem = (kTopkFixedWords + cache_words) * 4;
   cudaError_t e = cudaFuncSetAttribute(topk_kernel<TOPK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   topk_kernel<TOPK><<<static_cast<unsigned>(rows), kTopkThreads, static_cast<size_t>(smem), stream>>>(
-      md, row_begin, max_kv_len, scores, ld, topk_idx, cache_words, err);
+      md, row_begin, max_kv_len, scores, ld, topk_idx, out_slot0, cache_words, err);
   return check_launch();
 }
 
@@ -725,19 +732,21 @@ dsa_status run_topk(const Args &a, int32_t *topk_idx, void *ws, size_t ws_bytes,
   rows_fit = rows_fit / C::kTileTok * C::kTileTok;
   if (rows_fit < C::kTileTok) return DSA_ERR_WORKSPACE;
   CUtensorMap qmap, kmap;
-  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.tpr, a.num_kv_rows, &qmap, &kmap);
+  dsa_status st = make_maps<C>(a.q_idx, a.k_idx, a.count(), a.num_kv_rows, &qmap, &kmap);
   if (st != DSA_OK) return st;
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
   float *scores = static_cast<float *>(ws);
-  for (int64_t r0 = 0; r0 < a.tpr; r0 += rows_fit) {
-    const int32_t r1 = static_cast<int32_t>(r0 + rows_fit < a.tpr ? r0 + rows_fit : a.tpr);
+  const int64_t end = static_cast<int64_t>(a.slot0) + a.count();
+  for (int64_t r0 = a.slot0; r0 < end; r0 += rows_fit) {
+    const int32_t r1 = static_cast<int32_t>(r0 + rows_fit < end ? r0 + rows_fit : end);
     IdxParams P{*a.md, a.w, static_cast<const uint8_t *>(a.q_idx), static_cast<const uint8_t *>(a.k_idx), scores,
-                ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows, C::kKeyChunk, TOPK, err};
+                ld, a.tpr, static_cast<int32_t>(r0), r1, a.max_kv_len, a.num_kv_rows, a.slot0, C::kKeyChunk, TOPK,
+                err};
     st = launch_indexer<C>(qmap, kmap, P, stream);
     if (st != DSA_OK) return st;
     st = launch_topk<TOPK>(*a.md, static_cast<int32_t>(r0), r1 - static_cast<int32_t>(r0), a.max_kv_len, scores, ld,
-                           topk_idx, err, stream);
+                           topk_idx, a.slot0, err, stream);
     if (st != DSA_OK) return st;
   }
   return DSA_OK;
@@ -771,7 +780,7 @@ dsa_status indexer_topk_entry(bool fp8, const Args &a, int32_t topk, int32_t *to
   dsa_status st = validate(a);
   if (st != DSA_OK) return st;
   if (!topk_idx || !workspace || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
-  if (a.tpr == 0) return DSA_OK;
+  if (a.count() == 0) return DSA_OK;
   const bool big = a.HI == 64 && a.DI == 128 && topk == 2048, tiny = a.HI == 4 && a.DI == 32 && topk == 64;
   if (fp8) return big ? run_topk<BigIdx8, 2048>(a, topk_idx, workspace, ws_bytes, s) : DSA_ERR_UNSUPPORTED;
   if (big) return run_topk<BigIdx, 2048>(a, topk_idx, workspace, ws_bytes, s);
@@ -809,6 +818,17 @@ extern "C" dsa_status dsa_indexer_topk(const dsa_cp_local_metadata *md, int32_t 
                                        dsa_stream_t stream) {
   Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx, k_idx, w};
   return indexer_topk_entry(false, a, topk, topk_idx, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsa_status dsa_indexer_topk_rows(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                            int32_t max_kv_len, int32_t slot_begin, int32_t slot_count,
+                                            const void *q_idx_rows, const void *k_idx, const float *w_rows,
+                                            int32_t num_kv_rows, int32_t HI, int32_t DI, int32_t topk,
+                                            int32_t *topk_rows, void *workspace, size_t ws_bytes,
+                                            dsa_stream_t stream) {
+  Args a{md, batch, tpr, max_kv_len, num_kv_rows, HI, DI, q_idx_rows, k_idx, w_rows, slot_begin, slot_count};
+  if (slot_count < 0) return DSA_ERR_SHAPE;
+  return indexer_topk_entry(false, a, topk, topk_rows, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" dsa_status dsa_indexer_topk_fp8(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,

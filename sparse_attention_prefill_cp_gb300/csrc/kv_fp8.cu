@@ -48,28 +48,41 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) kv_fp8_quantize_kernel(con
   if (row >= num_rows) return;
   const __nv_bfloat16 *src = kv + row * g.D;
   uint8_t *dst = cache + row * g.row_bytes;
-  for (int t = 0; t < g.tiles; ++t) {
-    const int width = min(kTile, g.Dv - t * kTile);
-    const int c0 = t * kTile + 4 * lane;
-    const bool mine = 4 * lane < width;
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
-    if (mine) {
-      const uint2 v = *reinterpret_cast<const uint2 *>(src + c0);
-      x[0] = __uint_as_float(v.x << 16);
-      x[1] = __uint_as_float(v.x & 0xffff0000u);
-      x[2] = __uint_as_float(v.y << 16);
-      x[3] = __uint_as_float(v.y & 0xffff0000u);
-    }
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  // tiles in groups of kGroup: every load of a group is in flight before the
+  // first reduction waits on one
+  constexpr int kGroup = 4;
+  for (int t0 = 0; t0 < g.tiles; t0 += kGroup) {
+    float x[kGroup][4];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-    if (mine) {
-      const uint32_t lo = e4m3x2_sat(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
-      const uint32_t hi = e4m3x2_sat(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
-      *reinterpret_cast<uint32_t *>(dst + c0) = lo | (hi << 16);
+    for (int u = 0; u < kGroup; ++u) {
+      const int t = t0 + u;
+      const int c0 = t * kTile + 4 * lane;
+      x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0.f;
+      if (t < g.tiles && 4 * lane < min(kTile, g.Dv - t * kTile)) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src + c0);
+        x[u][0] = __uint_as_float(v.x << 16);
+        x[u][1] = __uint_as_float(v.x & 0xffff0000u);
+        x[u][2] = __uint_as_float(v.y << 16);
+        x[u][3] = __uint_as_float(v.y & 0xffff0000u);
+      }
     }
-    if (lane == 0) *reinterpret_cast<float *>(dst + g.Dv + 4 * t) = scale;
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      const int t = t0 + u;
+      if (t >= g.tiles) break;
+      const int c0 = t * kTile + 4 * lane;
+      const bool mine = 4 * lane < min(kTile, g.Dv - t * kTile);
+      float amax = fmaxf(fmaxf(fabsf(x[u][0]), fabsf(x[u][1])), fmaxf(fabsf(x[u][2]), fabsf(x[u][3])));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+      if (mine) {
+        const uint32_t lo = e4m3x2_sat(__fdiv_rn(x[u][0], scale), __fdiv_rn(x[u][1], scale));
+        const uint32_t hi = e4m3x2_sat(__fdiv_rn(x[u][2], scale), __fdiv_rn(x[u][3], scale));
+        *reinterpret_cast<uint32_t *>(dst + c0) = lo | (hi << 16);
+      }
+      if (lane == 0) *reinterpret_cast<float *>(dst + g.Dv + 4 * t) = scale;
+    }
   }
   // rope columns: the bf16 bytes as they are; then zero padding
   const uint32_t *rope_src = reinterpret_cast<const uint32_t *>(src + g.Dv);
@@ -87,6 +100,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) kv_fp8_dequantize_kernel(c
   if (row >= num_rows) return;
   const uint8_t *src = cache + row * g.row_bytes;
   __nv_bfloat16 *dst = kv + row * g.D;
+#pragma unroll 4
   for (int t = 0; t < g.tiles; ++t) {
     const int width = min(kTile, g.Dv - t * kTile);
     const int c0 = t * kTile + 4 * lane;

@@ -121,15 +121,21 @@ using TinyAttn = AttnCfg<1, false, 48, false>;
 
 struct AttnParams {
   dsa_cp_local_metadata md;
-  const __nv_bfloat16 *kv;   // [T][D]
-  const int32_t *topk_idx;   // [tpr][topk]
+  const __nv_bfloat16 *kv;   // [num_kv_rows][D]
+  const __nv_bfloat16 *kv2;  // second row source (rows num_kv_rows ..), or nullptr
+  const int32_t *topk_idx;   // [tpr][idx_stride]
+  const int32_t *counts;     // [tpr] valid entries per row (then the rows are not causal-clamped), or nullptr
   const float *sink;         // [H] or nullptr
   __nv_bfloat16 *out;        // [tpr][H][Dv], [cp][T][hc][Dv] when hc > 0, [T][H][Dv] when flat
   float scale_log2;          // softmax_scale * log2(e)
   int32_t topk, H, D, Dv, num_kv_rows;
+  int32_t idx_stride;        // entries per index row (topk, or topk + window)
+  int32_t num_rows2;         // rows of kv2
   int32_t hc;                // heads per rank of the head-sharded output, 0 = view layout
   int32_t flat;              // 1: q and out in flat token order (rows by local_token_pos)
   int32_t q_rows;            // rows of q: tpr, or T when flat
+  int32_t slot_begin;        // slot of CTA pair 0 (and of row 0 of the index rows, and of q / out in the view layout)
+  int32_t q_row0;            // flat layout: token of q / out row 0
   int *err;
 };
 
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = C::SPLIT ? cluster_ctarank() : 0u;
   const uint32_t peer = crank ^ 1u;
-  const int slot = C::SPLIT ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int slot = P.slot_begin + (C::SPLIT ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x));
   const int main_dim0 = C::SPLIT ? static_cast<int>(crank) * C::NMAIN * 64 : 0;
   const int tail_dim0 = C::NMAIN * 64 * (C::SPLIT ? 2 : 1) + 32 * static_cast<int>(crank);
 
@@ -219,9 +225,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int pos = g - P.md.local_req_pos_base[j];
       const int ratio = max(1, P.md.scalars[DSA_MD_COMPRESS_RATIO]);
       p = pos >= 0 ? (pos + 1) / ratio : -1;  // keys (entries) the query sees
-      if (pos < 0 || base < 0 || base + p > P.num_kv_rows || (P.flat && g >= P.q_rows)) {
+      if (pos < 0 || base < 0 || base + p > P.num_kv_rows || (P.flat && (g < P.q_row0 || g - P.q_row0 >= P.q_rows))) {
         record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 44, slot);
         p = -1;
+      } else if (P.counts) {  // an extended index row: its own entry count
+        p = P.counts[slot];
+        if (p < 0 || p > P.idx_stride) {
+          record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 46, slot);
+          p = -1;
+        }
       }
     }
     misc[1] = base;
@@ -260,9 +272,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const int p = misc[2];
-  const int n_valid = p >= 0 ? min(p, P.topk) : 0;
+  const int n_valid = p >= 0 ? (P.counts ? p : min(p, P.topk)) : 0;
   const int nb = (n_valid + C::kBN - 1) / C::kBN;
-  const int qrow = P.flat ? misc[3] : slot;  // the view's row of q and of the output
+  const int qrow = P.flat ? misc[3] - P.q_row0 : slot - P.slot_begin;  // the row of q and of the output
   __nv_bfloat16 *out_row = P.out + (static_cast<int64_t>(qrow) * P.H) * P.Dv + main_dim0;
 
   if (nb == 0) {
@@ -382,7 +394,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int kGroups = 3, kRowsPerThread = C::kBN / 8;
     const int g = (warp - 10) >> 1, t = ((warp - 10) & 1) * 32 + lane;
     const int v = t & 7, r0 = t >> 3;
-    const int32_t *idx_row = P.topk_idx + static_cast<int64_t>(slot) * P.topk;
+    const int32_t *idx_row = P.topk_idx + static_cast<int64_t>(slot - P.slot_begin) * P.idx_stride;
     int rows[kRowsPerThread];
     auto fetch = [&](int j) {
 #pragma unroll
@@ -402,11 +414,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int rr = 0; rr < kRowsPerThread; ++rr) {
         const int r = r0 + 8 * rr;
         int row = rows[rr];
-        if (j * C::kBN + r < n_valid && (row < 0 || row >= P.num_kv_rows)) {
+        if (j * C::kBN + r < n_valid && (row < 0 || row >= P.num_kv_rows + P.num_rows2)) {
           record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, j * C::kBN + r);
           row = -1;
         }
-        const __nv_bfloat16 *src = P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D;
+        // rows past num_kv_rows come from the second source (window rows of the original KV)
+        const __nv_bfloat16 *src = row < P.num_kv_rows ? P.kv + static_cast<int64_t>(row < 0 ? 0 : row) * P.D
+                                                      : P.kv2 + static_cast<int64_t>(row - P.num_kv_rows) * P.D;
         const uint32_t nbytes = row < 0 ? 0u : 16u;
 #pragma unroll
         for (int i = 0; i < C::NMAIN; ++i)
@@ -724,10 +738,21 @@ dsa_status launch_attn(const void *q, int32_t tpr, const AttnParams &P, cudaStre
 
 using namespace dsa;
 
+// An extended index row (the sliding-window call): `counts` valid entries per
+// row of `stride`, rows past num_kv_rows read from kv2.
+struct ExtIndex {
+  const void *kv2;
+  int32_t num_rows2;
+  const int32_t *counts;
+  int32_t stride;
+};
+
 static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr, const void *q,
                                    const void *kv, int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
                                    const float *attn_sink, float softmax_scale, int32_t H, int32_t D, int32_t Dv,
-                                   int32_t cp_size, void *out, int32_t flat_tokens, dsa_stream_t stream) {
+                                   int32_t cp_size, void *out, int32_t flat_tokens, dsa_stream_t stream,
+                                   const ExtIndex *ext = nullptr, int32_t slot_begin = 0, int32_t slot_count = -1,
+                                   int32_t q_row0 = 0) {
   if (!md || !q || !kv || !topk_idx || !out) return DSA_ERR_INVALID_ARG;
   if (!md->scalars || !md->local_query_start_loc || !md->local_req_kv_base || !md->local_token_pos ||
       !md->local_req_pos_base)
@@ -738,8 +763,16 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
   if (cp_size < 0) return DSA_ERR_INVALID_ARG;
   if (cp_size > 0 && (H < 1 || H % cp_size != 0)) return DSA_ERR_SHAPE;
   if (flat_tokens < 0) return DSA_ERR_SHAPE;
-  if (tpr == 0) return DSA_OK;
-  if (static_cast<int64_t>(tpr) * 2 > INT32_MAX) return DSA_ERR_SHAPE;
+  if (slot_count < 0) slot_count = tpr - slot_begin;
+  if (slot_begin < 0 || slot_count < 0 || static_cast<int64_t>(slot_begin) + slot_count > tpr || q_row0 < 0)
+    return DSA_ERR_SHAPE;
+  if (ext) {
+    if (!ext->counts || (ext->num_rows2 > 0 && (!ext->kv2 || !aligned16(ext->kv2)))) return DSA_ERR_INVALID_ARG;
+    if (ext->num_rows2 < 0 || ext->stride < topk) return DSA_ERR_SHAPE;
+    if (static_cast<int64_t>(num_kv_rows) + ext->num_rows2 > INT32_MAX) return DSA_ERR_SHAPE;
+  }
+  if (slot_count == 0) return DSA_OK;
+  if (static_cast<int64_t>(slot_count) * 2 > INT32_MAX) return DSA_ERR_SHAPE;
   const bool big = H == 128 && D == 576 && Dv == 512 && topk == 2048;
   const bool tiny = H == 8 && D == 64 && Dv == 48 && topk == 64;
   if (!big && !tiny) return DSA_ERR_UNSUPPORTED;
@@ -747,7 +780,9 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
   if (!err) return DSA_ERR_CUDA;
   AttnParams P{*md,
                static_cast<const __nv_bfloat16 *>(kv),
+               ext ? static_cast<const __nv_bfloat16 *>(ext->kv2) : nullptr,
                topk_idx,
+               ext ? ext->counts : nullptr,
                attn_sink,
                static_cast<__nv_bfloat16 *>(out),
                static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634),
@@ -756,12 +791,16 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
                D,
                Dv,
                num_kv_rows,
+               ext ? ext->stride : topk,
+               ext ? ext->num_rows2 : 0,
                cp_size > 0 ? H / cp_size : 0,
                flat_tokens > 0 ? 1 : 0,
-               flat_tokens > 0 ? flat_tokens : tpr,
+               flat_tokens > 0 ? flat_tokens : slot_count,
+               slot_begin,
+               flat_tokens > 0 ? q_row0 : 0,
                err};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return big ? launch_attn<BigAttn>(q, tpr, P, s) : launch_attn<TinyAttn>(q, tpr, P, s);
+  return big ? launch_attn<BigAttn>(q, slot_count, P, s) : launch_attn<TinyAttn>(q, slot_count, P, s);
 }
 
 extern "C" dsa_status dsa_sparse_attn_prefill(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
@@ -792,4 +831,26 @@ extern "C" dsa_status dsa_sparse_attn_prefill_headsharded(const dsa_cp_local_met
   if (cp_size < 1) return DSA_ERR_INVALID_ARG;
   return sparse_attn_impl(md, batch, tpr, q, kv, num_kv_rows, topk_idx, topk, attn_sink, softmax_scale, H, D, Dv,
                           cp_size, out, 0, stream);
+}
+
+extern "C" dsa_status dsa_sparse_attn_prefill_swa(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                                  const void *q, const void *kv, int32_t num_kv_rows,
+                                                  const void *kv_ori, int32_t num_ori_rows, const int32_t *ext_idx,
+                                                  int32_t ext_stride, const int32_t *counts, int32_t topk,
+                                                  const float *attn_sink, float softmax_scale, int32_t H, int32_t D,
+                                                  int32_t Dv, void *out, dsa_stream_t stream) {
+  const ExtIndex ext{kv_ori, kv_ori ? num_ori_rows : 0, counts, ext_stride};
+  return sparse_attn_impl(md, batch, tpr, q, kv, num_kv_rows, ext_idx, topk, attn_sink, softmax_scale, H, D, Dv, 0,
+                          out, 0, stream, &ext);
+}
+
+extern "C" dsa_status dsa_sparse_attn_prefill_rows(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                                   int32_t slot_begin, int32_t slot_count, const void *q_rows,
+                                                   int32_t q_row0, int32_t num_q_rows, const void *kv,
+                                                   int32_t num_kv_rows, const int32_t *topk_rows, int32_t topk,
+                                                   const float *attn_sink, float softmax_scale, int32_t H, int32_t D,
+                                                   int32_t Dv, void *out_rows, dsa_stream_t stream) {
+  if (num_q_rows < 1 || slot_count < 0) return num_q_rows == 0 && slot_count == 0 ? DSA_OK : DSA_ERR_SHAPE;
+  return sparse_attn_impl(md, batch, tpr, q_rows, kv, num_kv_rows, topk_rows, topk, attn_sink, softmax_scale, H, D,
+                          Dv, 0, out_rows, num_q_rows, stream, nullptr, slot_begin, slot_count, q_row0);
 }

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 6
+    assert lib.dsa_abi_version() == 8
     for code, name in _lib.STATUS.items():
         assert lib.dsa_status_string(code).decode().startswith(name)
 
@@ -172,3 +172,46 @@ def test_host_row_copies_validation(lib):
         assert fn(p, 0, 10, 2, 0, 0, p, None) == 2
         assert fn(p, 16, -3, 2, 0, 0, p, None) == 2
         assert fn(p, 1 << 40, 10, 2, 1, 0, p, None) == 2
+
+
+def test_slot_range_and_window_validation(lib):
+    # slot ranges, the window's extended rows and its attention: null pointers,
+    # ranges past the view, bad windows and strides, answered on the host
+    md = _lib.LocalMetadata()
+    assert lib.dsa_cp_metadata_bind(C.c_void_p(0x10000), 1, 16, 2, C.byref(md)) == 0
+    p = C.c_void_p(0x10000)
+    f = C.c_float(0.07)
+    # indexer over a slot range: the range must lie inside the view (tpr 8)
+    assert lib.dsa_indexer_topk_rows(C.byref(md), 1, 8, 16, 4, 5, p, p, p, 16, 64, 128, 2048, p, p, 1 << 20,
+                                     None) == 2
+    assert lib.dsa_indexer_topk_rows(C.byref(md), 1, 8, 16, -1, 2, p, p, p, 16, 64, 128, 2048, p, p, 1 << 20,
+                                     None) == 2
+    assert lib.dsa_indexer_topk_rows(C.byref(md), 1, 8, 16, 0, -1, p, p, p, 16, 64, 128, 2048, p, p, 1 << 20,
+                                     None) == 2
+    assert lib.dsa_indexer_topk_rows(C.byref(md), 1, 8, 16, 2, 0, p, p, p, 16, 64, 128, 2048, p, p, 1 << 20,
+                                     None) == 0
+    assert lib.dsa_indexer_topk_rows(C.byref(md), 1, 8, 16, 2, 3, p, p, p, 16, 32, 128, 2048, p, p, 1 << 20,
+                                     None) == 3
+    # attention over a slot range and a token window
+    assert lib.dsa_sparse_attn_prefill_rows(C.byref(md), 1, 8, 6, 3, p, 0, 16, p, 16, p, 2048, None, f, 128, 576,
+                                            512, p, None) == 2
+    assert lib.dsa_sparse_attn_prefill_rows(C.byref(md), 1, 8, 0, 3, p, -1, 16, p, 16, p, 2048, None, f, 128, 576,
+                                            512, p, None) == 2
+    assert lib.dsa_sparse_attn_prefill_rows(C.byref(md), 1, 8, 0, 3, p, 0, 0, p, 16, p, 2048, None, f, 128, 576,
+                                            512, p, None) == 2
+    assert lib.dsa_sparse_attn_prefill_rows(C.byref(md), 1, 8, 0, 0, p, 0, 0, p, 16, p, 2048, None, f, 128, 576,
+                                            512, p, None) == 0
+    assert lib.dsa_sparse_attn_prefill_rows(C.byref(md), 1, 8, 0, 3, p, 0, 16, p, 16, p, 2048, None, f, 96, 576,
+                                            512, p, None) == 3
+    # the window's extended rows: null pointers, W < 1, a stride below topk + W
+    assert lib.dsa_swa_index(C.byref(md), 1, 8, None, 16, p, 2048, 128, 2176, p, p, None) == 1
+    assert lib.dsa_swa_index(C.byref(md), 1, 8, p, 16, p, 2048, 0, 2176, p, p, None) == 2
+    assert lib.dsa_swa_index(C.byref(md), 1, 8, p, 16, p, 2048, 128, 2175, p, p, None) == 2
+    assert lib.dsa_swa_index(C.byref(md), 1, 0, p, 16, p, 2048, 128, 2176, p, p, None) == 0
+    # its attention: counts missing, a second source without rows' pointer, stride below topk
+    assert lib.dsa_sparse_attn_prefill_swa(C.byref(md), 1, 8, p, p, 16, None, 0, p, 2176, None, 2048, None, f, 128,
+                                           576, 512, p, None) == 1
+    assert lib.dsa_sparse_attn_prefill_swa(C.byref(md), 1, 8, p, p, 16, C.c_void_p(0x10008), 4, p, 2176, p, 2048,
+                                           None, f, 128, 576, 512, p, None) == 1
+    assert lib.dsa_sparse_attn_prefill_swa(C.byref(md), 1, 8, p, p, 16, None, 0, p, 2000, p, 2048, None, f, 128,
+                                           576, 512, p, None) == 2

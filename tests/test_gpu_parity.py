@@ -1108,3 +1108,133 @@ def test_topk_dense_bin_long_rows_bit_exact():
         r, i = g % wl.cp_size, g // wl.cp_size
         ref = O.indexer_scores(np.ones((HI, DI)), np.ones(HI), kf[:g + 1])
         check_topk_row(idx[r, i], ref, 0, wl.topk, exact=True)
+
+
+# ------------------------------------------------------------------ sliding window (SWA)
+
+def _swa_case(wl, c, prefixes):
+    """Inputs of a sliding-window case: the queries (chunked when prefixes are
+    given), the original rows of every request's whole sequence (kv_ori), and
+    at c > 1 compressed entries drawn separately (any rows serve as entries)."""
+    x = draw_inputs(wl)
+    if prefixes is not None:
+        x, q_lens, seq = chunk_inputs(x, wl.lengths, prefixes)
+    else:
+        q_lens, seq = list(wl.lengths), list(wl.lengths)
+    kv_ori = x["kv"]
+    if c > 1:
+        R = sum(n // c for n in seq)
+        x2 = draw_inputs(wl, seed_offset=100)
+        x["kv"], x["k_idx"] = x2["kv"][:R].contiguous(), x2["k_idx"][:R].contiguous()
+    return x, kv_ori, q_lens, seq
+
+
+SWA_CASES = [(c, W, pre) for c in (1, 4) for W in (3, 4, 7) for pre in (None, (150, 20))]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("c,window,prefixes", SWA_CASES, ids=lambda v: str(v))
+def test_swa_prefill_matches_oracle(c, window, prefixes, mode):
+    # integer indexer inputs (exact top-k), float q / kv, a sink: the whole
+    # path with the window equals the oracle's prefill_swa within the
+    # attention bar, and every extended index row is the oracle's selection
+    # plus its window rows (at c = 1 a row both selected and in the window
+    # once), bit-exact
+    wl = TINY_INT.with_(name="tiny-int-swa", lengths=(200, 56), sink=True)
+    x, kv_ori, q_lens, seq = _swa_case(wl, c, None if prefixes is None else prefixes)
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    pipe = DSAPrefill(q_lens, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      prefix_lens=prefixes, compress_ratio=c, window=window)
+    out = pipe.run(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"],
+                   kv_ori=kv_ori.cuda() if c > 1 else None)
+    dsa.dsa_poll_device_error()
+    ref = O.prefill_swa(f64(x["q"]), f64(x["kv"]), f64(x["q_idx"]), f64(x["k_idx"]), f64(x["w"]), qsl_of(q_lens),
+                        seq, wl.cp_size, mode, wl.topk, wl.scale, wl.Dv, window, kv_ori=f64(kv_ori),
+                        sink=f64(x["sink"]), compress_ratio=c)
+    check_attention(out.cpu().double().numpy(), ref)
+    ori_starts = np.concatenate([[0], np.cumsum(seq)])
+    R = x["kv"].shape[0]
+    ext, cnt = pipe.ext_idx.cpu().numpy(), pipe.ext_counts.cpu().numpy()
+    q_loc = O.split(f64(x["q"]), wl.cp_size, mode)
+    qi_loc = O.split(f64(x["q_idx"]), wl.cp_size, mode)
+    w_loc = O.split(f64(x["w"]), wl.cp_size, mode)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(qsl_of(q_lens), seq, wl.cp_size, r, mode, compress_ratio=c)
+        for i in range(pipe.tpr):
+            sel, win, _ = O.view_row_swa(md, i, q_loc[r], qi_loc[r], w_loc[r], f64(x["kv"]), f64(x["k_idx"]),
+                                         wl.topk, wl.scale, wl.Dv, window, f64(kv_ori), ori_starts, None)
+            n = int(cnt[r, i])
+            if sel is None:
+                assert n == 0 and np.all(ext[r, i] == -1)
+                continue
+            want = np.union1d(sel, win) if c == 1 else np.concatenate([sel, R + win])
+            assert n == want.shape[0], (r, i)
+            assert np.array_equal(np.sort(ext[r, i, :n]), np.sort(want)), (r, i)
+            assert np.array_equal(ext[r, i, :sel.shape[0]], sel), (r, i)  # the selection first, as the top-k left it
+            assert np.all(ext[r, i, n:] == -1)
+
+
+def test_swa_full_dims_sampled_rows():
+    # DeepSeek-V3.2 shapes, window 128, compressed KV at c = 4 and a sink; the
+    # GPU's own extended rows fed to the oracle's attention, sampled slots
+    wl = FLOAT_FULL.with_(name="float-full-swa", lengths=(5000, 1500))
+    c, window = 4, 128
+    x, kv_ori, q_lens, seq = _swa_case(wl, c, None)
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    pipe = DSAPrefill(q_lens, wl.cp_size, ROUND_ROBIN, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      compress_ratio=c, window=window)
+    pipe.run(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"], kv_ori=kv_ori.cuda())
+    dsa.dsa_poll_device_error()
+    rows_all = np.concatenate([f64(x["kv"]), f64(kv_ori)])
+    sink = f64(x["sink"])
+    ext, cnt = pipe.ext_idx.cpu().numpy(), pipe.ext_counts.cpu().numpy()
+    ori_starts = np.concatenate([[0], np.cumsum(seq)])
+    R = x["kv"].shape[0]
+    rng = np.random.default_rng(9)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(qsl_of(q_lens), seq, wl.cp_size, r, ROUND_ROBIN, compress_ratio=c)
+        for i in sorted(set(rng.choice(pipe.tpr, 12, replace=False)) | {0, 1, pipe.tpr - 1}):
+            g = md["local_token_pos"][i]
+            if g < 0:
+                continue
+            j = O.request_of_slot(md, i)
+            p = g - md["local_req_pos_base"][j]
+            n = int(cnt[r, i])
+            e = ext[r, i, :n]
+            win = O.window_rows(p, ori_starts[md["local_req_id"][j]], window)
+            assert np.array_equal(e[n - win.shape[0]:], R + win)  # every window row, after the selection
+            ref = O.sparse_attention(f64(x["q"][g]), rows_all[e], wl.scale, wl.Dv, sink)
+            check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref)
+
+
+# ------------------------------------------------------------------ slot ranges (inputs streamed a chunk at a time)
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("wl", [TINY_INT.with_(name="tiny-int-sink", sink=True), FLOAT_FULL], ids=lambda w: w.name)
+def test_slot_range_calls_are_bit_identical(wl, mode):
+    # dsa_indexer_topk_rows over pieces of a view's slots (operands holding only
+    # those slots) and dsa_sparse_attn_prefill_rows over a window of tokens give
+    # exactly the rows of the whole-view calls
+    x = {k: (v.cuda() if v is not None else None) for k, v in draw_inputs(wl).items()}
+    pipe, _ = run_pipeline(wl, mode, x)
+    flat = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, fused=True)
+    ref_out = flat.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"]).clone()
+    dsa.dsa_poll_device_error()
+    tpr, T = pipe.tpr, wl.num_tokens
+    for r in range(wl.cp_size):
+        ltp = pipe.md[r].to_host()["local_token_pos"]
+        cuts = sorted({0, tpr, 1, tpr // 3, tpr // 3 + 5, (2 * tpr) // 3} & set(range(tpr + 1)))
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            rows = dsa.dsa_indexer_topk_rows(pipe.md[r], a, pipe.qi_split[r, a:b].contiguous(), x["k_idx"],
+                                             pipe.w_split[r, a:b].contiguous(), wl.topk, pipe.max_kv_len)
+            assert torch.equal(rows, pipe.topk_idx[r, a:b]), (r, a, b)
+            toks = [g for g in ltp[a:b] if g >= 0]
+            if not toks:
+                continue
+            g0, g1 = min(toks), max(toks) + 1
+            out = torch.full((g1 - g0, wl.H, wl.Dv), float("nan"), dtype=torch.bfloat16, device="cuda")
+            dsa.dsa_sparse_attn_prefill_rows(pipe.md[r], a, b - a, x["q"][g0:g1].contiguous(), g0, x["kv"], rows,
+                                             wl.scale, wl.Dv, out, x["sink"])
+            dsa.dsa_poll_device_error()
+            for g in toks:
+                assert torch.equal(out[g - g0], ref_out[g]), (r, g)
