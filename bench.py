@@ -432,6 +432,19 @@ def aux_legs(args, wl, mode, dev, pk):
         aux[name] = {"ms": ms, "bytes": fp8_bytes, "gbs": fp8_bytes / (ms / 1e3) / 1e9,
                      "frac_hbm": fp8_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
 
+    # the same two passes over 2^20 rows (1.2 GB of bf16 rows): long enough to
+    # run at HBM rate (the workload's own KV is too small for that)
+    big_kv = torch.randn((1 << 20, wl.D), device=dev).to(torch.bfloat16)
+    big_cache = dsa.dsa_kv_fp8_quantize(big_kv, wl.Dv)
+    big_rows = torch.empty_like(big_kv)
+    big_bytes = big_kv.shape[0] * (wl.D * 2 + big_cache.shape[1])
+    for name, fn in (("kv_fp8_quantize_1M_rows", lambda: dsa.dsa_kv_fp8_quantize(big_kv, wl.Dv, big_cache)),
+                     ("kv_fp8_dequantize_1M_rows", lambda: dsa.dsa_kv_fp8_dequantize(big_cache, wl.D, wl.Dv, big_rows))):
+        ms = timed(fn)
+        aux[name] = {"ms": ms, "bytes": big_bytes, "gbs": big_bytes / (ms / 1e3) / 1e9,
+                     "frac_hbm": big_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    del big_kv, big_cache, big_rows
+
     def fp8_core():
         rows = dsa.dsa_kv_fp8_dequantize(cache, wl.D, wl.Dv, kv_rows)
         pipe.views(rows, x["k_idx"], x["sink"], torch.cuda.current_stream())
@@ -455,6 +468,22 @@ def aux_legs(args, wl, mode, dev, pk):
                                                          torch.cuda.current_stream()), reps=3)
     del p8
 
+    # sliding window (W = 128 original rows under the same softmax): the a3-a5
+    # core with dsa_swa_index and the attention over the extended rows (view
+    # layout), against the roofline of its own work
+    window = 128
+    pw = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
+                    view_streams=args.view_streams, window=window)
+    pw.run(x["q"], x["kv"], x["q_idx"], x["k_idx"], x["w"], x["sink"])
+    dsa.dsa_cp_split(x["q"], wl.cp_size, mode, -1, pw.q_split)
+    ms = timed(lambda: pw.views(x["kv"], x["k_idx"], x["sink"], torch.cuda.current_stream()), reps=3)
+    cnt = pw.ext_counts.float().sum().item()  # rows the attention of every view covers
+    fi, _, by = algorithmic(wl)
+    fa_w = cnt * wl.H * (wl.D + wl.Dv) * 2
+    roof_w = max((fi + fa_w) / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+    aux[f"a3_a5_swa_w{window}"] = {"ms": ms, "flops": fi + fa_w, "roofline_frac": roof_w / (ms / 1e3)}
+    del pw
+
     def unfused_step():  # the whole step with the split of q and the rerange as passes of their own
         pipe.fused = False
         try:
@@ -471,7 +500,8 @@ def aux_legs(args, wl, mode, dev, pk):
                    "a1_metadata_ms: every view's metadata (one launch per view); "
                    "a3_a5_compressed_c*: metadata + core over compressed KV at ratio c (T / c entries); "
                    "index_fp8_quantize: q_I and k_I to FP8 index rows; a3_a5_fp8index_ms / a3_a5_bf16index_ms: "
-                   "the core with the indexer over FP8 / bf16 index rows")
+                   "the core with the indexer over FP8 / bf16 index rows; a3_a5_swa_w128: the core with a "
+                   "128-row sliding window over the original KV (extended rows, view layout)")
     dsa.dsa_poll_device_error()
     del pipe, x
     torch.cuda.empty_cache()
