@@ -429,6 +429,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// A descriptor advanced by `units` x 16 bytes: a 32-bit add on the low word
+// (the start-address field is bits 0-13 and shared addresses stay below
+// 256 KB, so nothing carries into the upper word).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t units) {
+  return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + units);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 D.
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {

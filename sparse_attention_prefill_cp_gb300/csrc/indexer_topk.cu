@@ -269,8 +269,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mbar_wait(&k_full[j % C::kStages], (j / C::kStages) & 1, P.err, 13, j);
     } else if (warp == 1 && lane == 0) {
       // ---------------- MMA issuer
-      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
-      const uint32_t k_addr = smem_u32(smem + C::kOffK);
+      // descriptors built once, advanced by constant offsets (16-byte units)
+      const uint64_t a0 = smem_desc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kLayout);
+      const uint64_t b0 = smem_desc(smem_u32(smem + C::kOffQ), 16, C::kSBO, C::kLayout);
       bool ok = mbar_wait(q_full, 0, P.err, 14);
       for (int j = 0; ok && j < nblk; ++j) {
         const int s = j % C::kStages;
@@ -279,13 +280,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int g = 0; g < 2; ++g) {
           if (!(ok = mbar_wait(&t_empty[g], (j & 1) ^ 1, P.err, 16, j))) break;
           tc_fence_after();
+          const uint64_t as = desc_add(a0, static_cast<uint32_t>(s * C::kKStageBytes) >> 4);
+          const uint64_t bg = desc_add(b0, static_cast<uint32_t>(g * 256 * C::kCWB) >> 4);
 #pragma unroll
           for (int k = 0; k < C::kKSteps; ++k) {
             const int ch = k / C::kStepsPerChunk, sub = k % C::kStepsPerChunk;
-            const uint64_t a = smem_desc(k_addr + s * C::kKStageBytes + ch * C::kBK * C::kCWB + sub * 32, 16,
-                                         C::kSBO, C::kLayout);
-            const uint64_t b = smem_desc(q_addr + ch * C::kRowsQ * C::kCWB + g * 256 * C::kCWB + sub * 32, 16,
-                                         C::kSBO, C::kLayout);
+            const uint64_t a = desc_add(as, (ch * C::kBK * C::kCWB + sub * 32) >> 4);
+            const uint64_t b = desc_add(bg, (ch * C::kRowsQ * C::kCWB + sub * 32) >> 4);
             if constexpr (C::FP8) mma_ss_f8(tmem + g * 256, a, b, C::kIdesc, k > 0 ? 1u : 0u);
             else mma_ss(tmem + g * 256, a, b, C::kIdesc, k > 0 ? 1u : 0u);
           }

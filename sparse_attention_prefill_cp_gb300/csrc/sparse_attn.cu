@@ -295,6 +295,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
       const uint32_t p_addr = smem_u32(smem + C::kOffP);
       const uint32_t recv_addr = smem_u32(smem + C::kOffRecv);
+      // Descriptors are built once here and advanced by constant offsets (in
+      // 16-byte units; every shared address is below 256 KB, so the 14-bit
+      // address field never carries): rebuilding them per MMA made issue,
+      // not the tensor pipe, the limit of the 64-wide QK steps.
+      const uint64_t qk_b0 = smem_desc(st_addr, 16, 1024, kLayoutSW128);
+      const uint64_t qk_t0 = smem_desc(st_addr + C::kStageMain, 16, 512, kLayoutSW64);
+      const uint64_t qt_a0 = smem_desc(qt_addr, 16, 512, kLayoutSW64);
+      const uint64_t pv_a0 = smem_desc(C::SPLIT ? recv_addr : p_addr, 16, 1024, kLayoutSW128);
+      const uint64_t pv_b0 = smem_desc(st_addr, C::kBN * 128, 1024, kLayoutSW128);
+      const uint32_t s_tm = tmem + C::kSCol, q_tm = tmem + C::kQCol;
       bool ok = mbar_wait(q_full, 0, P.err, 23) && mbar_wait(q_ready, 0, P.err, 23);
       tc_fence_after();
       // event-driven issue: QK(j) as soon as its rows have landed and its S
@@ -306,36 +316,32 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (qk < nb && mbar_test(&kv_full[qk % C::kStages], (qk / C::kStages) & 1) &&
             (qk < 2 || mbar_test(&s_free[qk & 1], ((qk - 2) >> 1) & 1))) {
           tc_fence_after();
-          const int b = qk & 1;
-          const uint32_t kb = st_addr + (qk % C::kStages) * C::kStageBytes;
+          const uint32_t d = s_tm + (qk & 1) * C::kBN;
+          const uint32_t so = static_cast<uint32_t>((qk % C::kStages) * C::kStageBytes) >> 4;
+          const uint64_t kb = desc_add(qk_b0, so), kt = desc_add(qk_t0, so);
 #pragma unroll
           for (int k = 0; k < C::kQKSteps; ++k) {
             if (k < C::kQKMainSteps) {
               const int i = k >> 2, sub = k & 3;
-              const uint64_t bd = smem_desc(kb + i * (C::kBN * 128) + sub * 32, 16, 1024, kLayoutSW128);
-              mma_ts(tmem + C::kSCol + b * C::kBN, tmem + C::kQCol + k * 8, bd, C::kIdescQK, k > 0 ? 1u : 0u);
+              mma_ts(d, q_tm + k * 8, desc_add(kb, (i * (C::kBN * 128) + sub * 32) >> 4), C::kIdescQK,
+                     k > 0 ? 1u : 0u);
             } else {
               const int t = k - C::kQKMainSteps;
-              const uint64_t a = smem_desc(qt_addr + t * 32, 16, 512, kLayoutSW64);
-              const uint64_t bd = smem_desc(kb + C::kStageMain + t * 32, 16, 512, kLayoutSW64);
-              mma_ss(tmem + C::kSCol + b * C::kBN, a, bd, C::kIdescQK, 1u);
+              mma_ss(d, desc_add(qt_a0, t * 2), desc_add(kt, t * 2), C::kIdescQK, 1u);
             }
           }
-          mma_commit(&s_full[b]);
+          mma_commit(&s_full[qk & 1]);
           ++qk;
           progressed = true;
         }
         if (pv < qk && mbar_test(&p_full[pv & 1], (pv >> 1) & 1)) {
           tc_fence_after();
           const int bi = pv & 1, si = pv % C::kStages;
-          const uint32_t vb = st_addr + si * C::kStageBytes;
-          const uint32_t pb = C::SPLIT ? recv_addr + bi * C::kRecvBytes : p_addr;
+          const uint64_t vb = desc_add(pv_b0, static_cast<uint32_t>(si * C::kStageBytes) >> 4);
+          const uint64_t pb = desc_add(pv_a0, C::SPLIT ? static_cast<uint32_t>(bi * C::kRecvBytes) >> 4 : 0u);
 #pragma unroll
-          for (int k = 0; k < C::kPVSteps; ++k) {
-            const uint64_t a = smem_desc(pb + k * 32, 16, 1024, kLayoutSW128);
-            const uint64_t bd = smem_desc(vb + k * 2048, C::kBN * 128, 1024, kLayoutSW128);
-            mma_ss(tmem, a, bd, C::kIdescPV, (pv > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < C::kPVSteps; ++k)
+            mma_ss(tmem, desc_add(pb, k * 2), desc_add(vb, k * 128), C::kIdescPV, (pv > 0 || k > 0) ? 1u : 0u);
           mma_commit(&pv_done[bi]);
           mma_commit(&kv_empty[si]);
           ++pv;

@@ -9,11 +9,17 @@
 //
 // swa_index_kernel (one warp per local slot) writes the slot's extended
 // index row: its selected rows as the top-k left them, then its window rows
-// (at ratio 1 only those not selected, found by binary search in the
-// ascending selection; at ratio c > 1 every window row, numbered after the
-// num_kv_rows compressed rows so that the attention reads it from the
-// original KV), then -1; and the row's entry count.  Integer work: the result
-// is exact.
+// (at ratio 1 only those not selected; at ratio c > 1 every window row,
+// numbered after the num_kv_rows compressed rows so that the attention reads
+// it from the original KV), then -1; and the row's entry count.  Integer
+// work: the result is exact.
+//
+// At ratio 1 the window rows are consecutive and the selection ascending, so
+// the selected rows inside the window form one run of the selection: a
+// 32-way search finds where it starts, and each 32-row piece of the window
+// then takes the next (at most 32) entries of the run as a bit mask of the
+// rows it holds.  Rows are copied 16 bytes at a time when the row lengths
+// and pointers allow it.
 #include "dsa_common.cuh"
 #include "internal.h"
 
@@ -30,7 +36,25 @@ struct SwaParams {
   int *err;
 };
 
-constexpr int kSwaWarps = 8;
+constexpr int kSwaWarps = 4;
+
+// first index in sel[0, n) whose entry is >= x, for an ascending sel; warp-wide
+// (every lane returns it), ceil(log32(n)) + 1 rounds of one load per lane
+__device__ __forceinline__ int warp_lower_bound(const int32_t *sel, int n, int x, int lane) {
+  int lo = 0, hi = n;
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) >> 5;
+    const int at = lo + lane * step;
+    const unsigned below = __ballot_sync(0xffffffffu, at < hi && sel[at] < x);
+    const int c = __popc(below);  // probes 0 .. c-1 lie below x
+    if (c == 0) return lo;
+    const int nlo = lo + (c - 1) * step + 1;
+    hi = min(lo + c * step, hi);
+    lo = nlo;
+  }
+  const unsigned below = __ballot_sync(0xffffffffu, lo + lane < hi && sel[lo + lane] < x);
+  return lo + __popc(below);
+}
 
 __global__ void __launch_bounds__(32 * kSwaWarps) swa_index_kernel(const SwaParams P) {
   const int lane = threadIdx.x & 31;
@@ -40,17 +64,39 @@ __global__ void __launch_bounds__(32 * kSwaWarps) swa_index_kernel(const SwaPara
   int32_t *row = P.ext + static_cast<int64_t>(slot) * P.stride;
   const int g = P.md.local_token_pos[slot];
   const int nb = P.md.scalars[DSA_MD_LOCAL_BATCH];
+  const bool vec = ((P.topk | P.stride) & 3) == 0 && ((reinterpret_cast<uintptr_t>(P.topk_idx) |
+                                                       reinterpret_cast<uintptr_t>(P.ext)) & 15) == 0;
   int n_sel = 0, n_out = 0;
   if (g >= 0 && nb > 0) {
     const int j = find_local_request(P.md.local_query_start_loc, nb, slot);
     const int ratio = max(1, P.md.scalars[DSA_MD_COMPRESS_RATIO]);
     const int pos = g - P.md.local_req_pos_base[j];
     // the selection: its valid entries come first, then -1
-    for (int k = lane; k < P.topk; k += 32) {
-      const int32_t v = sel[k];
-      row[k] = v;
-      n_sel += __popc(__ballot_sync(0xffffffffu, v >= 0));
+    int mine = 0;
+    if (vec) {  // eight 16-byte loads per lane in flight before the stores
+      const int4 *s4 = reinterpret_cast<const int4 *>(sel);
+      int4 *r4 = reinterpret_cast<int4 *>(row);
+      const int n4 = P.topk >> 2;
+      for (int k0 = lane; k0 < n4; k0 += 8 * 32) {
+        int4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (k0 + 32 * u < n4) v[u] = __ldg(s4 + k0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (k0 + 32 * u < n4) {
+            r4[k0 + 32 * u] = v[u];
+            mine += (v[u].x >= 0) + (v[u].y >= 0) + (v[u].z >= 0) + (v[u].w >= 0);
+          }
+      }
+    } else {
+      for (int k = lane; k < P.topk; k += 32) {
+        const int32_t v = sel[k];
+        row[k] = v;
+        mine += v >= 0;
+      }
     }
+    n_sel = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(mine)));
     const int lo = max(0, pos - P.window + 1), nw = pos >= 0 ? pos - lo + 1 : 0;
     const int64_t first = ratio == 1 ? static_cast<int64_t>(P.md.local_req_kv_base[j]) + lo
                                      : static_cast<int64_t>(P.num_kv_rows) + P.ori_base[j] + lo;
@@ -58,23 +104,23 @@ __global__ void __launch_bounds__(32 * kSwaWarps) swa_index_kernel(const SwaPara
       if (lane == 0) record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 61, slot);
     } else {
       n_out = n_sel;
+      // at ratio 1: entries sel[ptr ..] are the selected rows at or past the
+      // current piece of the window
+      int ptr = ratio == 1 ? warp_lower_bound(sel, n_sel, static_cast<int>(first), lane) : n_sel;
       for (int k0 = 0; k0 < nw; k0 += 32) {
-        const int k = k0 + lane;
-        const int32_t r = static_cast<int32_t>(first + k);
-        bool keep = k < nw;
-        if (keep && ratio == 1) {  // counted once: drop rows the selection holds
-          int a = 0, b = n_sel;    // first selected entry >= r
-          while (a < b) {
-            const int m = (a + b) >> 1;
-            if (sel[m] < r) a = m + 1;
-            else b = m;
-          }
-          keep = !(a < n_sel && sel[a] == r);
+        const int r0 = static_cast<int>(first) + k0;
+        unsigned held = 0;  // bit b: row r0 + b is selected
+        if (ratio == 1) {
+          const int32_t v = ptr + lane < n_sel ? sel[ptr + lane] : INT32_MAX;
+          const bool in = v >= r0 && v - r0 < 32;
+          held = __reduce_or_sync(0xffffffffu, in ? 1u << (v - r0) : 0u);
+          ptr += __popc(__ballot_sync(0xffffffffu, in));
         }
+        const bool keep = k0 + lane < nw && !((held >> lane) & 1u);
         const unsigned bal = __ballot_sync(0xffffffffu, keep);
         if (keep) {
           const int at = n_out + __popc(bal & ((1u << lane) - 1u));
-          if (at < P.stride) row[at] = r;
+          if (at < P.stride) row[at] = r0 + lane;
           else record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 62, slot);
         }
         n_out += __popc(bal);

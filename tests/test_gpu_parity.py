@@ -1207,6 +1207,48 @@ def test_swa_full_dims_sampled_rows():
             check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref)
 
 
+@pytest.mark.parametrize("mode", (IN_SEQ_SPLIT, HEAD_TAIL))
+@pytest.mark.parametrize("window", (100, 128, 2100))
+def test_swa_ratio1_extended_rows_full_dims(window, mode):
+    # ratio 1, DeepSeek-V3.2 shapes: every slot's extended row is its top-k row
+    # as the top-k left it, then the window rows the selection does not hold,
+    # ascending, then -1 (window 100 ends in a ragged piece; 2100 is longer
+    # than the selection); sampled slots' outputs equal the oracle's attention
+    # over those rows
+    wl = FLOAT_FULL.with_(name="float-full-swa1", lengths=(5000, 1500))
+    x, kv_ori, q_lens, seq = _swa_case(wl, 1, None)
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    pipe = DSAPrefill(q_lens, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale,
+                      window=window)
+    pipe.run(xd["q"], xd["kv"], xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"])
+    dsa.dsa_poll_device_error()
+    ext, cnt = pipe.ext_idx.cpu().numpy(), pipe.ext_counts.cpu().numpy()
+    sel_all = pipe.topk_idx.cpu().numpy()
+    starts = np.concatenate([[0], np.cumsum(seq)])
+    kvf, sink = f64(x["kv"]), f64(x["sink"])
+    rng = np.random.default_rng(11)
+    for r in range(wl.cp_size):
+        md = O.build_local_metadata(qsl_of(q_lens), seq, wl.cp_size, r, mode)
+        picks = set(rng.choice(pipe.tpr, 6, replace=False)) | {0, pipe.tpr - 1}
+        for i in range(pipe.tpr):
+            g = md["local_token_pos"][i]
+            row, n = ext[r, i], int(cnt[r, i])
+            if g < 0:
+                assert n == 0 and np.all(row == -1), (r, i)
+                continue
+            j = O.request_of_slot(md, i)
+            p = g - md["local_req_pos_base"][j]
+            sel = sel_all[r, i][sel_all[r, i] >= 0]
+            win = np.setdiff1d(O.window_rows(p, starts[md["local_req_id"][j]], window), sel)
+            assert n == sel.shape[0] + win.shape[0], (r, i)
+            assert np.array_equal(row[:sel.shape[0]], sel), (r, i)
+            assert np.array_equal(row[sel.shape[0]:n], win), (r, i)
+            assert np.all(row[n:] == -1), (r, i)
+            if i in picks:
+                ref = O.sparse_attention(f64(x["q"][g]), kvf[row[:n]], wl.scale, wl.Dv, sink)
+                check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref)
+
+
 # ------------------------------------------------------------------ slot ranges (inputs streamed a chunk at a time)
 
 @pytest.mark.parametrize("mode", MODES)
