@@ -409,15 +409,26 @@ __device__ __forceinline__ void scan2(int a, int b, int &ea, int &eb, int &ta, i
   eb = pb + ib - b;
 }
 
+// Exclusive prefix over the warp's lanes, and the warp total, of a per-lane
+// count in [0, 7] (three ballots; the whole warp calls it).
+__device__ __forceinline__ void warp_count_scan(int c, int lane, int &excl, int &total) {
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned b0 = __ballot_sync(0xffffffffu, c & 1), b1 = __ballot_sync(0xffffffffu, c & 2),
+                 b2 = __ballot_sync(0xffffffffu, c & 4);
+  excl = __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+  total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+}
+
 // Radix select in three digits of the order key: bits 31..21 (2048 bins),
 // 20..10 (2048) and 9..0 (1024).  The first digit is counted while the row
 // is read; when the bin that holds the topk-th largest key has at most
 // kCandMax keys, they are collected and the last two digits are counted over
 // that short list only, otherwise over the whole row (keys whose higher
-// digits match).  Then one compaction pass in ascending key order takes every
-// key above the threshold and the lowest-index keys equal to it (one block
-// scan per chunk when every equal key is taken, the common case for float
-// scores; two otherwise; 4096 keys per chunk).  The first cache_words keys of the row stay in
+// digits match; a warp appends its candidates with one shared atomic).  Then
+// one compaction pass in ascending key order takes every key above the
+// threshold and the lowest-index keys equal to it (one block scan per chunk
+// when every equal key is taken, the common case for float scores; two
+// otherwise; 4096 keys per chunk).  The first cache_words keys of the row stay in
 // shared memory after the first pass; the rest of a longer row is read again
 // from global memory by the later passes.
 constexpr int kBins = 2048;
@@ -535,13 +546,27 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const dsa_cp_local_m
   find_digit(kBins);
   uint32_t prefix = static_cast<uint32_t>(s_digit) << 21, mask = 0xFFE00000u;
   const bool use_cand = s_cnt <= kCandMax;
-  if (use_cand) {  // pass 2: the keys of that bin
-    for (int i = tid * 4; i < n; i += kTopkThreads * 4) {
+  const int lane = tid & 31, warp = tid >> 5;
+  if (use_cand) {  // pass 2: the keys of that bin (warp-uniform loop: the ballots need every lane)
+    for (int i0 = warp * 128; i0 < n; i0 += kTopkThreads * 4) {
+      const int i = i0 + lane * 4;
       uint32_t k4[4];
-      keys4_at(i, k4);
+      keys4_at(i < n ? i : n, k4);
+      bool m[4];
+      int c = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        m[k] = i + k < n && (k4[k] & mask) == prefix;
+        c += m[k];
+      }
+      int ex, tot;
+      warp_count_scan(c, lane, ex, tot);
+      int at = 0;
+      if (lane == 0 && tot > 0) at = atomicAdd(&s_ncand, tot);
+      at = __shfl_sync(0xffffffffu, at, 0) + ex;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        if (i + k < n && (k4[k] & mask) == prefix) cand[atomicAdd(&s_ncand, 1)] = k4[k];
+        if (m[k]) cand[at++] = k4[k];
     }
   }
   // digits 2 and 3 over the candidates (or the whole row)

@@ -62,40 +62,41 @@ __global__ void __launch_bounds__(32 * kSwaWarps) swa_index_kernel(const SwaPara
   if (slot >= P.tpr) return;
   const int32_t *sel = P.topk_idx + static_cast<int64_t>(slot) * P.topk;
   int32_t *row = P.ext + static_cast<int64_t>(slot) * P.stride;
-  const int g = P.md.local_token_pos[slot];
-  const int nb = P.md.scalars[DSA_MD_LOCAL_BATCH];
   const bool vec = ((P.topk | P.stride) & 3) == 0 && ((reinterpret_cast<uintptr_t>(P.topk_idx) |
                                                        reinterpret_cast<uintptr_t>(P.ext)) & 15) == 0;
+  // the selection first (it needs no metadata, so its loads overlap the
+  // lookups below): its valid entries come first, then -1
+  int mine = 0;
+  if (vec) {  // eight 16-byte loads per lane in flight before the stores
+    const int4 *s4 = reinterpret_cast<const int4 *>(sel);
+    int4 *r4 = reinterpret_cast<int4 *>(row);
+    const int n4 = P.topk >> 2;
+    for (int k0 = lane; k0 < n4; k0 += 8 * 32) {
+      int4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (k0 + 32 * u < n4) v[u] = __ldg(s4 + k0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (k0 + 32 * u < n4) {
+          r4[k0 + 32 * u] = v[u];
+          mine += (v[u].x >= 0) + (v[u].y >= 0) + (v[u].z >= 0) + (v[u].w >= 0);
+        }
+    }
+  } else {
+    for (int k = lane; k < P.topk; k += 32) {
+      const int32_t v = sel[k];
+      row[k] = v;
+      mine += v >= 0;
+    }
+  }
+  const int g = P.md.local_token_pos[slot];
+  const int nb = P.md.scalars[DSA_MD_LOCAL_BATCH];
   int n_sel = 0, n_out = 0;
   if (g >= 0 && nb > 0) {
     const int j = find_local_request(P.md.local_query_start_loc, nb, slot);
     const int ratio = max(1, P.md.scalars[DSA_MD_COMPRESS_RATIO]);
     const int pos = g - P.md.local_req_pos_base[j];
-    // the selection: its valid entries come first, then -1
-    int mine = 0;
-    if (vec) {  // eight 16-byte loads per lane in flight before the stores
-      const int4 *s4 = reinterpret_cast<const int4 *>(sel);
-      int4 *r4 = reinterpret_cast<int4 *>(row);
-      const int n4 = P.topk >> 2;
-      for (int k0 = lane; k0 < n4; k0 += 8 * 32) {
-        int4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (k0 + 32 * u < n4) v[u] = __ldg(s4 + k0 + 32 * u);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (k0 + 32 * u < n4) {
-            r4[k0 + 32 * u] = v[u];
-            mine += (v[u].x >= 0) + (v[u].y >= 0) + (v[u].z >= 0) + (v[u].w >= 0);
-          }
-      }
-    } else {
-      for (int k = lane; k < P.topk; k += 32) {
-        const int32_t v = sel[k];
-        row[k] = v;
-        mine += v >= 0;
-      }
-    }
     n_sel = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(mine)));
     const int lo = max(0, pos - P.window + 1), nw = pos >= 0 ? pos - lo + 1 : 0;
     const int64_t first = ratio == 1 ? static_cast<int64_t>(P.md.local_req_kv_base[j]) + lo
