@@ -215,6 +215,26 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int main_dim0 = C::SPLIT ? static_cast<int>(crank) * C::NMAIN * 64 : 0;
   const int tail_dim0 = C::NMAIN * 64 * (C::SPLIT ? 2 : 1) + 32 * static_cast<int>(crank);
 
+  // Q's TMA first (warp 8, lane 0): it needs only the token's row, so its
+  // latency overlaps the metadata lookup, the barrier set-up and the cluster
+  // barrier.  An out-of-range row reads the fill value (the lookup below
+  // reports it); a token that turns out to see no key drains the load before
+  // it exits.
+  bool q_issued = false;
+  if (warp == 8 && lane == 0) {
+    const int g0 = P.md.local_token_pos[slot];
+    mbar_init(q_full, 1);
+    fence_mbar_init();
+    if (g0 >= 0) {
+      const int qrow0 = P.flat ? g0 - P.q_row0 : slot - P.slot_begin;
+      tma_prefetch_desc(&qmain_map);
+      mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail);
+      for (int i = 0; i < C::NMAIN; ++i)
+        tma_load_3d(smem + C::kOffQStage + i * 16384, &qmain_map, main_dim0 + 64 * i, 0, qrow0, q_full);
+      if (C::TAIL) tma_load_3d(smem + C::kOffQTail, &qtail_map, tail_dim0, 0, qrow0, q_full);
+      q_issued = true;
+    }
+  }
   if (tid == 0) {
     int base = 0, p = -1;
     const int g = P.md.local_token_pos[slot];
@@ -240,7 +260,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     misc[2] = p;
     misc[3] = g;
     misc[4] = P.md.scalars[DSA_MD_NUM_TOKENS];
-    mbar_init(q_full, 1);
     mbar_init(q_ready, 8);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&kv_full[s], 64);
@@ -282,15 +301,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // or a token that sees no compressed entry (zero rows in every layout)
     if (warp < 4 && tid < P.H && ((misc[3] >= 0 && p == 0) || (P.hc == 0 && !P.flat)))
       zero_row(P, out_row, tid, misc[3], misc[4], main_dim0, C::DVC);
+    if (q_issued) mbar_wait(q_full, 0, P.err, 24);  // the Q load issued at the start has landed
   } else if (warp == 8) {
     if (lane == 0) {
-      // ---------------- TMA: Q (main dims to a staging tile, tail dims in place)
-      tma_prefetch_desc(&qmain_map);
-      mbar_arrive_expect_tx(q_full, C::kQMain + C::kQTail);
-      for (int i = 0; i < C::NMAIN; ++i)
-        tma_load_3d(smem + C::kOffQStage + i * 16384, &qmain_map, main_dim0 + 64 * i, 0, qrow, q_full);
-      if (C::TAIL) tma_load_3d(smem + C::kOffQTail, &qtail_map, tail_dim0, 0, qrow, q_full);
-      // ---------------- MMA issuer: QK runs two blocks ahead of PV
+      // ---------------- MMA issuer: QK runs two blocks ahead of PV (Q was
+      // loaded by TMA at the start: main dims to a staging tile, tail dims in place)
       const uint32_t st_addr = smem_u32(smem + C::kOffStage);
       const uint32_t qt_addr = smem_u32(smem + C::kOffQTail);
       const uint32_t p_addr = smem_u32(smem + C::kOffP);
