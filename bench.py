@@ -451,6 +451,18 @@ def aux_legs(args, wl, mode, dev, pk):
 
     pipe._q = x["q"]
     aux["a3_a5_fp8kv_ms"] = timed(fp8_core, reps=3)
+    # the same core with the attention reading the cache itself (its gather
+    # dequantises the selected rows; no bf16 copy of the rows)
+    pd = DSAPrefill(wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale, dev,
+                    view_streams=args.view_streams, fused=True, kv_fp8=True, kv_fp8_direct=True)
+    pd.run(x["q"], cache, x["q_idx"], x["k_idx"], x["w"], x["sink"])
+
+    def fp8_direct_core():
+        pd._q = x["q"]
+        pd.views(cache, x["k_idx"], x["sink"], torch.cuda.current_stream())
+
+    aux["a3_a5_fp8kv_direct_ms"] = timed(fp8_direct_core, reps=3)
+    del pd
     # FP8 index rows: q_I and k_I quantised (HBM passes, bytes read + written),
     # and the a3-a5 core with the indexer over them beside the same core over
     # bf16 index rows, timed the same way
@@ -496,6 +508,7 @@ def aux_legs(args, wl, mode, dev, pk):
                    "a3_a5_headsharded_ms: the core with that permutation fused into the attention stores; "
                    "kv_fp8_*: the FP8 latent-KV cache (E4M3, per-128-column scales, bf16 rope); "
                    "a3_a5_fp8kv_ms: the core over that cache (one dequantisation, then the views); "
+                   "a3_a5_fp8kv_direct_ms: the core with the attention reading the cache; "
                    "step_unfused_ms: a whole step with a2 (q) and a6 as passes of their own; "
                    "a1_metadata_ms: every view's metadata (one launch per view); "
                    "a3_a5_compressed_c*: metadata + core over compressed KV at ratio c (T / c entries); "

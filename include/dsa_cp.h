@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define DSA_CP_ABI_VERSION 8
+#define DSA_CP_ABI_VERSION 9
 
 typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 
@@ -527,6 +527,25 @@ dsa_status dsa_kv_fp8_quantize(const void *kv, int32_t num_rows, int32_t D, int3
  * an FP8 cache reads these rows. */
 dsa_status dsa_kv_fp8_dequantize(const void *cache, int32_t num_rows, int32_t D, int32_t Dv, void *kv,
                                  dsa_stream_t stream);
+
+/* dsa_sparse_attn_prefill (num_tokens = 0: the view layout) or
+ * dsa_sparse_attn_prefill_flat (num_tokens > 0: q and out in flat token
+ * order) over an FP8 latent cache instead of bf16 rows ([blog] 1 核心改动总结:
+ * round-robin-split lets CP prefill use an FP8 KV cache):
+ *   kv_cache   [num_kv_rows][row_bytes] in the layout above
+ *              (dsa_kv_fp8_quantize writes it; row_bytes from
+ *              dsa_kv_fp8_row_bytes), 16-byte aligned
+ * The gather dequantises each selected row exactly as dsa_kv_fp8_dequantize
+ * does, so the result equals dsa_sparse_attn_prefill over the dequantised
+ * rows bit for bit; the cache is read instead of bf16 rows (328 instead of
+ * 576 bytes per row and CTA).  Only H = 128, D = 576, Dv = 512, topk = 2048
+ * is compiled (DSA_ERR_UNSUPPORTED otherwise).  Same errors as
+ * dsa_sparse_attn_prefill. */
+dsa_status dsa_sparse_attn_prefill_fp8kv(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                         const void *q, int32_t num_tokens, const void *kv_cache,
+                                         int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
+                                         const float *attn_sink, float softmax_scale, int32_t H, int32_t D,
+                                         int32_t Dv, void *out, dsa_stream_t stream);
 
 /* Synchronise `stream`, then return (and clear) the first error a kernel
  * recorded on the current device since the last poll: DSA_OK, or

@@ -537,6 +537,34 @@ def dsa_kv_fp8_row_bytes(D: int, Dv: int) -> int:
     return n.value
 
 
+def dsa_sparse_attn_prefill_fp8kv(md: CPLocalMetadata, q: torch.Tensor, kv_cache: torch.Tensor,
+                                  topk_idx: torch.Tensor, softmax_scale: float, D: int, Dv: int, out: torch.Tensor,
+                                  attn_sink: torch.Tensor | None = None, flat: bool = False,
+                                  stream=None) -> torch.Tensor:
+    """The attention over an FP8 latent cache uint8 [R, row_bytes] (as
+    dsa_kv_fp8_quantize writes it), dequantised by the gather.  flat=False:
+    the view layout (q [tpr, H, D], out [tpr, H, Dv]); flat=True: q [T, H, D]
+    and out [T, H, Dv] in token order, as dsa_sparse_attn_prefill_flat."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv_cache, torch.uint8, "kv_cache")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(out, torch.bfloat16, "out")
+    if attn_sink is not None:
+        _need(attn_sink, torch.float32, "attn_sink")
+    rows, H, Dq = q.shape
+    tpr = md.tokens_per_rank
+    if Dq != D or kv_cache.dim() != 2 or kv_cache.shape[1] != dsa_kv_fp8_row_bytes(D, Dv):
+        raise ValueError("q / kv_cache do not match (D, Dv)")
+    if rows != (md.num_tokens if flat else tpr) or topk_idx.shape[0] != tpr or tuple(out.shape) != (rows, H, Dv):
+        raise ValueError("q / topk_idx / out shapes do not match the view")
+    check(load().dsa_sparse_attn_prefill_fp8kv(C.byref(md.struct), md.batch, tpr, _ptr(q), rows if flat else 0,
+                                               _ptr(kv_cache), kv_cache.shape[0], _ptr(topk_idx), topk_idx.shape[1],
+                                               _ptr(attn_sink), float(softmax_scale), H, D, Dv, _ptr(out),
+                                               _stream(stream)),
+          "dsa_sparse_attn_prefill_fp8kv")
+    return out
+
+
 def dsa_kv_fp8_quantize(kv: torch.Tensor, Dv: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """kv bf16 [R, D] -> FP8 cache uint8 [R, row_bytes]."""
     _need(kv, torch.bfloat16, "kv")

@@ -73,6 +73,9 @@ SIGNATURES = {
     "dsa_sparse_attn_prefill_flat": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_void_p, C.c_int32,
                                                C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_float,
                                                C.c_int32, C.c_int32, C.c_int32, C.c_void_p, c_stream]),
+    "dsa_sparse_attn_prefill_fp8kv": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_void_p,
+                                                C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
+                                                C.c_float, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, c_stream]),
     "dsa_sparse_attn_prefill_rows": (C.c_int, [C.POINTER(LocalMetadata), C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                                C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
                                                C.c_int32, C.c_void_p, C.c_float, C.c_int32, C.c_int32, C.c_int32,

@@ -30,12 +30,6 @@ __device__ __forceinline__ uint32_t e4m3x2_sat(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(two_codes));
-  return r;
-}
-
 struct Fp8Geom {
   int D, Dv, tiles, rope_units, row_bytes;  // rope_units: 4-byte units of the bf16 rope columns
 };

@@ -43,6 +43,13 @@
 // The tiny shapes (H = 8, D = 64, Dv = 48) run the same kernel on one CTA
 // with Q rows 8..127 zero-filled by the TMA.
 //
+// Over the FP8 latent cache ("[DeepSeek v3.2] 上下文并行详解", 1 核心改动总结:
+// round-robin-split lets CP prefill use an FP8 KV cache) the gather warps read
+// each selected row's E4M3 codes, tile scales and bf16 rope columns (328
+// bytes per row and CTA instead of 576) and dequantise into the same bf16
+// tiles, exactly as the cache's dequantiser does; the rest of the kernel is
+// unchanged, so the result equals the attention over the dequantised rows.
+//
 // Output layouts: the view's [tpr][H][Dv] (pad rows zero), or, fused into the
 // epilogue's stores, the head-sharded layout that the head/token all-to-all
 // after the attention produces (单层前向数据流 (6)): [cp][T][H / cp][Dv], rank
@@ -61,12 +68,13 @@
 namespace dsa {
 namespace {
 
-template <int NMAIN_, bool TAIL_, int DVC_, bool SPLIT_>
+template <int NMAIN_, bool TAIL_, int DVC_, bool SPLIT_, bool FP8KV_ = false>
 struct AttnCfg {
   static constexpr int NMAIN = NMAIN_;  // 64-wide latent chunks per CTA (128B swizzle)
   static constexpr bool TAIL = TAIL_;   // plus one 32-wide chunk (64B swizzle)
   static constexpr int DVC = DVC_;      // value columns per CTA
   static constexpr bool SPLIT = SPLIT_; // 2-CTA cluster per token
+  static constexpr bool FP8KV = FP8KV_; // the rows come from the FP8 latent cache (dequantised by the gather)
   static constexpr int kBN = 64;        // selected rows per block
   static constexpr int kHalf = kBN / 2; // columns per softmax warpgroup
   static constexpr int kStages = 4;
@@ -118,11 +126,14 @@ struct AttnCfg {
 
 using BigAttn = AttnCfg<4, true, 256, true>;
 using TinyAttn = AttnCfg<1, false, 48, false>;
+using BigAttnFp8 = AttnCfg<4, true, 256, true, true>;
 
 struct AttnParams {
   dsa_cp_local_metadata md;
   const __nv_bfloat16 *kv;   // [num_kv_rows][D]
   const __nv_bfloat16 *kv2;  // second row source (rows num_kv_rows ..), or nullptr
+  const uint8_t *kv8;        // FP8 latent cache [num_kv_rows][kv8_row_bytes] (FP8KV configurations)
+  int32_t kv8_row_bytes, kv8_rope;  // its row stride, and the byte offset of the bf16 rope columns
   const int32_t *topk_idx;   // [tpr][idx_stride]
   const int32_t *counts;     // [tpr] valid entries per row (then the rows are not causal-clamped), or nullptr
   const float *sink;         // [H] or nullptr
@@ -180,6 +191,78 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// The FP8 cache's share of one gather thread (2-CTA configuration): for rows
+// r0, r0 + 8, ... of the block, the codes [32 v, 32 v + 32) of the CTA's 256
+// value dims and their tile's scale are read with 16-byte loads (four rows in
+// flight), dequantised exactly as the cache's dequantiser does
+// (bf16(fp32(decode(code)) * scale)) and stored into the 128B-swizzled main
+// tiles; the rope columns are bf16 in the cache and go to the tail tile by
+// cp.async as they are.  An entry outside the rows is zero-filled (and
+// reported if it is a valid entry).
+template <class C>
+__device__ __forceinline__ void gather_fp8(const AttnParams &P, uint32_t sb, int (&rows)[C::kBN / 8], int k0,
+                                           int n_valid, int v, int r0, int crank) {
+  static_assert(C::SPLIT && C::NMAIN == 4 && C::TAIL, "the 2-CTA latent split");
+  const int cb = C::NMAIN * 64 * crank + 32 * v;   // code byte of the thread's first dim
+  const int sbyte = P.Dv + 4 * (cb / 128);          // its tile's scale
+  const int chunk = v >> 1;                         // 64-dim chunk of the stage
+#pragma unroll
+  for (int rr = 0; rr < C::kBN / 8; ++rr) {
+    const int row = rows[rr];
+    if (k0 + r0 + 8 * rr < n_valid && (row < 0 || row >= P.num_kv_rows)) {
+      record_error(P.err, DSA_ERR_DEVICE_BOUNDS, 45, k0 + r0 + 8 * rr);
+      rows[rr] = -1;
+    } else if (row >= P.num_kv_rows) {
+      rows[rr] = -1;
+    }
+  }
+#pragma unroll
+  for (int h4 = 0; h4 < C::kBN / 32; ++h4) {  // four rows at a time
+    uint4 c0[4], c1[4];
+    float scl[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int row = rows[h4 * 4 + q];
+      if (row >= 0) {
+        const uint8_t *src = P.kv8 + static_cast<int64_t>(row) * P.kv8_row_bytes;
+        c0[q] = __ldg(reinterpret_cast<const uint4 *>(src + cb));
+        c1[q] = __ldg(reinterpret_cast<const uint4 *>(src + cb + 16));
+        scl[q] = __ldg(reinterpret_cast<const float *>(src + sbyte));
+      } else {
+        c0[q] = c1[q] = make_uint4(0u, 0u, 0u, 0u);
+        scl[q] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + 8 * (h4 * 4 + q);
+      const uint32_t w8[8] = {c0[q].x, c0[q].y, c0[q].z, c0[q].w, c1[q].x, c1[q].y, c1[q].z, c1[q].w};
+      const float sc = scl[q];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // 8 codes -> one 16-byte unit of bf16
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float a, b;
+          unpack_f16x2(e4m3x2_to_f16x2((w8[2 * u + (e >> 1)] >> (16 * (e & 1))) & 0xffffu), a, b);
+          o[e] = pack_bf16x2(__fmul_rn(a, sc), __fmul_rn(b, sc));
+        }
+        const int unit = (v & 1) * 4 + u;
+        st_shared_v4(sb + chunk * (C::kBN * 128) + r * 128 + ((unit ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+  // the rope columns (bf16 in the cache): four threads per row, 16 bytes each
+  if (v < 4) {
+#pragma unroll
+    for (int rr = 0; rr < C::kBN / 8; ++rr) {
+      const int r = r0 + 8 * rr, row = rows[rr];
+      const uint8_t *src = P.kv8 + static_cast<int64_t>(row < 0 ? 0 : row) * P.kv8_row_bytes + P.kv8_rope + 64 * crank;
+      cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + 16 * v, row < 0 ? 0u : 16u);
+    }
+  }
 }
 
 template <class C>
@@ -431,6 +514,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // stages 1 and 2 held the staged Q until the softmax warps moved it to TMEM
       if ((j == 1 || j == 2) && !mbar_wait(q_ready, 0, P.err, 20, j)) break;
       const uint32_t sb = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+      if constexpr (C::FP8KV) {
+        gather_fp8<C>(P, sb, rows, j * C::kBN, n_valid, v, r0, static_cast<int>(crank));
+      } else {
 #pragma unroll
       for (int rr = 0; rr < kRowsPerThread; ++rr) {
         const int r = r0 + 8 * rr;
@@ -449,6 +535,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                       nbytes);
         if (C::TAIL && v < 4)
           cp_async_16(sb + C::kStageMain + r * 64 + ((v ^ ((r >> 1) & 3)) << 4), src + tail_dim0 + v * 8, nbytes);
+      }
       }
       cp_async_commit();
       if (j + kGroups < nb) fetch(j + kGroups);
@@ -768,12 +855,18 @@ struct ExtIndex {
   int32_t stride;
 };
 
+// The latent rows as the FP8 cache (E4M3 value columns, fp32 tile scales,
+// bf16 rope columns per row).
+struct Fp8Rows {
+  int32_t row_bytes, rope;
+};
+
 static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr, const void *q,
                                    const void *kv, int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
                                    const float *attn_sink, float softmax_scale, int32_t H, int32_t D, int32_t Dv,
                                    int32_t cp_size, void *out, int32_t flat_tokens, dsa_stream_t stream,
                                    const ExtIndex *ext = nullptr, int32_t slot_begin = 0, int32_t slot_count = -1,
-                                   int32_t q_row0 = 0) {
+                                   int32_t q_row0 = 0, const Fp8Rows *fp8 = nullptr) {
   if (!md || !q || !kv || !topk_idx || !out) return DSA_ERR_INVALID_ARG;
   if (!md->scalars || !md->local_query_start_loc || !md->local_req_kv_base || !md->local_token_pos ||
       !md->local_req_pos_base)
@@ -797,11 +890,15 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
   const bool big = H == 128 && D == 576 && Dv == 512 && topk == 2048;
   const bool tiny = H == 8 && D == 64 && Dv == 48 && topk == 64;
   if (!big && !tiny) return DSA_ERR_UNSUPPORTED;
+  if (fp8 && (!big || ext)) return DSA_ERR_UNSUPPORTED;
   int *err = device_error_word();
   if (!err) return DSA_ERR_CUDA;
   AttnParams P{*md,
-               static_cast<const __nv_bfloat16 *>(kv),
+               fp8 ? nullptr : static_cast<const __nv_bfloat16 *>(kv),
                ext ? static_cast<const __nv_bfloat16 *>(ext->kv2) : nullptr,
+               fp8 ? static_cast<const uint8_t *>(kv) : nullptr,
+               fp8 ? fp8->row_bytes : 0,
+               fp8 ? fp8->rope : 0,
                topk_idx,
                ext ? ext->counts : nullptr,
                attn_sink,
@@ -821,6 +918,7 @@ static dsa_status sparse_attn_impl(const dsa_cp_local_metadata *md, int32_t batc
                flat_tokens > 0 ? q_row0 : 0,
                err};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fp8) return launch_attn<BigAttnFp8>(q, slot_count, P, s);
   return big ? launch_attn<BigAttn>(q, slot_count, P, s) : launch_attn<TinyAttn>(q, slot_count, P, s);
 }
 
@@ -874,4 +972,17 @@ extern "C" dsa_status dsa_sparse_attn_prefill_rows(const dsa_cp_local_metadata *
   if (num_q_rows < 1 || slot_count < 0) return num_q_rows == 0 && slot_count == 0 ? DSA_OK : DSA_ERR_SHAPE;
   return sparse_attn_impl(md, batch, tpr, q_rows, kv, num_kv_rows, topk_rows, topk, attn_sink, softmax_scale, H, D,
                           Dv, 0, out_rows, num_q_rows, stream, nullptr, slot_begin, slot_count, q_row0);
+}
+
+extern "C" dsa_status dsa_sparse_attn_prefill_fp8kv(const dsa_cp_local_metadata *md, int32_t batch, int32_t tpr,
+                                                    const void *q, int32_t num_tokens, const void *kv_cache,
+                                                    int32_t num_kv_rows, const int32_t *topk_idx, int32_t topk,
+                                                    const float *attn_sink, float softmax_scale, int32_t H, int32_t D,
+                                                    int32_t Dv, void *out, dsa_stream_t stream) {
+  if (num_tokens < 0 || D < 1 || Dv < 1 || Dv > D || Dv % 8 != 0 || (D - Dv) % 8 != 0) return DSA_ERR_SHAPE;
+  // the cache row: Dv codes, one fp32 scale per 128 columns, the D - Dv rope columns as bf16, 16-byte padded
+  const int32_t tiles = (Dv + 127) / 128;
+  const Fp8Rows fp8{(Dv + 4 * tiles + 2 * (D - Dv) + 15) / 16 * 16, Dv + 4 * tiles};
+  return sparse_attn_impl(md, batch, tpr, q, kv_cache, num_kv_rows, topk_idx, topk, attn_sink, softmax_scale, H, D,
+                          Dv, 0, out, num_tokens, stream, nullptr, 0, -1, 0, &fp8);
 }

@@ -24,7 +24,8 @@ from . import (HEAD_TAIL, IN_SEQ_SPLIT, ROUND_ROBIN, CPLocalMetadata, dsa_cp_all
                dsa_cp_rerange, dsa_cp_rerange_to_host, dsa_cp_split, dsa_cp_split_from_host, dsa_indexer_topk,
                dsa_indexer_topk_fp8, dsa_indexer_topk_rows, dsa_sparse_attn_prefill_rows,
                dsa_indexer_topk_workspace_size, dsa_kv_fp8_dequantize, dsa_kv_fp8_row_bytes, dsa_sparse_attn_prefill,
-               dsa_sparse_attn_prefill_flat, dsa_sparse_attn_prefill_headsharded, dsa_sparse_attn_prefill_swa,
+               dsa_sparse_attn_prefill_flat, dsa_sparse_attn_prefill_fp8kv, dsa_sparse_attn_prefill_headsharded,
+               dsa_sparse_attn_prefill_swa,
                dsa_swa_index)
 
 
@@ -32,13 +33,16 @@ class DSAPrefill:
     def __init__(self, lengths, cp_size: int, mode: int, H: int, D: int, Dv: int, HI: int, DI: int, topk: int,
                  softmax_scale: float, device=None, workspace_bytes: int | None = None, view_streams: int = 1,
                  prefix_lens=None, kv_fp8: bool = False, fused: bool = False, compress_ratio: int = 1,
-                 index_fp8: bool = False, window: int = 0):
+                 index_fp8: bool = False, window: int = 0, kv_fp8_direct: bool = False):
         """``lengths``: query tokens per request.  ``prefix_lens`` (chunked
         prefill): KV positions per request that precede its queries; the KV
         and index-key tensors passed to ``run`` then hold every request's
         whole sequence (prefix + queries), requests in order.  ``kv_fp8``:
         the latent KV passed to ``run`` is the FP8 cache (uint8 rows of
-        dsa_kv_fp8_row_bytes), dequantised once per batch before the views.
+        dsa_kv_fp8_row_bytes), dequantised once per batch before the views;
+        with ``kv_fp8_direct`` the attention reads the cache itself and
+        dequantises in its gather (dsa_sparse_attn_prefill_fp8kv, the same
+        results; DeepSeek-V3.2 shapes, no window).
         ``fused``: ``run`` skips the split of q and the rerange of the
         outputs; each view's attention reads its queries from the full q and
         writes its rows of ``out`` in place (dsa_sparse_attn_prefill_flat),
@@ -97,8 +101,11 @@ class DSAPrefill:
         self._side = None
         self.out_hs = None  # [cp][T][H / cp][Dv], allocated on first use
         self.kv_fp8 = bool(kv_fp8)
-        self.kv_rows = (torch.empty((self.num_kv_rows, D), dtype=torch.bfloat16, device=dev) if self.kv_fp8
-                        else None)
+        self.kv_fp8_direct = bool(kv_fp8_direct)
+        if self.kv_fp8_direct and (not self.kv_fp8 or window):
+            raise ValueError("kv_fp8_direct needs kv_fp8 and no window")
+        self.kv_rows = (torch.empty((self.num_kv_rows, D), dtype=torch.bfloat16, device=dev)
+                        if self.kv_fp8 and not self.kv_fp8_direct else None)
         self.attention_events = None  # a list: (view, start, end) CUDA events of every attention launch
         self._q = None
         self.window = int(window)
@@ -142,7 +149,8 @@ class DSAPrefill:
         splits, reranges = (2, 0) if self.fused else (3, 1)
         md = self.cp_size * (2 if self.window and self.compress_ratio > 1 else 1)
         swa = self.cp_size if self.window else 0
-        return md + splits + int(self.kv_fp8) + self.cp_size * (2 * chunks + 1) + swa + reranges
+        dequant = int(self.kv_fp8 and not self.kv_fp8_direct)
+        return md + splits + dequant + self.cp_size * (2 * chunks + 1) + swa + reranges
 
     def metadata(self, stream=None):                                     # a1
         for r in range(self.cp_size):
@@ -180,6 +188,10 @@ class DSAPrefill:
             dsa_sparse_attn_prefill_swa(self.md[r], self.q_split[r], kv, self._kv_ori, self.ext_idx[r],
                                         self.ext_counts[r], self.topk, self.scale, self.Dv, sink, self.out_split[r],
                                         st)
+        elif self.kv_fp8_direct:
+            q, out = (self._q, self.out) if self.fused else (self.q_split[r], self.out_split[r])
+            dsa_sparse_attn_prefill_fp8kv(self.md[r], q, kv, self.topk_idx[r], self.scale, self.D, self.Dv, out, sink,
+                                          flat=self.fused, stream=st)
         elif self.fused:
             dsa_sparse_attn_prefill_flat(self.md[r], self._q, kv, self.topk_idx[r], self.scale, self.Dv, self.out,
                                          sink, st)
@@ -194,7 +206,7 @@ class DSAPrefill:
         """The bf16 latent rows the attention reads: ``kv`` itself, or the
         rows an FP8 cache stands for (dequantised into a buffer of this
         object)."""
-        if not self.kv_fp8:
+        if not self.kv_fp8 or self.kv_fp8_direct:
             return kv
         return dsa_kv_fp8_dequantize(kv, self.D, self.Dv, self.kv_rows, stream)
 
@@ -272,6 +284,8 @@ class DSAPrefill:
     def run_headsharded(self, q, kv, q_idx, k_idx, w, sink=None, stream=None):
         """a1, a2, then per view a3 + a4 + a5 with the attention writing the
         head-sharded layout directly; returns out_hs [cp, T, H / cp, Dv]."""
+        if self.kv_fp8_direct:
+            raise ValueError("the head-sharded attention reads bf16 rows (build without kv_fp8_direct)")
         out = self._head_sharded_buffer()
         self.metadata(stream)
         self.split(q, q_idx, w, stream)

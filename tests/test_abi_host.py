@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 8
+    assert lib.dsa_abi_version() == 9
     for code, name in _lib.STATUS.items():
         assert lib.dsa_status_string(code).decode().startswith(name)
 

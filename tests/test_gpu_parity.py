@@ -658,6 +658,60 @@ def test_prefill_over_fp8_kv_cache(wl, mode):
             check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref)
 
 
+@pytest.mark.parametrize("wl,mode,fused", [(FLOAT_FULL, ROUND_ROBIN, False), (FLOAT_FULL, IN_SEQ_SPLIT, True),
+                                            (FLOAT_FULL, HEAD_TAIL, True), (VARLEN_4, ROUND_ROBIN, True),
+                                            (LONG_8K, IN_SEQ_SPLIT, True)],
+                         ids=lambda v: v.name if isinstance(v, Workload) else str(v))
+def test_attention_reads_fp8_cache_directly(wl, mode, fused):
+    # the attention reading the FP8 cache (its gather dequantises each selected
+    # row) equals the attention over the rows dsa_kv_fp8_dequantize writes, bit
+    # for bit, in the view and the flat layouts; those rows are the oracle's
+    # (test_prefill_over_fp8_kv_cache), and sampled outputs are within the
+    # attention bar of the oracle over the oracle's dequantised rows
+    xd = draw_inputs(wl, device="cuda")
+    cache = dsa.dsa_kv_fp8_quantize(xd["kv"], wl.Dv)
+    args = (wl.lengths, wl.cp_size, mode, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale)
+    ref_pipe = DSAPrefill(*args, kv_fp8=True, fused=fused)
+    ref = ref_pipe.run(xd["q"], cache, xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"]).clone()
+    pipe = DSAPrefill(*args, kv_fp8=True, kv_fp8_direct=True, fused=fused)
+    out = pipe.run(xd["q"], cache, xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"])
+    dsa.dsa_poll_device_error()
+    assert torch.equal(pipe.topk_idx, ref_pipe.topk_idx)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    if wl is FLOAT_FULL and not fused:
+        kv_ref = O.kv_fp8_dequantize(O.kv_fp8_quantize(xd["kv"].float().cpu().numpy(), wl.Dv), wl.D, wl.Dv)
+        sink = None if xd["sink"] is None else f64(xd["sink"])
+        idx = pipe.topk_idx.cpu().numpy()
+        rng = np.random.default_rng(12)
+        for r in range(wl.cp_size):
+            md = O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
+            for i in sorted(set(rng.choice(pipe.tpr, 24, replace=False)) | {0, pipe.tpr - 1}):
+                g = md["local_token_pos"][i]
+                if g < 0:
+                    continue
+                sel = idx[r, i][idx[r, i] >= 0]
+                ref_o = O.sparse_attention(f64(xd["q"][g]), kv_ref[sel], wl.scale, wl.Dv, sink)
+                check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref_o)
+
+
+@pytest.mark.parametrize("bad_row", [-1, 10 ** 9])
+def test_fp8_cache_attention_reports_out_of_range_index(bad_row):
+    # an index past the cache rows, or -1 inside the valid entries, is a device
+    # bounds error and is not read, as on the bf16 path
+    wl = FLOAT_FULL
+    xd = draw_inputs(wl, device="cuda")
+    cache = dsa.dsa_kv_fp8_quantize(xd["kv"], wl.Dv)
+    pipe, _ = run_pipeline(wl, ROUND_ROBIN, xd)
+    bad = pipe.topk_idx[0].clone()
+    assert int(bad[5, 0]) >= 0
+    bad[5, 0] = bad_row
+    out = torch.empty_like(pipe.out_split[0])
+    dsa.dsa_sparse_attn_prefill_fp8kv(pipe.md[0], pipe.q_split[0], cache, bad, wl.scale, wl.D, wl.Dv, out)
+    with pytest.raises(dsa.DSAError) as e:
+        dsa.dsa_poll_device_error()
+    assert e.value.status == 7
+
+
 # ------------------------------------------------------------------ full-size configurations, sampled rows
 
 def _device_inputs(wl):
