@@ -1104,16 +1104,17 @@ def test_indexer_scores_cover_tiles_across_requests(mode):
 
 @pytest.mark.parametrize("mode", MODES)
 def test_topk_long_rows_bit_exact(mode):
-    # rows longer than the top-k's shared-memory key cache (22,016 keys: the
-    # rest of the row is read again from global memory), integer variant;
-    # rows at 22,015 / 22,016 / 22,017 keys, each request's last row and 48
-    # sampled slots per view must select the oracle's sets, bit-exact
+    # rows longer than the top-k's shared-memory key cache (12,800 keys for
+    # these row lengths: the rest of the row is read again from global
+    # memory), integer variant; rows at 12,799 / 12,800 / 12,801 keys, rows
+    # far past the cache, each request's last row and 48 sampled slots per
+    # view must select the oracle's sets, bit-exact
     wl = INT_FULL.with_(name="int-long-rows", lengths=(30000, 4000), cp_size=2, seed=33)
     xi = draw_index_inputs(wl, device="cuda")
     pipe = _index_views(wl, mode, xi)
     md_all = [O.build_local_metadata(wl.query_start_loc(), wl.seq_lens(), wl.cp_size, r, mode)
               for r in range(wl.cp_size)]
-    want = {22014, 22015, 22016, 29999, 33999}
+    want = {12798, 12799, 12800, 22014, 22015, 22016, 29999, 33999}
     rng = np.random.default_rng(4)
     slots = []
     for md in md_all:
@@ -1156,7 +1157,8 @@ def test_topk_dense_bin_long_rows_bit_exact():
     dsa.dsa_poll_device_error()
     idx = pipe.topk_idx.cpu().numpy()
     kf = f64(k_idx)
-    rows = sample_rows(T, 40, seed=7, must=[22014, 22015, 22016, 22017, 24000, T - 2, T - 1])
+    rows = sample_rows(T, 40, seed=7, must=[12798, 12799, 12800, 12801, 22014, 22015, 22016, 22017, 24000, T - 2,
+                                            T - 1])
     for g in rows:
         g = int(g)
         r, i = g % wl.cp_size, g // wl.cp_size
