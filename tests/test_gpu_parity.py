@@ -694,6 +694,32 @@ def test_attention_reads_fp8_cache_directly(wl, mode, fused):
                 check_attention(pipe.out_split[r, i].cpu().double().numpy(), ref_o)
 
 
+@pytest.mark.parametrize("kind", ["chunked", "compressed"])
+def test_attention_reads_fp8_cache_with_prefix_and_compressed_kv(kind):
+    # the FP8-cache attention over the other geometries (a prefix before the
+    # queries; compressed entries at c = 4): bit-identical to the attention
+    # over the dequantised rows
+    wl = FLOAT_FULL.with_(name="float-fp8-" + kind, lengths=(2200, 600))
+    x = draw_inputs(wl)
+    if kind == "chunked":
+        prefixes, c = (1500, 100), 1
+        x, q_lens, _ = chunk_inputs(x, wl.lengths, prefixes)
+    else:
+        prefixes, c = None, 4
+        q_lens = list(wl.lengths)
+        R = sum(n // c for n in wl.lengths)
+        x["kv"], x["k_idx"] = x["kv"][:R].contiguous(), x["k_idx"][:R].contiguous()
+    xd = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    cache = dsa.dsa_kv_fp8_quantize(xd["kv"], wl.Dv)
+    args = (q_lens, wl.cp_size, ROUND_ROBIN, wl.H, wl.D, wl.Dv, wl.HI, wl.DI, wl.topk, wl.scale)
+    kw = dict(prefix_lens=prefixes, compress_ratio=c, kv_fp8=True, fused=True)
+    ref = DSAPrefill(*args, **kw).run(xd["q"], cache, xd["q_idx"], xd["k_idx"], xd["w"], xd["sink"]).clone()
+    out = DSAPrefill(*args, kv_fp8_direct=True, **kw).run(xd["q"], cache, xd["q_idx"], xd["k_idx"], xd["w"],
+                                                          xd["sink"])
+    dsa.dsa_poll_device_error()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
 @pytest.mark.parametrize("bad_row", [-1, 10 ** 9])
 def test_fp8_cache_attention_reports_out_of_range_index(bad_row):
     # an index past the cache rows, or -1 inside the valid entries, is a device
