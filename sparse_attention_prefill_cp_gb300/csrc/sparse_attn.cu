@@ -608,20 +608,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     };
 
     float m_used = -__builtin_huge_valf(), l = 0.f;  // m in log2 units; l over this warpgroup's columns
-    float nxt[32];  // our partial S of the next block, carried across iterations
+    // S of block i in one register array and block i + 1 loaded into the other;
+    // the loop takes two blocks per turn with the arrays' roles swapped, so no
+    // copy of S between blocks
+    float s_a[32], s_b[32];
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[0], 0, P.err, 27, 0));
       if (ok) {
         tc_fence_after();
-        load_s(0, nxt);
-        if (C::SPLIT) stage(0, nxt);
+        load_s(0, s_a);
+        if (C::SPLIT) stage(0, s_a);
       }
     }
-    for (int i = 0; ok && i < nb; ++i) {
+    auto block = [&](int i, float (&x)[32], float (&nxt)[32]) -> bool {
       const int b = i & 1;
-      float x[C::kHalf];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) x[k] = nxt[k];
       if (i + 1 < nb) {
         // fetch (and for the pair, ship) block i+1 ahead: the peer has it by the
         // time it starts block i+1
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b1], ((i + 1) >> 1) & 1, P.err, 27, i + 1) &&
                                          (!C::SPLIT || i < 1 ||
                                           mbar_wait(&stg_free[(i + 1) & 1], ((i - 1) >> 1) & 1, P.err, 28, i + 1)));
-        if (!ok) break;
+        if (!ok) return false;
         tc_fence_after();
         load_s(i + 1, nxt);
         if (C::SPLIT) stage(i + 1, nxt);
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (C::SPLIT) {
         if (tid == 0) mbar_arrive_expect_tx(&recv_full[b], C::kRecvTx);
         ok = __all_sync(0xffffffffu, mbar_wait<true>(&recv_full[b], (i >> 1) & 1, P.err, 29, i));
-        if (!ok) break;
+        if (!ok) return false;
         const uint8_t *my_recv = recv0 + b * C::kRecvBytes + h * 128;
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       red[(b * 2 + w) * 128 + h] = fmaxf(fmax3(m3[0], m3[1], m3[2]), m3[3]);
       warp_arrive(&red_full[b], lane);
       ok = __all_sync(0xffffffffu, mbar_wait(&red_full[b], (i >> 1) & 1, P.err, 33, i));
-      if (!ok) break;
+      if (!ok) return false;
       const float mblk = fmaxf(red[(b * 2) * 128 + h], red[(b * 2 + 1) * 128 + h]);  // log2 units
       // lazy rescale: only when some row of the warp saw its max grow by more
       // than 2^8; rows whose max did not grow get alpha = 1 (exact).  Both
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (i >= 1) {
           // O holds PV(i-1): rescale this warpgroup's half of it before PV(i) accumulates
           ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, P.err, 30, i));
-          if (!ok) break;
+          if (!ok) return false;
           tc_fence_after();
           scale_o_cols(lane_base, w * (C::kOCols / 2), (w + 1) * (C::kOCols / 2), alpha);
         }
@@ -689,7 +689,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // writes P over the peer's tile of this block, which nothing else reads)
       if (!C::SPLIT && i >= 1) {
         ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, P.err, 32, i));
-        if (!ok) break;
+        if (!ok) return false;
       }
       uint32_t packed[16];
       const uint64_t nm2 = f2_pack(-m_used, -m_used);
@@ -716,6 +716,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       fence_proxy_async_smem();
       warp_arrive(&p_full[b], lane);
+      return true;
+    };
+    for (int i = 0; ok && i < nb; i += 2) {
+      ok = block(i, s_a, s_b);
+      if (ok && i + 1 < nb) ok = block(i + 1, s_b, s_a);
     }
     ok = __all_sync(0xffffffffu, ok && mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, P.err, 31, nb));
     // the two warpgroups' partial sums of the softmax denominator
