@@ -26,10 +26,10 @@
 // the exchange agent, 10-15 gather of the selected rows with 16-byte cp.async
 // straight into the 128B / 64B swizzled tiles (two warps per stage, eight
 // threads per 128-byte chunk so that loads coalesce into whole lines).  Key blocks of
-// 64 rows, 4 smem stages.  S is scaled to log2 units (softmax_scale *
-// log2 e) as it leaves TMEM, and the partial S tiles are exchanged in fp16
-// (11 significant bits; the scaled logits are far inside its range, and the
-// conversion saturates rather than overflow): the softmax threads stage their
+// 64 rows, 4 smem stages.  S leaves TMEM as raw q.k sums; the softmax scale
+// (times log2 e) is applied in the exponent's FMA.  The partial S tiles are
+// exchanged in fp16 (11 significant bits; the logits are far inside its
+// range, and the conversion saturates rather than overflow): the softmax threads stage their
 // rows locally and warp 9 ships each tile to the peer's double-buffered
 // receive tiles with one bulk copy that completes the peer's mbarrier
 // transaction count, one block ahead of the softmax that needs it.  Each CTA
@@ -593,16 +593,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       fence_proxy_async_smem();  // the bulk copy reads the tile through the async proxy
       warp_arrive(&staged[b], lane);
     };
-    // load our 32 columns of S(j) from TMEM once, scaled to log2 units; the
-    // buffer is then free for QK(j+2)
+    // load our 32 columns of S(j) from TMEM once (raw q.k units: the softmax
+    // scale is applied in the exponent); the buffer is then free for QK(j+2)
     const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
     auto load_s = [&](int j, float (&v)[32]) {
       uint32_t r[32];
       tmem_ld32(lane_base + C::kSCol + (j & 1) * C::kBN + w * C::kHalf, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < 32; k += 2)
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2), v[k], v[k + 1]);
+      for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
       tc_fence_before();
       warp_arrive(&s_free[j & 1], lane);
     };
@@ -668,7 +667,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       warp_arrive(&red_full[b], lane);
       ok = __all_sync(0xffffffffu, mbar_wait(&red_full[b], (i >> 1) & 1, P.err, 33, i));
       if (!ok) return false;
-      const float mblk = fmaxf(red[(b * 2) * 128 + h], red[(b * 2 + 1) * 128 + h]);  // log2 units
+      const float mblk = fmaxf(red[(b * 2) * 128 + h], red[(b * 2 + 1) * 128 + h]) * P.scale_log2;  // log2 units
       // lazy rescale: only when some row of the warp saw its max grow by more
       // than 2^8; rows whose max did not grow get alpha = 1 (exact).  Both
       // warpgroups see the same row maxima, so they decide alike.
@@ -697,7 +696,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
         float t0, t1;
-        f2_unpack(f2_add(f2_pack(x[k], x[k + 1]), nm2), t0, t1);
+        f2_unpack(f2_fma(f2_pack(x[k], x[k + 1]), sc2, nm2), t0, t1);
         const uint32_t pk = pack_bf16x2(ex2(t0), ex2(t1));
         packed[k >> 1] = pk;
         // the denominator sums the bf16 values that PV multiplies
