@@ -36,7 +36,7 @@
 // softmaxes its own fp32 partial plus the peer's fp16 one and normalises its
 // own O half.  P (bf16) goes to a shared-memory tile, so an S buffer is free
 // as soon as it has been read and QK runs two blocks ahead of PV; the
-// denominator sums the same bf16-rounded P that the PV product uses.  The
+// denominator sums the fp32 exponentials whose bf16 roundings PV uses.  The
 // running max is rescaled lazily: O and l change only when some row of a warp
 // sees its block max exceed the max in use by more than 2^8.
 //
@@ -697,10 +697,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int k = 0; k < 32; k += 2) {
         float t0, t1;
         f2_unpack(f2_fma(f2_pack(x[k], x[k + 1]), sc2, nm2), t0, t1);
-        const uint32_t pk = pack_bf16x2(ex2(t0), ex2(t1));
-        packed[k >> 1] = pk;
-        // the denominator sums the bf16 values that PV multiplies
-        acc[(k >> 1) & 1] = f2_add(acc[(k >> 1) & 1], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
+        const float e0 = ex2(t0), e1 = ex2(t1);
+        packed[k >> 1] = pack_bf16x2(e0, e1);
+        // the denominator sums the fp32 exponentials (PV multiplies their bf16
+        // roundings: the weights then sum to 1 within ~1e-5)
+        acc[(k >> 1) & 1] = f2_add(acc[(k >> 1) & 1], f2_pack(e0, e1));
       }
       float s0, s1, s2, s3;
       f2_unpack(acc[0], s0, s1);
