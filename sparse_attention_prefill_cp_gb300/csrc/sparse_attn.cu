@@ -405,13 +405,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t s_tm = tmem + C::kSCol, q_tm = tmem + C::kQCol;
       bool ok = mbar_wait(q_full, 0, P.err, 23) && mbar_wait(q_ready, 0, P.err, 23);
       tc_fence_after();
-      // event-driven issue: QK(j) as soon as its rows have landed and its S
-      // buffer is free, PV(i) as soon as P(i) is written; each stream in order
+      // event-driven issue: QK(j) as soon as its rows have landed, its S buffer
+      // is free and PV(j - 3) has been issued, PV(i) as soon as P(i) is
+      // written; each stream in order.  S(j) is first read when the softmax
+      // starts block j - 1, one block after P(j - 3) is written, so the gate
+      // costs QK nothing, and it keeps a QK that became ready early from
+      // holding the issuing thread (and the tensor pipe) when P(j - 3) arrives.
       int qk = 0, pv = 0;
       long long t_prog = clock64(), t_check = t_prog;
       while (ok && pv < nb) {
         bool progressed = false;
-        if (qk < nb && mbar_test(&kv_full[qk % C::kStages], (qk / C::kStages) & 1) &&
+        if (qk < nb && qk < pv + 3 && mbar_test(&kv_full[qk % C::kStages], (qk / C::kStages) & 1) &&
             (qk < 2 || mbar_test(&s_free[qk & 1], ((qk - 2) >> 1) & 1))) {
           tc_fence_after();
           const uint32_t d = s_tm + (qk & 1) * C::kBN;
