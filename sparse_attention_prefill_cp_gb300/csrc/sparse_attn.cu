@@ -22,7 +22,7 @@
 //
 // Per CTA, 16 warps: 0-7 softmax in two warpgroups (one head row = one TMEM
 // lane per thread; warpgroup w owns columns [32w, 32w + 32) of each block),
-// 8 TMA for Q and the index row then event-driven MMA issue (TMEM owner), 9
+// 8 TMA for Q then event-driven MMA issue (TMEM owner), 9
 // the exchange agent, 10-15 gather of the selected rows with 16-byte cp.async
 // straight into the 128B / 64B swizzled tiles (two warps per stage, eight
 // threads per 128-byte chunk so that loads coalesce into whole lines).  Key blocks of
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-  uint64_t *q_full = bars;                     // Q staged + tail + index row landed (TMA)
+  uint64_t *q_full = bars;                     // Q staged + tail landed (TMA)
   uint64_t *q_ready = bars + 1;                // Q main copied into TMEM, staging free (8 softmax warps)
   uint64_t *kv_full = bars + 2;                // [kStages] gathered rows landed (64 gather threads)
   uint64_t *kv_empty = kv_full + C::kStages;   // [kStages] PV done with the stage (MMA commit)
